@@ -1,0 +1,389 @@
+#!/usr/bin/env python
+"""Benchmark of the sparse MLA hot path on one GB300 (or N replicas).
+
+A step is one sparse-MLA decode of the bf16 decode batch: 64 requests x 64 heads, top-k
+2048 over contexts of 8K-32K tokens in a page_size-64 cache with shuffled pages (slot
+resolution, gather, both contractions, online softmax, epilogue and the split merge, all in
+the library's kernels). The headline is decode queries/s; gather GB/s and the roofline are
+reported beside it, and the grouped prefill (8192 new tokens, 64 heads, groups of 2) is
+measured after it as a second line item (union build + attention, TFLOP/s).
+
+Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events on the
+launching stream, with a 256 MB buffer written before every step (outside the events) so
+that L2 starts cold; barrier + synchronize on both sides; max over ranks.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl svt|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-MLA decode queries/s + gather HBM GB/s; grouped prefill TFLOP/s"
+UNIT = "queries/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the decode attention kernel,
+# keyed by the sha256 of the attention source it was measured on (stale -> null).
+TRAFFIC_BY_SOURCE = {}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["svt", "reference"], default="svt")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the grouped-prefill line item")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--decode-T", type=int, default=64, help="decode batch size (64 = the benchmark workload)")
+    ap.add_argument("--prefill-T", type=int, default=8192)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    with open(os.path.join(ROOT, "sparse_mla_attention_top_gb300", "csrc", "attention.cu"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def decode_bytes(w) -> dict:
+    live = int(np.count_nonzero(w.topk >= 0))
+    gathered = live * w.row_bytes
+    other = (w.T * w.H * 576 * 2 + w.T * w.H * 512 * 2 + w.T * w.H * 4   # q, out, lse
+             + w.T * w.K * 4 + live * 4)                                   # top-k list, page-table reads
+    flops = 2 * w.H * live * (576 + 512)
+    return {"gathered": gathered, "algorithmic": gathered + other, "flops": flops, "live": live}
+
+
+def cpu_baseline(w, budget_s: float = 15.0):
+    """The oracle as it stands, on the host cores, over a bounded sample of the queries."""
+    import oracle
+
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.decode(w.q_bits, w.kv, w.kv_dtype, w.num_pages, w.page_size, w.topk, w.scale,
+                  block_table=w.block_table, seq_lens=w.seq_lens, query_ids=[0])
+    one = max(time.perf_counter() - t0, 1e-3)
+    cores = oracle.num_threads()
+    n = int(max(1, min(w.T, budget_s / one * cores)))
+    ids = np.arange(n) % w.T
+    t0 = time.perf_counter()
+    oracle.decode(w.q_bits, w.kv, w.kv_dtype, w.num_pages, w.page_size, w.topk, w.scale,
+                  block_table=w.block_table, seq_lens=w.seq_lens, query_ids=ids)
+    dt = time.perf_counter() - t0
+    return {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} of the {w.T} queries of the bf16 decode batch, all {w.H} heads, fp64, OpenMP over queries",
+            "seconds": round(dt, 3)}
+
+
+def run_reference(args):
+    from sparse_mla_attention_top_gb300 import workloads as W
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1 and rank != 0:
+        return
+    w = W.decode_bf16_batch(args.decode_T)
+    for _ in range(args.warmup):
+        cpu_baseline(w, budget_s=2.0)
+    vals = [cpu_baseline(w, budget_s=8.0) for _ in range(args.steps)]
+    value = statistics.median(v["value"] for v in vals)
+    cb = dict(vals[0])
+    cb["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * w.T / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "top_k": w.K, "page_size": w.page_size},
+            "cpu_baseline": cb, "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                                        "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def time_steps(step, steps, flush, stream):
+    import torch
+
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for s, e in evs:
+        flush.zero_()
+        s.record(stream)
+        step()
+        e.record(stream)
+    torch.cuda.synchronize()
+    return [s.elapsed_time(e) for s, e in evs]
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+
+    import sparse_mla_attention_top_gb300 as S
+    from sparse_mla_attention_top_gb300 import build as B
+    from sparse_mla_attention_top_gb300 import workloads as W
+
+    world, rank, local = dist_setup(args)
+    if rank == 0:
+        B.build()
+    barrier(world)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
+
+    # ---- decode batch, resident in HBM
+    w = W.decode_bf16_batch(args.decode_T)
+    kv = S.KVCache(torch.from_numpy(w.kv).to(dev), w.num_pages, w.page_size, w.kv_dtype)
+    q = torch.from_numpy(w.q_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+    topk = torch.from_numpy(w.topk).to(dev)
+    bt = torch.from_numpy(w.block_table).to(dev)
+    seq = torch.from_numpy(w.seq_lens).to(dev)
+    out = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+    ws = S.Workspace(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    launches_per_step = 2 if S.svt.lib().svt_sparse_mla_decode_workspace_size(w.T, w.H, w.K, 0) > 256 else 1
+
+    def step():
+        S.sparse_mla_decode(q, kv, topk, w.scale, block_table=bt, seq_lens=seq, out=out, lse=lse, ws=ws)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert ws.read_status() == 0, "device status flagged an error during warm-up"
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    times = time_steps(step, args.steps, flush, stream)
+    barrier(world)
+    clk = clocks.stop()
+    ms = max_over_ranks(statistics.mean(times), world)
+    ms_med = max_over_ranks(statistics.median(times), world)
+    nb = decode_bytes(w)
+    value = w.T * world / (ms / 1000.0)
+    achieved = nb["algorithmic"] / (ms / 1000.0) / 1e9
+    th = source_hash()
+
+    # ---- end to end: host buffers in, results out, through the public API
+    e2e = None
+    if not args.no_e2e:
+        q_h = torch.from_numpy(w.q_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
+        topk_h = torch.from_numpy(w.topk).pin_memory()
+        out_h = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16).pin_memory()
+        lse_h = torch.empty((w.T, w.H), dtype=torch.float32).pin_memory()
+        q_d, topk_d = torch.empty_like(q), torch.empty_like(topk)
+
+        def e2e_step():
+            q_d.copy_(q_h, non_blocking=True)
+            topk_d.copy_(topk_h, non_blocking=True)
+            o, l = S.sparse_mla_decode(q_d, kv, topk_d, w.scale, block_table=bt, seq_lens=seq, out=out, lse=lse,
+                                       ws=ws)
+            out_h.copy_(o, non_blocking=True)
+            lse_h.copy_(l, non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        et = time_steps(e2e_step, args.steps, flush, stream)
+        barrier(world)
+        ems = max_over_ranks(statistics.mean(et), world)
+        e2e = {"value": w.T * world / (ems / 1000.0), "unit": UNIT, "ms_per_step": ems,
+               "h2d_bytes_per_step": q_h.numel() * 2 + topk_h.numel() * 4,
+               "d2h_bytes_per_step": out_h.numel() * 2 + lse_h.numel() * 4}
+
+    # ---- grouped prefill line item (union + attention)
+    prefill = None
+    if not args.no_prefill:
+        pw = W.grouped_prefill(args.prefill_T)
+        pkv = S.KVCache(torch.from_numpy(pw.kv).to(dev), pw.num_pages, pw.page_size, pw.kv_dtype)
+        pq = torch.from_numpy(pw.q_bits.view(np.int16)).to(dev).view(torch.bfloat16)
+        ptopk = torch.from_numpy(pw.topk).to(dev)
+        pbt = torch.from_numpy(pw.block_table).to(dev)
+        pseq = torch.from_numpy(pw.seq_lens).to(dev)
+        preq = torch.from_numpy(pw.req_of_token).to(dev)
+        slots = torch.empty_like(ptopk)
+        groups = (pw.T + pw.G - 1) // pw.G
+        enc = torch.empty((groups, pw.G * pw.K), dtype=torch.int32, device=dev)
+        lens = torch.empty((groups,), dtype=torch.int32, device=dev)
+        pout = torch.empty((pw.T, pw.H, 512), dtype=torch.bfloat16, device=dev)
+        plse = torch.empty((pw.T, pw.H), dtype=torch.float32, device=dev)
+
+        def union_step():
+            S.resolve_topk_slots(ptopk, block_table=pbt, seq_lens=pseq, req_of_token=preq, page_size=pw.page_size,
+                                 num_pages=pw.num_pages, out=slots, ws=ws)
+            S.build_group_union(slots, pw.G, pw.num_slots, enc=enc, lens=lens, ws=ws)
+
+        def attn_step():
+            S.sparse_mla_prefill_grouped(pq, pw.G, pkv, enc, lens, pw.K, pw.scale, out=pout, lse=plse, ws=ws)
+
+        for _ in range(max(3, args.warmup)):
+            union_step()
+            attn_step()
+        torch.cuda.synchronize()
+        assert ws.read_status() == 0
+        psteps = max(3, args.steps // 2)
+        ut = time_steps(union_step, psteps, flush, stream)
+        at = time_steps(attn_step, psteps, flush, stream)
+        lens_h = lens.cpu().numpy().astype(np.int64)
+        live = np.count_nonzero(pw.topk >= 0, axis=1)
+        executed = float(2 * 128 * lens_h.sum() * (576 + 512))
+        useful = float(2 * pw.H * live.sum() * (576 + 512))
+        a_ms, u_ms = statistics.mean(at), statistics.mean(ut)
+        prefill = {"workload": pw.name, "union_ms": round(u_ms, 4), "attention_ms": round(a_ms, 4),
+                   "step_ms": round(u_ms + a_ms, 4),
+                   "tflops_executed": executed / (a_ms / 1e3) / 1e12,
+                   "tflops_useful": useful / (a_ms / 1e3) / 1e12,
+                   "tflops_step_useful": useful / ((a_ms + u_ms) / 1e3) / 1e12,
+                   "union_lists": float(lens_h.mean() / live.mean()),
+                   "frac_of_bf16_peak": executed / (a_ms / 1e3) / 1e12 / bf16_peak,
+                   "peak_tflops": bf16_peak, "peak_source": peak_src}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(w)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_median": ms_med, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "top_k": w.K, "page_size": w.page_size,
+                       "kv_dtype": "bf16", "contexts": "uniform 8192..32768", "l2": "256 MB flush before each step",
+                       "parallelism": f"replicas x{world}"},
+            "gather_gbs": nb["gathered"] / (ms / 1000.0) / 1e9,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": TRAFFIC_BY_SOURCE.get(th),
+                         "kernel": "decode call: attention_kernel + streamk_merge_kernel",
+                         "algorithmic_bytes": nb["algorithmic"], "peak_source": peak_src, "source_hash": th},
+            "clocks": clk, "gpu_launches": launches_per_step * args.steps, "e2e": e2e, "cpu_baseline": cpu,
+            "prefill": prefill,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * svt.h -- sparse MLA attention over a paged latent KV cache, for one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libsvt.so. Plain pointers and sizes only; no framework types.
+ *
+ * Common rules for every entry point below
+ * ----------------------------------------
+ *  - Every array argument is a DEVICE pointer owned by the caller (cudaMalloc, a PyTorch
+ *    tensor, ...). The library never allocates device memory, never frees what it is given
+ *    and never synchronises the stream (except svt_read_status, whose job is to read back).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream)
+ *    and enqueues a fixed set of kernels whose grids depend only on the scalar arguments and
+ *    the device, so a call can be captured in a CUDA graph.
+ *  - Arguments are checked on the host before anything is enqueued. A failed check returns a
+ *    non-zero svt_status, enqueues nothing, and svt_last_error_string() says why.
+ *  - Faults found on the device (an index outside the request or the cache, a wait that ran
+ *    out of time) never trap: the offending entry is treated as dead (never read), and a bit
+ *    is ORed into the status word that lives in the first 256 bytes of the caller's
+ *    workspace. Read and clear it with svt_read_status().
+ *  - Every workspace must be at least the size its query returns and 256-byte aligned;
+ *    zero its first 256 bytes once before first use (svt_workspace_init does that).
+ *  - Arrays are contiguous, row-major, in the layouts stated per argument. Every cache row
+ *    and every q row must start on a 16-byte boundary.
+ *
+ * Notation: T queries, H heads per query, K top-k width, 576 = 512 latent + 64 rope
+ * columns per cache row (K of attention is the whole row, V its first 512 columns), G
+ * queries per prefill group, P page size.
+ */
+#ifndef SVT_H_
+#define SVT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SVT_API __attribute__((visibility("default")))
+#else
+#define SVT_API
+#endif
+
+typedef struct CUstream_st* svt_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  SVT_OK = 0,
+  SVT_ERR_INVALID_ARG = 1,  /* null pointer, negative size, misaligned pointer, bad stride   */
+  SVT_ERR_UNSUPPORTED = 2,  /* H*G != 128, G not in {2,4,8}, cache of 2^24-1 or more rows for
+                               the union path, H > 128, K or G*K beyond the kernel limits    */
+  SVT_ERR_WORKSPACE = 3,    /* workspace smaller than the size query asks for              */
+  SVT_ERR_CUDA = 4          /* a CUDA runtime call failed (launch, attribute, copy)        */
+} svt_status;
+
+/* Bits of the device status word (ORed by kernels, read by svt_read_status). */
+#define SVT_DEV_ERR_INDEX_RANGE 0x1 /* a live index pointed outside its request or the cache  */
+#define SVT_DEV_ERR_TIMEOUT 0x2     /* a pipeline wait gave up; that call's outputs are junk  */
+
+typedef enum { SVT_KV_BF16 = 0, SVT_KV_FP8_E4M3 = 1 } svt_kv_dtype;
+
+/*
+ * The paged latent cache: logically [num_pages, page_size, row], one row per token slot,
+ * slot = page * page_size + offset. Row layouts (little-endian):
+ *   SVT_KV_BF16     : 576 bf16 (1152 bytes): 512 latent then 64 rope.
+ *   SVT_KV_FP8_E4M3 : 512 e4m3 latent codes | 4 fp32 scales (channels 0-127, 128-255,
+ *                     256-383, 384-511) | 64 bf16 rope = 656 bytes. The latent value of
+ *                     channel d is e4m3(d) * scale[d / 128].
+ * row_stride_bytes = 0 means packed (1152 or 656); otherwise it must be >= that and a
+ * multiple of 16. The bf16 layout is the pages' (vLLM PR #63104, bench script: 512 + 64
+ * columns viewed as (-1, 64, 576)); the pages name an e4m3 cache ("The Assertion That
+ * Changed Everything", --kv-cache-dtype fp8_e4m3) without a byte layout, and the one above
+ * is this library's choice.
+ */
+typedef struct {
+  const void* data;
+  int64_t num_pages;
+  int32_t page_size;
+  int32_t row_stride_bytes;
+  svt_kv_dtype dtype;
+} svt_kv_cache;
+
+/* Human-readable reason for the last non-OK status returned on this thread. */
+SVT_API const char* svt_last_error_string(void);
+
+/* Zeroes the 256-byte status header of a workspace (asynchronous, on `stream`). */
+SVT_API svt_status svt_workspace_init(void* ws, size_t ws_bytes, svt_stream_t stream);
+
+/* Copies the device status word to *host_out, clears it, and waits for the stream.
+ * Returns SVT_ERR_CUDA if the copy or the synchronisation fails. */
+SVT_API svt_status svt_read_status(void* ws, svt_stream_t stream, int32_t* host_out);
+
+/*
+ * Slot resolution ("The Virtual Block Table: Reusing Triton MLA for Sparse Attention on
+ * Blackwell GPUs", The Investigation: slot = table[req, pos / P] * P + pos % P; Assumptions
+ * and Reasoning, assumption 1: with P = 1 this is table[req, pos]).
+ *   topk_pos     [T, K] int32 token positions inside each query's request, -1 = none.
+ *   topk_len     [T] int32 live entries per query, or NULL for K. Entries j >= len are dead.
+ *   req_of_token [T] int32 request of each query, or NULL for the identity.
+ *   block_table  [num_reqs, max_blocks] int32 physical page ids, or NULL: then topk_pos
+ *                already holds slots and is only range-checked against num_pages*page_size.
+ *                A request id outside [0, num_reqs) makes all of its query's entries dead
+ *                and sets SVT_DEV_ERR_INDEX_RANGE.
+ *   seq_lens     [num_reqs] int32 tokens per request, or NULL to skip that check.
+ *   slots_out    [T, K] int32: the slot, or -1 for a dead entry. A live entry that is past
+ *                its request, past max_blocks, or on a page id outside [0, num_pages) gives
+ *                -1 and sets SVT_DEV_ERR_INDEX_RANGE.
+ * Requires num_pages * page_size < 2^31. Workspace: svt_resolve_workspace_size().
+ */
+SVT_API size_t svt_resolve_workspace_size(void);
+SVT_API svt_status svt_resolve_topk_slots(const int32_t* topk_pos, int32_t T, int32_t K, const int32_t* topk_len,
+                                  const int32_t* req_of_token, const int32_t* block_table, int32_t num_reqs,
+                                  int32_t max_blocks, const int32_t* seq_lens, int32_t page_size, int64_t num_pages,
+                                  int32_t* slots_out, void* ws, size_t ws_bytes, svt_stream_t stream);
+
+/*
+ * Sparse MLA decode: one query per request, all H heads share the one latent KV row of each
+ * selected token (MQA), out = softmax(scale * q . K^T) . V with K = row[0:576] and
+ * V = row[0:512] ("The Virtual Block Table", The Breakthrough: the resolved top-k list is
+ * read as a page_size-1 block table and the live count as the sequence length; vLLM PR
+ * #63104, bench script: out [.., 512] and the LSE).
+ *   q_bf16   [T, H, 576] bf16 (latent part first, then rope), H in 1..128.
+ *   kv       the cache (either dtype). block_table/num_reqs/max_blocks/req_of_token/seq_lens/
+ *            topk/topk_len are as for svt_resolve_topk_slots (slot resolution is fused here).
+ *   out_bf16 [T, H, 512] bf16; lse [T, H] fp32 natural-log normaliser, or NULL.
+ *            A query with no live entry gets out = 0 and lse = -inf.
+ *   num_splits  0 = automatic (persistent CTAs over the whole batch, partial results merged
+ *            in a second kernel), 1 = one CTA per (query, 64-head chunk), S > 1 = each query's
+ *            list cut into S slices merged afterwards ("parallel tiled softmax", the
+ *            explainer of arXiv 2511.11581, section 4.5).
+ * Workspace: svt_sparse_mla_decode_workspace_size(T, H, K, num_splits) (depends on the
+ * current device's SM count when num_splits == 0).
+ */
+SVT_API size_t svt_sparse_mla_decode_workspace_size(int32_t T, int32_t H, int32_t K, int32_t num_splits);
+SVT_API svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const svt_kv_cache* kv,
+                                 const int32_t* block_table, int32_t num_reqs, int32_t max_blocks,
+                                 const int32_t* req_of_token,
+                                 const int32_t* seq_lens, const int32_t* topk, int32_t K, const int32_t* topk_len,
+                                 float softmax_scale, void* out_bf16, float* lse, int32_t num_splits, void* ws,
+                                 size_t ws_bytes, svt_stream_t stream);
+
+/*
+ * Group union (vLLM PR #63104, Details / Changes: each group of G consecutive queries gets
+ * the sorted union of its members' converted KV rows; Tests: empty groups, entries past a
+ * query's count, negative rows and rows up to the 24-bit limit; each member keeps to its
+ * own rows through a membership bit).
+ *   slots    [T, K] int32 cache slots (from svt_resolve_topk_slots), -1 = none.
+ *   topk_len [T] int32 or NULL (K).
+ *   G        2, 4 or 8; group g = queries gG .. gG+G-1 that exist (the last group may be
+ *            short: its missing members have no bit and no rows).
+ *   num_slots  rows in the cache; must be < 2^24 - 1 (0xFFFFFF is the pad pattern).
+ *   enc      [ceil(T/G), G*K] int32: for i < lens[g], (mask << 24) | slot, ascending by
+ *            slot, bit m of mask set iff member m selected that slot; -1 after lens[g].
+ *   lens     [ceil(T/G)] int32 union length.
+ * A live slot >= num_slots is dropped and sets SVT_DEV_ERR_INDEX_RANGE. G*K <= 32768.
+ */
+SVT_API size_t svt_build_group_union_workspace_size(int32_t T, int32_t K, int32_t G);
+SVT_API svt_status svt_build_group_union(const int32_t* slots, const int32_t* topk_len, int32_t T, int32_t K, int32_t G,
+                                 int64_t num_slots, int32_t* enc, int32_t* lens, void* ws, size_t ws_bytes,
+                                 svt_stream_t stream);
+
+/*
+ * Grouped sparse prefill (vLLM PR #63104, Overview: G = 128 / H consecutive queries share a
+ * 128-row tile, token-major, row r = (member r / H, head r mod H); they gather their union
+ * once and each row keeps to its member's entries through the mask bit).
+ *   q_bf16   [T, H, 576] bf16, token-major. H * G must be 128, G in {2, 4, 8}.
+ *   kv       the cache, addressed by flat slot (page_size is only used to size it).
+ *   enc/lens from svt_build_group_union with the same T, K, G.
+ *   out_bf16 [T, H, 512] bf16; lse [T, H] fp32 or NULL. A query whose member bit is set on
+ *            no entry gets out = 0 and lse = -inf.
+ * The cache must hold fewer than 2^24 - 1 rows. Workspace:
+ * svt_sparse_mla_prefill_grouped_workspace_size(T, H, G).
+ */
+SVT_API size_t svt_sparse_mla_prefill_grouped_workspace_size(int32_t T, int32_t H, int32_t G);
+SVT_API svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T, int32_t H, int32_t G,
+                                          const svt_kv_cache* kv, const int32_t* enc, const int32_t* lens, int32_t K,
+                                          float softmax_scale, void* out_bf16, float* lse, void* ws,
+                                          size_t ws_bytes, svt_stream_t stream);
+
+/*
+ * Merge of split-KV partials (explainer of arXiv 2511.11581, section 4.5: programs that own
+ * slices of the KV list produce partial results that are merged):
+ *   lse = ln sum_s exp(lse_part[s]),  out = sum_s exp(lse_part[s] - lse) * o_part[s].
+ *   o_part   [S, T, H, 512] fp32, each split's normalised output.
+ *   lse_part [S, T, H] fp32; a split at -inf weighs nothing.
+ *   out_bf16 [T, H, 512] bf16; lse [T, H] fp32 or NULL. All splits at -inf give out = 0,
+ *   lse = -inf. S in 1..64. No workspace.
+ */
+SVT_API svt_status svt_merge_splits(const float* o_part, const float* lse_part, int32_t S, int32_t T, int32_t H,
+                            void* out_bf16, float* lse, svt_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SVT_H_ */

@@ -1,0 +1,318 @@
+// The C ABI of libsvt.so: argument checks, workspace sizing, launch configuration and
+// status readback. Every check happens before anything is enqueued; nothing here allocates
+// device memory or synchronises a stream (except svt_read_status).
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+svt_status fail(svt_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+svt_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(SVT_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Checks the cache descriptor and returns its row stride in bytes.
+svt_status check_kv(const svt_kv_cache* kv, long long* row_stride) {
+  if (kv == nullptr) return fail(SVT_ERR_INVALID_ARG, "kv is null");
+  if (kv->data == nullptr) return fail(SVT_ERR_INVALID_ARG, "kv->data is null");
+  if (!aligned(kv->data, 16)) return fail(SVT_ERR_INVALID_ARG, "kv->data must be 16-byte aligned");
+  if (kv->num_pages <= 0 || kv->page_size <= 0) return fail(SVT_ERR_INVALID_ARG, "kv num_pages and page_size must be > 0");
+  if (kv->dtype != SVT_KV_BF16 && kv->dtype != SVT_KV_FP8_E4M3)
+    return fail(SVT_ERR_UNSUPPORTED, "unknown kv dtype %d", static_cast<int>(kv->dtype));
+  const int packed = kv->dtype == SVT_KV_BF16 ? svt::kRowBytesBf16 : svt::kRowBytesFp8;
+  const int stride = kv->row_stride_bytes == 0 ? packed : kv->row_stride_bytes;
+  if (stride < packed || stride % 16 != 0)
+    return fail(SVT_ERR_INVALID_ARG, "row_stride_bytes %d must be 0 or >= %d and a multiple of 16", stride, packed);
+  if (kv->num_pages * static_cast<long long>(kv->page_size) >= (1ll << 31))
+    return fail(SVT_ERR_UNSUPPORTED, "the cache must hold fewer than 2^31 rows");
+  *row_stride = stride;
+  return SVT_OK;
+}
+
+svt_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (ws == nullptr) return fail(SVT_ERR_INVALID_ARG, "workspace is null");
+  if (!aligned(ws, 256)) return fail(SVT_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (ws_bytes < need) return fail(SVT_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  return SVT_OK;
+}
+
+// Decode launch shape: (number of CTAs, partial slots needed).
+struct DecodePlan {
+  int rowsets, hchunks, tiles_per_rowset;
+  long long total_tiles;
+  int num_ctas;
+  bool partials;
+};
+
+DecodePlan plan_decode(int T, int H, int K, int num_splits) {
+  DecodePlan d{};
+  d.hchunks = (H + svt::kRowsetRows - 1) / svt::kRowsetRows;
+  d.rowsets = T * d.hchunks;
+  d.tiles_per_rowset = (K + svt::kTileRows - 1) / svt::kTileRows;
+  d.total_tiles = static_cast<long long>(d.rowsets) * d.tiles_per_rowset;
+  if (d.total_tiles == 0) {
+    d.num_ctas = 0;
+    d.partials = false;
+    return d;
+  }
+  long long n;
+  if (num_splits == 0) {
+    n = sm_count();
+    if (n <= 0) n = 1;
+  } else {
+    const int s = num_splits > d.tiles_per_rowset ? d.tiles_per_rowset : num_splits;
+    n = static_cast<long long>(d.rowsets) * s;
+  }
+  if (n > d.total_tiles) n = d.total_tiles;
+  d.num_ctas = static_cast<int>(n);
+  d.partials = (d.total_tiles % n) != 0 || (d.total_tiles / n) % d.tiles_per_rowset != 0;
+  return d;
+}
+
+size_t decode_ws_bytes(const DecodePlan& d) {
+  size_t b = svt::kStatusBytes;
+  if (d.partials) {
+    b += round_up(2ull * d.num_ctas * svt::kRowsetRows * svt::kVdim * sizeof(float), 256);
+    b += round_up(2ull * d.num_ctas * svt::kRowsetRows * sizeof(float), 256);
+  }
+  return b;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* svt_last_error_string(void) { return g_err; }
+
+svt_status svt_workspace_init(void* ws, size_t ws_bytes, svt_stream_t stream) {
+  svt_status st = check_ws(ws, ws_bytes, svt::kStatusBytes);
+  if (st != SVT_OK) return st;
+  cudaError_t e = cudaMemsetAsync(ws, 0, svt::kStatusBytes, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "svt_workspace_init");
+  return SVT_OK;
+}
+
+svt_status svt_read_status(void* ws, svt_stream_t stream, int32_t* host_out) {
+  if (ws == nullptr || host_out == nullptr) return fail(SVT_ERR_INVALID_ARG, "null argument");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(host_out, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, sizeof(int32_t), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "svt_read_status");
+  return SVT_OK;
+}
+
+size_t svt_resolve_workspace_size(void) { return svt::kStatusBytes; }
+
+svt_status svt_resolve_topk_slots(const int32_t* topk_pos, int32_t T, int32_t K, const int32_t* topk_len,
+                                  const int32_t* req_of_token, const int32_t* block_table, int32_t num_reqs,
+                                  int32_t max_blocks, const int32_t* seq_lens, int32_t page_size, int64_t num_pages,
+                                  int32_t* slots_out, void* ws, size_t ws_bytes, svt_stream_t stream) {
+  if (T < 0 || K < 0) return fail(SVT_ERR_INVALID_ARG, "T and K must be >= 0");
+  if (page_size <= 0 || num_pages <= 0) return fail(SVT_ERR_INVALID_ARG, "page_size and num_pages must be > 0");
+  if (num_pages * static_cast<long long>(page_size) >= (1ll << 31))
+    return fail(SVT_ERR_UNSUPPORTED, "the cache must hold fewer than 2^31 rows");
+  if (block_table != nullptr && (num_reqs <= 0 || max_blocks <= 0))
+    return fail(SVT_ERR_INVALID_ARG, "num_reqs and max_blocks must be > 0 with a block table");
+  if (static_cast<long long>(T) * K > 0 && (topk_pos == nullptr || slots_out == nullptr))
+    return fail(SVT_ERR_INVALID_ARG, "topk_pos and slots_out must not be null");
+  svt_status st = check_ws(ws, ws_bytes, svt_resolve_workspace_size());
+  if (st != SVT_OK) return st;
+  cudaError_t e = svt::launch_resolve(topk_pos, T, K, topk_len, req_of_token, block_table, num_reqs, max_blocks,
+                                      seq_lens, page_size, num_pages, slots_out, static_cast<int*>(ws),
+                                      reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "resolve launch");
+  return SVT_OK;
+}
+
+size_t svt_sparse_mla_decode_workspace_size(int32_t T, int32_t H, int32_t K, int32_t num_splits) {
+  if (T < 0 || H <= 0 || K < 0 || num_splits < 0) return svt::kStatusBytes;
+  return decode_ws_bytes(plan_decode(T, H, K, num_splits));
+}
+
+svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const svt_kv_cache* kv,
+                                 const int32_t* block_table, int32_t num_reqs, int32_t max_blocks,
+                                 const int32_t* req_of_token, const int32_t* seq_lens, const int32_t* topk, int32_t K,
+                                 const int32_t* topk_len, float softmax_scale, void* out_bf16, float* lse,
+                                 int32_t num_splits, void* ws, size_t ws_bytes, svt_stream_t stream) {
+  if (T < 0 || K < 0) return fail(SVT_ERR_INVALID_ARG, "T and K must be >= 0");
+  if (H <= 0) return fail(SVT_ERR_INVALID_ARG, "H must be > 0");
+  if (H > 128) return fail(SVT_ERR_UNSUPPORTED, "decode supports at most 128 heads, got %d", H);
+  if (num_splits < 0) return fail(SVT_ERR_INVALID_ARG, "num_splits must be >= 0");
+  if (!std::isfinite(softmax_scale)) return fail(SVT_ERR_INVALID_ARG, "softmax_scale must be finite");
+  long long row_stride = 0;
+  svt_status st = check_kv(kv, &row_stride);
+  if (st != SVT_OK) return st;
+  if (block_table != nullptr && (num_reqs <= 0 || max_blocks <= 0))
+    return fail(SVT_ERR_INVALID_ARG, "num_reqs and max_blocks must be > 0 with a block table");
+  const DecodePlan d = plan_decode(T, H, K, num_splits);
+  st = check_ws(ws, ws_bytes, decode_ws_bytes(d));
+  if (st != SVT_OK) return st;
+  if (T == 0) return SVT_OK;
+  if (q_bf16 == nullptr || out_bf16 == nullptr) return fail(SVT_ERR_INVALID_ARG, "q and out must not be null");
+  if (K > 0 && topk == nullptr) return fail(SVT_ERR_INVALID_ARG, "topk must not be null");
+  if (!aligned(q_bf16, 16) || !aligned(out_bf16, 16)) return fail(SVT_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+
+  svt::AttnParams p{};
+  p.q = static_cast<const uint16_t*>(q_bf16);
+  p.T = T;
+  p.H = H;
+  p.kv = static_cast<const uint8_t*>(kv->data);
+  p.row_stride = row_stride;
+  p.kv_dtype = kv->dtype;
+  p.num_slots = kv->num_pages * static_cast<long long>(kv->page_size);
+  p.mode = svt::kModeDecode;
+  p.topk = topk;
+  p.K = K;
+  p.topk_len = topk_len;
+  p.block_table = block_table;
+  p.num_reqs = num_reqs;
+  p.max_blocks = max_blocks;
+  p.req_of_token = req_of_token;
+  p.seq_lens = seq_lens;
+  p.page_size = kv->page_size;
+  p.num_pages = kv->num_pages;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.out = static_cast<uint16_t*>(out_bf16);
+  p.lse = lse;
+  p.sched = svt::kSchedStreamK;
+  p.num_rowsets = d.rowsets;
+  p.hchunks = d.hchunks;
+  p.tiles_per_rowset = d.tiles_per_rowset;
+  p.total_tiles = d.total_tiles;
+  p.num_ctas = d.num_ctas;
+  p.status = static_cast<int*>(ws);
+  if (d.partials) {
+    char* base = static_cast<char*>(ws) + svt::kStatusBytes;
+    p.part_o = reinterpret_cast<float*>(base);
+    p.part_lse = reinterpret_cast<float*>(
+        base + round_up(2ull * d.num_ctas * svt::kRowsetRows * svt::kVdim * sizeof(float), 256));
+  }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (d.num_ctas == 0) {
+    // K == 0: every query is empty; one CTA per row-set writes out = 0 and lse = -inf
+    p.tiles_per_rowset = 1;
+    p.total_tiles = d.rowsets;
+    p.num_ctas = d.rowsets;
+  }
+  cudaError_t e = svt::launch_attention(p, s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+  if (d.partials) {
+    e = svt::launch_streamk_merge(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode merge launch");
+  }
+  return SVT_OK;
+}
+
+size_t svt_build_group_union_workspace_size(int32_t, int32_t, int32_t) { return svt::kStatusBytes; }
+
+svt_status svt_build_group_union(const int32_t* slots, const int32_t* topk_len, int32_t T, int32_t K, int32_t G,
+                                 int64_t num_slots, int32_t* enc, int32_t* lens, void* ws, size_t ws_bytes,
+                                 svt_stream_t stream) {
+  if (T < 0 || K <= 0) return fail(SVT_ERR_INVALID_ARG, "T must be >= 0 and K > 0");
+  if (G != 2 && G != 4 && G != 8) return fail(SVT_ERR_UNSUPPORTED, "G must be 2, 4 or 8, got %d", G);
+  if (static_cast<long long>(G) * K > 32768) return fail(SVT_ERR_UNSUPPORTED, "G*K must be <= 32768");
+  if (num_slots <= 0) return fail(SVT_ERR_INVALID_ARG, "num_slots must be > 0");
+  if (num_slots >= 0xFFFFFF) return fail(SVT_ERR_UNSUPPORTED, "the union path needs fewer than 2^24-1 cache rows");
+  svt_status st = check_ws(ws, ws_bytes, svt_build_group_union_workspace_size(T, K, G));
+  if (st != SVT_OK) return st;
+  if (T == 0) return SVT_OK;
+  if (slots == nullptr || enc == nullptr || lens == nullptr) return fail(SVT_ERR_INVALID_ARG, "null array argument");
+  cudaError_t e = svt::launch_union(slots, topk_len, T, K, G, num_slots, enc, lens, static_cast<int*>(ws),
+                                    reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "union launch");
+  return SVT_OK;
+}
+
+size_t svt_sparse_mla_prefill_grouped_workspace_size(int32_t, int32_t, int32_t) { return svt::kStatusBytes; }
+
+svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T, int32_t H, int32_t G,
+                                          const svt_kv_cache* kv, const int32_t* enc, const int32_t* lens, int32_t K,
+                                          float softmax_scale, void* out_bf16, float* lse, void* ws,
+                                          size_t ws_bytes, svt_stream_t stream) {
+  if (T < 0 || K <= 0 || H <= 0) return fail(SVT_ERR_INVALID_ARG, "T must be >= 0, K and H > 0");
+  if (G != 2 && G != 4 && G != 8) return fail(SVT_ERR_UNSUPPORTED, "G must be 2, 4 or 8, got %d", G);
+  if (H * G != 128) return fail(SVT_ERR_UNSUPPORTED, "H * G must be 128 (H = %d, G = %d)", H, G);
+  if (!std::isfinite(softmax_scale)) return fail(SVT_ERR_INVALID_ARG, "softmax_scale must be finite");
+  long long row_stride = 0;
+  svt_status st = check_kv(kv, &row_stride);
+  if (st != SVT_OK) return st;
+  const long long num_slots = kv->num_pages * static_cast<long long>(kv->page_size);
+  if (num_slots >= 0xFFFFFF) return fail(SVT_ERR_UNSUPPORTED, "grouped prefill needs fewer than 2^24-1 cache rows");
+  st = check_ws(ws, ws_bytes, svt_sparse_mla_prefill_grouped_workspace_size(T, H, G));
+  if (st != SVT_OK) return st;
+  if (T == 0) return SVT_OK;
+  if (q_bf16 == nullptr || out_bf16 == nullptr || enc == nullptr || lens == nullptr)
+    return fail(SVT_ERR_INVALID_ARG, "null array argument");
+  if (!aligned(q_bf16, 16) || !aligned(out_bf16, 16)) return fail(SVT_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+
+  svt::AttnParams p{};
+  p.q = static_cast<const uint16_t*>(q_bf16);
+  p.T = T;
+  p.H = H;
+  p.kv = static_cast<const uint8_t*>(kv->data);
+  p.row_stride = row_stride;
+  p.kv_dtype = kv->dtype;
+  p.num_slots = num_slots;
+  p.mode = svt::kModePrefill;
+  p.K = K;
+  p.enc = enc;
+  p.lens = lens;
+  p.G = G;
+  p.list_stride = G * K;
+  p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.out = static_cast<uint16_t*>(out_bf16);
+  p.lse = lse;
+  p.sched = svt::kSchedRowsets;
+  const int groups = (T + G - 1) / G;
+  p.num_rowsets = 2 * groups;
+  p.hchunks = 1;
+  int sms = sm_count();
+  if (sms <= 0) sms = 1;
+  p.num_ctas = p.num_rowsets < sms ? p.num_rowsets : sms;
+  p.status = static_cast<int*>(ws);
+  cudaError_t e = svt::launch_attention(p, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
+  return SVT_OK;
+}
+
+svt_status svt_merge_splits(const float* o_part, const float* lse_part, int32_t S, int32_t T, int32_t H,
+                            void* out_bf16, float* lse, svt_stream_t stream) {
+  if (S < 1 || S > 64) return fail(SVT_ERR_INVALID_ARG, "S must be in 1..64");
+  if (T < 0 || H <= 0) return fail(SVT_ERR_INVALID_ARG, "T must be >= 0 and H > 0");
+  if (T == 0) return SVT_OK;
+  if (o_part == nullptr || lse_part == nullptr || out_bf16 == nullptr)
+    return fail(SVT_ERR_INVALID_ARG, "null array argument");
+  if (!aligned(o_part, 16) || !aligned(out_bf16, 16)) return fail(SVT_ERR_INVALID_ARG, "o_part and out must be 16-byte aligned");
+  cudaError_t e = svt::launch_merge_splits(o_part, lse_part, S, static_cast<long long>(T) * H, H,
+                                           static_cast<uint16_t*>(out_bf16), lse,
+                                           reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return SVT_OK;
+}
+
+}  // extern "C"

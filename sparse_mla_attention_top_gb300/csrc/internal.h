@@ -1,0 +1,95 @@
+// Host/device shared declarations of libsvt: kernel parameter blocks, the work schedule of
+// the attention kernel, and the launchers each .cu file provides to the C-ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "svt.h"
+
+namespace svt {
+
+constexpr int kRow = 576;          // 512 latent + 64 rope columns per cache row
+constexpr int kVdim = 512;         // V is the first 512 columns
+constexpr int kRowBytesBf16 = 1152;
+constexpr int kRowBytesFp8 = 656;  // 512 e4m3 | 4 fp32 scales | 64 bf16 rope
+constexpr size_t kStatusBytes = 256;  // status header at the start of every workspace
+
+// Attention kernel geometry (the tcgen05 tile): a tile is 128 KV rows (the MMA M), a
+// row-set is up to 64 query rows sharing one KV list (the MMA N).
+constexpr int kTileRows = 128;
+constexpr int kRowsetRows = 64;
+
+enum AttnMode : int { kModeDecode = 0, kModePrefill = 1 };
+enum Sched : int { kSchedStreamK = 0, kSchedRowsets = 1 };
+
+struct AttnParams {
+  // queries [T, H, 576] bf16
+  const uint16_t* q;
+  int T, H;
+  // cache
+  const uint8_t* kv;
+  long long row_stride;
+  int kv_dtype;
+  long long num_slots;
+  int mode;
+  // decode lists
+  const int* topk;
+  int K;
+  const int* topk_len;
+  const int* block_table;
+  int num_reqs;
+  int max_blocks;
+  const int* req_of_token;
+  const int* seq_lens;
+  int page_size;
+  long long num_pages;
+  // prefill lists
+  const int* enc;
+  const int* lens;
+  int G;
+  int list_stride;  // G * K
+  // softmax
+  float scale_log2;  // softmax_scale * log2(e)
+  // outputs
+  uint16_t* out;
+  float* lse;
+  // schedule
+  int sched;
+  int num_rowsets;
+  int hchunks;           // decode: 64-head chunks per query
+  int tiles_per_rowset;  // stream-K: tiles of the longest list
+  long long total_tiles;
+  int num_ctas;
+  float* part_o;    // [2 * num_ctas, 64, 512] fp32 (stream-K partial segments)
+  float* part_lse;  // [2 * num_ctas, 64]
+  int* status;
+};
+
+// First flattened tile of CTA c under the stream-K split of `total` tiles over n CTAs.
+__host__ __device__ inline long long streamk_lo(long long c, long long total, long long n) {
+  return c * total / n;
+}
+// The CTA whose stream-K range holds flattened tile `pos`.
+__host__ __device__ inline long long streamk_owner(long long pos, long long total, long long n) {
+  return ((pos + 1) * n - 1) / total;
+}
+
+// Launchers (each returns cudaSuccess or the launch error).
+cudaError_t launch_resolve(const int32_t* topk, int T, int K, const int32_t* topk_len, const int32_t* req_of_token,
+                           const int32_t* block_table, int num_reqs, int max_blocks, const int32_t* seq_lens,
+                           int page_size, long long num_pages, int32_t* slots, int* status, cudaStream_t stream);
+
+size_t union_smem_bytes(int G, int K);
+cudaError_t launch_union(const int32_t* slots, const int32_t* topk_len, int T, int K, int G, long long num_slots,
+                         int32_t* enc, int32_t* lens, int* status, cudaStream_t stream);
+
+cudaError_t launch_merge_splits(const float* o_part, const float* lse_part, int S, long long rows, int H_rows,
+                                uint16_t* out, float* lse, cudaStream_t stream);
+
+cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
+cudaError_t launch_streamk_merge(const AttnParams& p, cudaStream_t stream);
+int attention_smem_bytes();
+
+}  // namespace svt

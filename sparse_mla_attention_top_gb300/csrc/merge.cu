@@ -1,0 +1,123 @@
+// Merge of split-KV partial results.
+//
+// Explainer of arXiv 2511.11581 (Triton paged attention), section 4.5 "parallel tiled
+// softmax": several programs each own a slice of the KV list; their partial results are
+// combined afterwards. With lse_s the natural-log normaliser of slice s and o_s its
+// normalised output:  lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s.
+//
+// One warp per output row: the slice LSEs are reduced with warp shuffles, then each lane
+// accumulates 16 of the 512 channels. HBM-bound on reading the fp32 partials.
+#include <math_constants.h>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace svt {
+
+namespace {
+
+__device__ __forceinline__ float warp_allmax(float v) {
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+__device__ __forceinline__ float warp_allsum(float v) {
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+// Merges S partial rows for one output row. `lse_of(s)` / `o_of(s)` give slice s.
+template <typename LseOf, typename OOf>
+__device__ __forceinline__ void merge_row(int S, LseOf lse_of, OOf o_of, uint16_t* out_row, float* lse_out) {
+  const int lane = threadIdx.x & 31;
+  float mx = -CUDART_INF_F;
+  for (int s = lane; s < S; s += 32) mx = fmaxf(mx, lse_of(s));
+  mx = warp_allmax(mx);
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  float L = -CUDART_INF_F;
+  if (mx != -CUDART_INF_F) {
+    float tot = 0.f;
+    for (int s = lane; s < S; s += 32) tot += expf(lse_of(s) - mx);
+    tot = warp_allsum(tot);
+    L = mx + logf(tot);
+    for (int s = 0; s < S; ++s) {
+      const float ls = lse_of(s);
+      if (ls == -CUDART_INF_F) continue;
+      const float w = expf(ls - L);
+      const float4* o = reinterpret_cast<const float4*>(o_of(s)) + lane * 4;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const float4 x = o[v];
+        acc[4 * v + 0] += w * x.x;
+        acc[4 * v + 1] += w * x.y;
+        acc[4 * v + 2] += w * x.z;
+        acc[4 * v + 3] += w * x.w;
+      }
+    }
+  }
+  uint4 packed[2];
+  uint32_t* pw = reinterpret_cast<uint32_t*>(packed);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) pw[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+  uint4* dst = reinterpret_cast<uint4*>(out_row) + lane * 2;
+  dst[0] = packed[0];
+  dst[1] = packed[1];
+  if (lse_out != nullptr && lane == 0) *lse_out = L;
+}
+
+__global__ void __launch_bounds__(256) merge_splits_kernel(const float* __restrict__ o_part,
+                                                           const float* __restrict__ lse_part, int S,
+                                                           long long rows, uint16_t* __restrict__ out,
+                                                           float* __restrict__ lse) {
+  const long long r = blockIdx.x * 8ll + (threadIdx.x >> 5);
+  if (r >= rows) return;
+  merge_row(
+      S, [&](int s) { return lse_part[s * rows + r]; },
+      [&](int s) { return o_part + (s * rows + r) * kVdim; }, out + r * kVdim, lse ? lse + r : nullptr);
+}
+
+// Stream-K merge for the attention kernel: row-set r's tiles were spread over CTAs
+// owner(r*n) .. owner(r*n + n - 1); each wrote a partial into slot 2c (its first segment)
+// or 2c + 1 (its last one). Row-sets covered by a single CTA were written directly.
+__global__ void __launch_bounds__(256) streamk_merge_kernel(AttnParams p) {
+  const int r = blockIdx.x;
+  const long long n = p.tiles_per_rowset;
+  const long long first = r * n, last = r * n + n - 1;
+  const long long c_lo = streamk_owner(first, p.total_tiles, p.num_ctas);
+  const long long c_hi = streamk_owner(last, p.total_tiles, p.num_ctas);
+  if (c_lo == c_hi) return;
+  const int S = static_cast<int>(c_hi - c_lo + 1);
+  const int t = r / p.hchunks, hc = r - t * p.hchunks;
+  for (int row = threadIdx.x >> 5; row < kRowsetRows; row += 8) {
+    const int h = hc * kRowsetRows + row;
+    if (h >= p.H) break;
+    auto slot_of = [&](int s) -> long long {
+      const long long c = c_lo + s;
+      return (streamk_lo(c, p.total_tiles, p.num_ctas) < first) ? 2 * c + 1 : 2 * c;
+    };
+    merge_row(
+        S, [&](int s) { return p.part_lse[slot_of(s) * kRowsetRows + row]; },
+        [&](int s) { return p.part_o + (slot_of(s) * kRowsetRows + row) * kVdim; },
+        p.out + (static_cast<long long>(t) * p.H + h) * kVdim,
+        p.lse ? p.lse + static_cast<long long>(t) * p.H + h : nullptr);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_merge_splits(const float* o_part, const float* lse_part, int S, long long rows, int /*H_rows*/,
+                                uint16_t* out, float* lse, cudaStream_t stream) {
+  if (rows == 0) return cudaSuccess;
+  const long long blocks = (rows + 7) / 8;
+  merge_splits_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_part, lse_part, S, rows, out, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_streamk_merge(const AttnParams& p, cudaStream_t stream) {
+  if (p.num_rowsets == 0) return cudaSuccess;
+  streamk_merge_kernel<<<p.num_rowsets, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace svt

@@ -1,0 +1,148 @@
+// Group union with per-member membership masks.
+//
+// vLLM PR #63104 (grouped sparse-MLA prefill on FA4), Details / Changes: each group of G
+// consecutive queries needs the sorted union of its members' converted KV rows, built from
+// the rows themselves so that the cost does not depend on the sequence length; Tests: empty
+// groups, entries past a query's count, negative rows and rows up to the 24-bit limit, and
+// every query keeps to its own rows through its membership bit.
+//
+// One CTA per group. The G*K candidate entries become 27-bit keys (slot << 3 | member) in
+// shared memory, a bitonic sort orders them by slot (then member), and a block scan over
+// run starts gives each distinct slot its output position; the run's members are ORed into
+// the mask. Output entry: (mask << 24) | slot, then -1 padding up to G*K. Integer only, so
+// the result is bit-exact by construction. Bound by shared-memory traffic of the sort.
+#include "device.cuh"
+#include "internal.h"
+
+namespace svt {
+
+namespace {
+
+constexpr uint32_t kSentinel = 0xFFFFFFFFu;
+
+__host__ __device__ inline int next_pow2(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+__global__ void union_kernel(const int32_t* __restrict__ slots, const int32_t* __restrict__ topk_len, int T, int K,
+                             int G, long long num_slots, int npow, int32_t* __restrict__ enc,
+                             int32_t* __restrict__ lens, int* status) {
+  extern __shared__ uint32_t keys[];  // [npow] then [32] warp totals
+  uint32_t* warp_tot = keys + npow;
+  const int g = blockIdx.x;
+  const int n = G * K;
+  const int tid = threadIdx.x;
+  const int nthreads = blockDim.x;
+
+  // 1. candidate keys
+  int err = 0;
+  for (int i = tid; i < npow; i += nthreads) {
+    uint32_t key = kSentinel;
+    if (i < n) {
+      const int m = i / K;
+      const int j = i - m * K;
+      const int t = g * G + m;
+      if (t < T) {
+        const int len = topk_len ? topk_len[t] : K;
+        if (j < len) {
+          const int s = slots[static_cast<long long>(t) * K + j];
+          if (s >= 0) {
+            if (static_cast<long long>(s) >= num_slots || s >= 0xFFFFFF) {
+              err = 1;
+            } else {
+              key = (static_cast<uint32_t>(s) << 3) | static_cast<uint32_t>(m);
+            }
+          }
+        }
+      }
+    }
+    keys[i] = key;
+  }
+  if (__any_sync(0xffffffffu, err) && (tid & 31) == 0) atomicOr(status, SVT_DEV_ERR_INDEX_RANGE);
+  __syncthreads();
+
+  // 2. bitonic sort, ascending; each thread takes pairs (i, i + j)
+  for (int k = 2; k <= npow; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int p = tid; p < (npow >> 1); p += nthreads) {
+        const int i = ((p / j) * (j << 1)) + (p % j);
+        const int ixj = i + j;
+        const uint32_t a = keys[i], b = keys[ixj];
+        const bool up = (i & k) == 0;
+        if ((a > b) == up) {
+          keys[i] = b;
+          keys[ixj] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+
+  // 3. run starts: a distinct slot begins where the slot part changes
+  const int chunk = (npow + nthreads - 1) / nthreads;
+  const int begin = tid * chunk;
+  const int end = min(npow, begin + chunk);
+  int cnt = 0;
+  for (int i = begin; i < end; ++i) {
+    const uint32_t k0 = keys[i];
+    if (k0 != kSentinel && (i == 0 || (keys[i - 1] >> 3) != (k0 >> 3))) ++cnt;
+  }
+  // block exclusive scan of cnt
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = cnt;
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) warp_tot[warp] = static_cast<uint32_t>(incl);
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = nthreads >> 5;
+    int v = lane < nw ? static_cast<int>(warp_tot[lane]) : 0;
+    int w = v;
+    for (int off = 1; off < 32; off <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += u;
+    }
+    if (lane < nw) warp_tot[lane] = static_cast<uint32_t>(w - v);  // exclusive
+    if (lane == 31) lens[g] = w;                                      // total distinct slots
+  }
+  __syncthreads();
+  int pos = static_cast<int>(warp_tot[warp]) + (incl - cnt);
+  int32_t* out = enc + static_cast<long long>(g) * n;
+  for (int i = begin; i < end; ++i) {
+    const uint32_t k0 = keys[i];
+    if (k0 == kSentinel || (i > 0 && (keys[i - 1] >> 3) == (k0 >> 3))) continue;
+    const uint32_t slot = k0 >> 3;
+    uint32_t mask = 0;
+    for (int r = i; r < npow && keys[r] != kSentinel && (keys[r] >> 3) == slot; ++r) mask |= 1u << (keys[r] & 7u);
+    out[pos++] = static_cast<int32_t>((mask << 24) | slot);
+  }
+  __syncthreads();
+  // 4. -1 padding after the union
+  const int total = lens[g];
+  for (int i = total + tid; i < n; i += nthreads) out[i] = -1;
+}
+
+}  // namespace
+
+size_t union_smem_bytes(int G, int K) { return (static_cast<size_t>(next_pow2(G * K)) + 32) * sizeof(uint32_t); }
+
+cudaError_t launch_union(const int32_t* slots, const int32_t* topk_len, int T, int K, int G, long long num_slots,
+                         int32_t* enc, int32_t* lens, int* status, cudaStream_t stream) {
+  const int groups = (T + G - 1) / G;
+  if (groups == 0) return cudaSuccess;
+  const int npow = next_pow2(G * K);
+  int threads = npow / 4;
+  threads = threads < 64 ? 64 : (threads > 1024 ? 1024 : threads);
+  const size_t smem = union_smem_bytes(G, K);
+  cudaError_t e = cudaFuncSetAttribute(union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  union_kernel<<<groups, threads, smem, stream>>>(slots, topk_len, T, K, G, num_slots, npow, enc, lens, status);
+  return cudaGetLastError();
+}
+
+}  // namespace svt

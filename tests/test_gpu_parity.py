@@ -1,0 +1,314 @@
+"""Parity of the CUDA path with the CPU oracle on small seeded inputs that still span
+several tiles and a ragged tail. Integer outputs (slots, unions) must be bit-exact; float
+outputs must stay within the stated tolerances (out 2e-2 bf16 / 5e-2 fp8, lse 1e-3)."""
+
+import numpy as np
+import pytest
+
+import oracle
+from sparse_mla_attention_top_gb300 import workloads as W
+from tests import _golden
+from tests._dev import BF16_OUT_TOL, FP8_OUT_TOL, LSE_TOL, compare, kv_of, out_tol, to_dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def S():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_mla_attention_top_gb300 as S
+    from sparse_mla_attention_top_gb300 import build
+
+    build.build()
+    return S
+
+
+@pytest.fixture(scope="module")
+def dev(S):
+    return torch.device("cuda", 0)
+
+
+@pytest.fixture()
+def ws(S, dev):
+    return S.Workspace(dev)
+
+
+def gpu_decode(S, w, dev, ws, topk=None, topk_len=None, num_splits=0, use_table=True):
+    topk = w.topk if topk is None else topk
+    return S.sparse_mla_decode(to_dev(w.q_bits, dev), kv_of(w, dev), to_dev(topk, dev), w.scale,
+                               block_table=to_dev(w.block_table, dev) if use_table else None,
+                               seq_lens=to_dev(w.seq_lens, dev) if use_table else None,
+                               req_of_token=to_dev(w.req_of_token, dev) if use_table else None,
+                               topk_len=to_dev(topk_len, dev), num_splits=num_splits, ws=ws)
+
+
+def oracle_decode(w, topk=None, topk_len=None, query_ids=None):
+    topk = w.topk if topk is None else topk
+    return oracle.decode(w.q_bits, w.kv, w.kv_dtype, w.num_pages, w.page_size, topk, w.scale,
+                         block_table=w.block_table, seq_lens=w.seq_lens, req_of_token=w.req_of_token,
+                         topk_len=topk_len, query_ids=query_ids)
+
+
+# ------------------------------------------------------------------------ slot resolution
+
+def test_resolve_hand_worked_example(S, dev, ws):
+    c = _golden.resolve_case()
+    slots = S.resolve_topk_slots(to_dev(c["topk"], dev), block_table=to_dev(c["block_table"], dev),
+                                 seq_lens=to_dev(c["seq_lens"], dev), req_of_token=to_dev(c["req_of_token"], dev),
+                                 topk_len=to_dev(c["topk_len"], dev), page_size=c["page_size"],
+                                 num_pages=c["num_pages"], ws=ws)
+    assert np.array_equal(slots.cpu().numpy(), c["slots"])
+    assert ws.read_status() == S.svt.DEV_ERR_INDEX_RANGE
+
+
+@pytest.mark.parametrize("page_size", [1, 16, 64])
+def test_resolve_matches_oracle_bit_exact(S, dev, ws, page_size):
+    w = W.make_decode(21, T=9, H=1, K=333, ctx_lo=100, ctx_hi=5000, page_size=page_size)
+    topk = w.topk.copy()
+    rng = np.random.default_rng(page_size)
+    topk[rng.random(topk.shape) < 0.05] = -1
+    topk[0, 5] = w.seq_lens[0] + 3  # past the request: range error
+    topk_len = rng.integers(0, w.K + 1, size=w.T).astype(np.int32)
+    slots = S.resolve_topk_slots(to_dev(topk, dev), block_table=to_dev(w.block_table, dev),
+                                 seq_lens=to_dev(w.seq_lens, dev), topk_len=to_dev(topk_len, dev),
+                                 page_size=w.page_size, num_pages=w.num_pages, ws=ws)
+    ref, err = oracle.resolve(topk, topk_len, None, w.block_table, w.seq_lens, w.page_size, w.num_pages)
+    assert np.array_equal(slots.cpu().numpy().astype(np.int64), ref)
+    assert ws.read_status() == (S.svt.DEV_ERR_INDEX_RANGE if err & 1 else 0)
+
+
+# ---------------------------------------------------------------------------------- union
+
+def test_union_hand_worked_cases(S, dev, ws):
+    for c in _golden.union_cases():
+        slots = np.array(c["rows"], np.int32)
+        ln = np.array(c["lens_rows"], np.int32)
+        enc, lens = S.build_group_union(to_dev(slots, dev), c["G"], c["num_slots"], topk_len=to_dev(ln, dev), ws=ws)
+        ref_enc, ref_lens, _ = oracle.group_union(slots, c["G"], c["num_slots"], topk_len=ln)
+        assert np.array_equal(lens.cpu().numpy(), ref_lens), c["name"]
+        assert np.array_equal(enc.cpu().numpy(), ref_enc), c["name"]
+        for g, (n, pairs) in c["groups"].items():
+            assert enc[g, :n].cpu().tolist() == [_golden.encode(m, s) for m, s in pairs]
+    assert ws.read_status() == 0
+
+
+@pytest.mark.parametrize("G,K,T", [(2, 64, 17), (4, 100, 22), (8, 33, 70), (2, 2048, 9), (8, 2048, 11)])
+def test_union_matches_oracle_bit_exact(S, dev, ws, G, K, T):
+    rng = np.random.default_rng(G * 1000 + K)
+    num_slots = 5000
+    slots = np.full((T, K), -1, np.int32)
+    for t in range(T):
+        n = int(rng.integers(0, K + 1))
+        base = rng.choice(num_slots, size=n, replace=False).astype(np.int32)
+        if t > 0 and n:  # neighbours overlap
+            prev = slots[t - 1][slots[t - 1] >= 0]
+            k = min(len(prev), n // 2)
+            base[:k] = prev[:k]
+            base = np.unique(base)
+            rng.shuffle(base)
+        slots[t, :len(base)] = base
+        slots[t] = slots[t][rng.permutation(K)]
+    ln = rng.integers(0, K + 1, size=T).astype(np.int32)
+    enc, lens = S.build_group_union(to_dev(slots, dev), G, num_slots, topk_len=to_dev(ln, dev), ws=ws)
+    ref_enc, ref_lens, err = oracle.group_union(slots, G, num_slots, topk_len=ln)
+    assert err == 0
+    assert np.array_equal(lens.cpu().numpy(), ref_lens)
+    assert np.array_equal(enc.cpu().numpy(), ref_enc)
+
+
+def test_union_out_of_range_slot_is_dropped_and_flagged(S, dev, ws):
+    slots = np.array([[3, 900, 5], [5, -1, 7]], np.int32)
+    enc, lens = S.build_group_union(to_dev(slots, dev), 2, 100, ws=ws)
+    ref_enc, ref_lens, err = oracle.group_union(slots, 2, 100)
+    assert err == 1 and np.array_equal(enc.cpu().numpy(), ref_enc) and lens.item() == 3
+    assert ws.read_status() == S.svt.DEV_ERR_INDEX_RANGE
+
+
+# --------------------------------------------------------------------------------- decode
+
+def test_tiny_decode(S, dev, ws):
+    w = W.tiny_decode()
+    out, lse = gpu_decode(S, w, dev, ws)
+    ref, ref_lse, err = oracle_decode(w)
+    assert err == 0
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    assert ws.read_status() == 0
+
+
+@pytest.mark.parametrize("num_splits", [0, 1, 2, 3])
+def test_decode_ragged_tail_and_splits(S, dev, ws, num_splits):
+    # K = 300: two full 128-row tiles and a tail of 44
+    w = W.make_decode(31, T=7, H=64, K=300, ctx_lo=250, ctx_hi=4000, page_size=64)
+    out, lse = gpu_decode(S, w, dev, ws, num_splits=num_splits)
+    ref, ref_lse, err = oracle_decode(w)
+    assert err == 0
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    assert ws.read_status() == 0
+
+
+@pytest.mark.parametrize("H", [1, 8, 16, 33, 64, 100, 128])
+def test_decode_head_counts(S, dev, ws, H):
+    w = W.make_decode(40 + H, T=3, H=H, K=200, ctx_lo=300, ctx_hi=900, page_size=16)
+    out, lse = gpu_decode(S, w, dev, ws)
+    ref, ref_lse, _ = oracle_decode(w)
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+
+
+def test_decode_fp8_cache(S, dev, ws):
+    w = W.make_decode(51, T=5, H=64, K=260, ctx_lo=300, ctx_hi=3000, page_size=64, kv_dtype=W.KV_FP8_E4M3)
+    out, lse = gpu_decode(S, w, dev, ws)
+    ref, ref_lse, err = oracle_decode(w)
+    assert err == 0
+    compare(out, lse, ref, ref_lse, FP8_OUT_TOL)
+    assert ws.read_status() == 0
+
+
+def test_decode_virtual_block_table_equals_paged(S, dev, ws):
+    # slots passed directly (no table, page_size-1 view) give the same result as positions
+    w = W.make_decode(52, T=4, H=32, K=190, ctx_lo=200, ctx_hi=2000, page_size=64)
+    out, lse = gpu_decode(S, w, dev, ws)
+    slots, _ = oracle.resolve(w.topk, block_table=w.block_table, seq_lens=w.seq_lens, page_size=w.page_size,
+                              num_pages=w.num_pages)
+    out2, lse2 = gpu_decode(S, w, dev, ws, topk=slots.astype(np.int32), use_table=False)
+    assert torch.equal(out, out2) and torch.equal(lse, lse2)
+
+
+def test_decode_padding_and_live_counts(S, dev, ws):
+    w = W.make_decode(53, T=4, H=16, K=256, ctx_lo=400, ctx_hi=900, page_size=8)
+    rng = np.random.default_rng(1)
+    padded = np.full((w.T, 400), -1, np.int32)
+    for t in range(w.T):
+        where = np.sort(rng.choice(400, w.K, replace=False))
+        padded[t, where] = w.topk[t]
+    out, lse = gpu_decode(S, w, dev, ws, topk=padded)
+    ref, ref_lse, _ = oracle_decode(w)
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    lens = np.array([0, 1, 129, 256], np.int32)
+    out, lse = gpu_decode(S, w, dev, ws, topk_len=lens)
+    ref, ref_lse, _ = oracle_decode(w, topk_len=lens)
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))  # empty query
+
+
+def test_decode_single_index_returns_v_row(S, dev, ws):
+    w = W.make_decode(54, T=3, H=64, K=5, ctx_lo=100, ctx_hi=100, page_size=4)
+    topk = np.full((3, 5), -1, np.int32)
+    topk[:, 2] = [7, 50, 99]
+    out, lse = gpu_decode(S, w, dev, ws, topk=topk)
+    slots, _ = oracle.resolve(topk, block_table=w.block_table, seq_lens=w.seq_lens, page_size=w.page_size,
+                              num_pages=w.num_pages)
+    rows = oracle.fetch_rows(w.kv, w.kv_dtype, slots[:, 2])
+    o = out.float().cpu().numpy()
+    for t in range(3):  # exactly the bf16 V row (P = 1, l = 1)
+        assert np.array_equal(o[t], np.broadcast_to(rows[t, :512], (64, 512)))
+    ref, ref_lse, _ = oracle_decode(w, topk=topk)
+    assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) <= LSE_TOL
+
+
+def test_decode_zero_query_gives_mean_and_log_count(S, dev, ws):
+    w = W.make_decode(55, T=2, H=8, K=300, ctx_lo=1000, ctx_hi=1000, page_size=64)
+    w.q_bits[:] = 0
+    out, lse = gpu_decode(S, w, dev, ws)
+    slots, _ = oracle.resolve(w.topk, block_table=w.block_table, seq_lens=w.seq_lens, page_size=w.page_size,
+                              num_pages=w.num_pages)
+    for t in range(2):
+        mean = oracle.fetch_rows(w.kv, w.kv_dtype, slots[t])[:, :512].mean(axis=0)
+        assert np.max(np.abs(out[t].float().cpu().numpy() - mean)) <= BF16_OUT_TOL
+    assert np.allclose(lse.cpu().numpy(), np.log(300), atol=LSE_TOL)
+
+
+def test_decode_order_invariance(S, dev, ws):
+    w = W.make_decode(56, T=3, H=64, K=384, ctx_lo=500, ctx_hi=3000, page_size=64)
+    out, lse = gpu_decode(S, w, dev, ws)
+    perm = np.random.default_rng(2).permutation(w.K)
+    out2, lse2 = gpu_decode(S, w, dev, ws, topk=np.ascontiguousarray(w.topk[:, perm]))
+    assert float((out.float() - out2.float()).abs().max()) <= BF16_OUT_TOL
+    assert float((lse - lse2).abs().max()) <= LSE_TOL
+
+
+def test_decode_out_of_range_entries_are_dead_and_flagged(S, dev, ws):
+    w = W.make_decode(57, T=2, H=16, K=130, ctx_lo=500, ctx_hi=600, page_size=64)
+    bad = w.topk.copy()
+    bad[1, 7] = 10 ** 6
+    out, lse = gpu_decode(S, w, dev, ws, topk=bad)
+    ref, ref_lse, err = oracle_decode(w, topk=bad)
+    assert err == 1
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    assert ws.read_status() == S.svt.DEV_ERR_INDEX_RANGE
+
+
+def test_decode_large_scores_rescale(S, dev, ws):
+    # Scores that grow tile after tile force the reference maximum to move (rescale path).
+    w = W.make_decode(58, T=2, H=64, K=512, ctx_lo=600, ctx_hi=600, page_size=64)
+    scale = 0.5  # wide score spread
+    out, lse = S.sparse_mla_decode(to_dev(w.q_bits, dev), kv_of(w, dev), to_dev(w.topk, dev), scale,
+                                   block_table=to_dev(w.block_table, dev), seq_lens=to_dev(w.seq_lens, dev), ws=ws)
+    ref, ref_lse, _ = oracle.decode(w.q_bits, w.kv, w.kv_dtype, w.num_pages, w.page_size, w.topk, scale,
+                                    block_table=w.block_table, seq_lens=w.seq_lens)
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+
+
+# ---------------------------------------------------------------------------------- merge
+
+def test_merge_splits_matches_oracle(S, dev):
+    rng = np.random.default_rng(3)
+    Sn, T, H = 5, 3, 7
+    o = rng.standard_normal((Sn, T, H, 512)).astype(np.float32)
+    l = rng.standard_normal((Sn, T, H)).astype(np.float32) * 3
+    l[1, 0, :] = -np.inf
+    l[:, 2, 3] = -np.inf  # an all-empty row
+    out, lse = S.merge_splits(to_dev(o, dev), to_dev(l, dev))
+    ref, ref_lse = oracle.merge(o, l)
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    assert torch.all(out[2, 3] == 0)
+
+
+# -------------------------------------------------------------------------- grouped prefill
+
+def gpu_prefill(S, w, dev, ws):
+    slots = S.resolve_topk_slots(to_dev(w.topk, dev), block_table=to_dev(w.block_table, dev),
+                                 seq_lens=to_dev(w.seq_lens, dev), req_of_token=to_dev(w.req_of_token, dev),
+                                 page_size=w.page_size, num_pages=w.num_pages, ws=ws)
+    enc, lens = S.build_group_union(slots, w.G, w.num_slots, ws=ws)
+    out, lse = S.sparse_mla_prefill_grouped(to_dev(w.q_bits, dev), w.G, kv_of(w, dev), enc, lens, w.K, w.scale, ws=ws)
+    return slots, enc, lens, out, lse
+
+
+@pytest.mark.parametrize("H,G,T", [(64, 2, 13), (32, 4, 22), (16, 8, 37)])
+def test_prefill_matches_oracle(S, dev, ws, H, G, T):
+    w = W.make_prefill(60 + G, n_new=T, n_cached=150, H=H, G=G, K=160, page_size=16)
+    slots, enc, lens, out, lse = gpu_prefill(S, w, dev, ws)
+    ref_slots, _ = oracle.resolve(w.topk, req_of_token=w.req_of_token, block_table=w.block_table,
+                                  seq_lens=w.seq_lens, page_size=w.page_size, num_pages=w.num_pages)
+    assert np.array_equal(slots.cpu().numpy().astype(np.int64), ref_slots)
+    ref_enc, ref_lens, _ = oracle.group_union(ref_slots.astype(np.int32), G, w.num_slots)
+    assert np.array_equal(enc.cpu().numpy(), ref_enc) and np.array_equal(lens.cpu().numpy(), ref_lens)
+    ref, ref_lse, err = oracle.prefill_grouped(w.q_bits, G, w.kv, w.kv_dtype, w.num_slots, ref_enc, ref_lens, w.K,
+                                               w.scale)
+    assert err == 0
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    assert ws.read_status() == 0
+
+
+def test_prefill_equals_per_query_decode_on_gpu(S, dev, ws):
+    w = W.make_prefill(70, n_new=9, n_cached=300, H=64, G=2, K=200, page_size=64)
+    _, _, _, out, lse = gpu_prefill(S, w, dev, ws)
+    out_d, lse_d = gpu_decode(S, w, dev, ws)
+    assert float((out.float() - out_d.float()).abs().max()) <= BF16_OUT_TOL
+    assert float((lse - lse_d).abs().max()) <= LSE_TOL
+
+
+def test_prefill_membership_bit_negative_control(S, dev, ws):
+    # A flipped membership bit must change that member's rows: the parity check has teeth.
+    w = W.make_prefill(71, n_new=4, n_cached=400, H=64, G=2, K=128, page_size=64)
+    slots, enc, lens, out, lse = gpu_prefill(S, w, dev, ws)
+    e = enc.clone()
+    row = e[0, : int(lens[0])]
+    has1 = ((row.view(torch.int32) >> 24) & 2) != 0
+    idx = int(torch.nonzero(~has1)[0])
+    e[0, idx] = row[idx] | (2 << 24)
+    out2, lse2 = S.sparse_mla_prefill_grouped(to_dev(w.q_bits, dev), w.G, kv_of(w, dev), e, lens, w.K, w.scale, ws=ws)
+    assert float((lse2[1] - lse[1]).abs().max()) > LSE_TOL
+    assert torch.equal(out2[0], out[0])
