@@ -17,8 +17,10 @@
  *    out of time) never trap: the offending entry is treated as dead (never read), and a bit
  *    is ORed into the status word that lives in the first 256 bytes of the caller's
  *    workspace. Read and clear it with svt_read_status().
- *  - Every workspace must be at least the size its query returns and 256-byte aligned;
- *    zero its first 256 bytes once before first use (svt_workspace_init does that).
+ *  - Every workspace must be at least the size its query returns and 256-byte aligned, and
+ *    must be zeroed once before its first use (svt_workspace_init does that). Kernels leave
+ *    the parts they use zero again (apart from status bits), so calls that run one after
+ *    another on a stream can share one workspace; calls that overlap on the GPU must not.
  *  - Arrays are contiguous, row-major, in the layouts stated per argument. Every cache row
  *    and every q row must start on a 16-byte boundary.
  *
@@ -83,7 +85,7 @@ typedef struct {
 /* Human-readable reason for the last non-OK status returned on this thread. */
 SVT_API const char* svt_last_error_string(void);
 
-/* Zeroes the 256-byte status header of a workspace (asynchronous, on `stream`). */
+/* Zeroes a whole workspace (asynchronous, on `stream`). */
 SVT_API svt_status svt_workspace_init(void* ws, size_t ws_bytes, svt_stream_t stream);
 
 /* Copies the device status word to *host_out, clears it, and waits for the stream.
@@ -124,10 +126,11 @@ SVT_API svt_status svt_resolve_topk_slots(const int32_t* topk_pos, int32_t T, in
  *            topk/topk_len are as for svt_resolve_topk_slots (slot resolution is fused here).
  *   out_bf16 [T, H, 512] bf16; lse [T, H] fp32 natural-log normaliser, or NULL.
  *            A query with no live entry gets out = 0 and lse = -inf.
- *   num_splits  0 = automatic (persistent CTAs over the whole batch, partial results merged
- *            in a second kernel), 1 = one CTA per (query, 64-head chunk), S > 1 = each query's
- *            list cut into S slices merged afterwards ("parallel tiled softmax", the
- *            explainer of arXiv 2511.11581, section 4.5).
+ *   num_splits  0 = automatic (persistent CTAs share the whole batch's tiles evenly; a
+ *            query whose list is split between CTAs is merged in the same kernel by the
+ *            last CTA to finish its part), 1 = one CTA per (query, 64-head chunk), S > 1 =
+ *            each query's list cut into S slices ("parallel tiled softmax", the explainer of
+ *            arXiv 2511.11581, section 4.5), merged the same way.
  * Workspace: svt_sparse_mla_decode_workspace_size(T, H, K, num_splits) (depends on the
  * current device's SM count when num_splits == 0).
  */

@@ -17,21 +17,26 @@
 //   O^T[512 x 64] += V_tile^T[512 x 128] . P^T         (MN-major A and B, 4 x 8 MMAs)
 // S^T takes 64 TMEM columns and O^T 4 x 64, leaving the fp32 accumulators of a whole
 // 64-row row-set on chip (a 128-row O would need all 512 columns by itself).
+//
 // Warp roles (512 threads, 4 warps per SM sub-partition, so 128 registers each):
 //   warps 0-7  softmax + epilogue: warp w reads TMEM lanes 32*(w%4).. (KV rows) and column
 //              half w/4 (32 query rows) of S^T; online softmax in fp32 with a lazily moved
 //              reference maximum (rescale only when a score exceeds it by 2^8); P^T is
-//              written as bf16 into the smem block that held the tile's rope columns.
-//              Lane 0 of warp 0 also owns TMEM and issues every MMA: PV right after the
-//              group has written P^T, then the next tile's S^T, which the group waits for
-//              anyway, so a dedicated issuing warp would add registers and nothing else.
-//   warps 8-15 loaders: resolve the tile's 128 entries to slots (fused slot resolution),
-//              then gather each row's 9 blocks of 128 bytes with 16-byte cp.async into the
-//              128-byte-swizzled operand layout; dead rows are zero-filled.
-// The smem stage (9 x 16 KB) is released block by block as the PV MMAs finish with it, so
-// the next tile's gather overlaps this tile's PV. Persistent CTAs walk a static schedule:
-// stream-K over (row-set, tile) for decode (partials merged by a second kernel), whole
-// row-sets round-robin for grouped prefill.
+//              written into the smem block that held the tile's rope columns. Lane 0 of
+//              warp 0 also owns TMEM and issues every MMA: PV right after the group has
+//              written P^T, then the next tile's S^T, which the group waits for anyway.
+//   warps 8-15 loaders. Per tile they resolve the 128 entries to cache slots (fused slot
+//              resolution, one tile ahead), then fill the single smem stage (9 blocks of
+//              128 rows x 128 bytes in the 128-byte-swizzled operand layout, dead rows
+//              zero): blocks 4-8 are read into registers while the previous tile is still
+//              being computed and stored the moment its PV releases them; blocks 0-3 go by
+//              16-byte cp.async. The S^T MMAs consume blocks 4..8 first, then 0..3.
+//              For e4m3 caches every block is staged in registers and converted to f16.
+// Persistent CTAs walk a static schedule: stream-K over (row-set, tile) for decode, whole
+// row-sets round-robin for grouped prefill. A row-set split between CTAs is merged inside
+// the kernel by the last CTA to finish its part (an atomic count per split row-set, kept
+// in the workspace at the index of the row-set's first CTA, which no other split row-set
+// shares).
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
@@ -47,23 +52,25 @@ constexpr int kThreads = 512;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kLoaderWarp0 = 8;
 constexpr int kLoaderThreads = 256;
-constexpr int kBlocks = 9;                      // 64-column blocks of a 576-wide row
-constexpr int kBlockBytes = kTileRows * 128;    // 16 KB: 128 rows x 64 bf16
+constexpr int kBlocks = 9;                       // 64-column blocks of a 576-wide row
+constexpr int kBlockBytes = kTileRows * 128;     // 16 KB: 128 rows x 64 bf16
 constexpr int kQBlockBytes = kRowsetRows * 128;  // 8 KB: 64 rows x 64 bf16
-constexpr float kTau = 8.0f;                    // lazy-rescale threshold, log2 units
+constexpr int kRegBlock0 = 4;                    // bf16 blocks 4..8 staged in registers
+constexpr float kTau = 8.0f;                     // lazy-rescale threshold, log2 units
 
 // shared memory map (offsets from a 1024-aligned base)
 constexpr int kOffStage = 0;
-constexpr int kOffQ = kOffStage + kBlocks * kBlockBytes;   // 147456
-constexpr int kOffSlot = kOffQ + kBlocks * kQBlockBytes;   // 221184: int[2][128]
-constexpr int kOffMask = kOffSlot + 2 * kTileRows * 4;     // uint[2][128]
-constexpr int kOffMref = kOffMask + 2 * kTileRows * 4;     // float[64]
-constexpr int kOffAlpha = kOffMref + kRowsetRows * 4;      // float[64]
-constexpr int kOffRed = kOffAlpha + kRowsetRows * 4;       // float[8][32]
-constexpr int kOffLfin = kOffRed + 8 * 32 * 4;             // float[64]
-constexpr int kOffBars = kOffLfin + kRowsetRows * 4;       // uint64[24]
-constexpr int kOffMisc = kOffBars + 24 * 8;                // tmem base, abort flag
-constexpr int kSmemUsed = kOffMisc + 16;
+constexpr int kOffQ = kOffStage + kBlocks * kBlockBytes;  // 147456
+constexpr int kOffSlot = kOffQ + kBlocks * kQBlockBytes;  // 221184: int[2][128]
+constexpr int kOffMask = kOffSlot + 2 * kTileRows * 4;    // uint[2][128]
+constexpr int kOffMref = kOffMask + 2 * kTileRows * 4;    // float[64]
+constexpr int kOffAlpha = kOffMref + kRowsetRows * 4;     // float[64]
+constexpr int kOffRed = kOffAlpha + kRowsetRows * 4;      // float[8][32]
+constexpr int kOffLfin = kOffRed + 8 * 32 * 4;            // float[64]
+constexpr int kOffBars = kOffLfin + kRowsetRows * 4;      // uint64[24]
+constexpr int kOffMisc = kOffBars + 24 * 8;               // tmem base, abort flag, fixup flag, npending
+constexpr int kOffPending = kOffMisc + 16;                // int[2]: split row-sets this CTA merges
+constexpr int kSmemUsed = kOffPending + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for 1024-byte alignment
 
 // barrier indices
@@ -161,20 +168,29 @@ struct Schedule {
   }
 };
 
-// Query row n of row-set r -> (token, head), or token = -1 for a padding row.
-__device__ __forceinline__ void rowset_row(const AttnParams& p, int r, int n, int& tok, int& h) {
+// Query row n (< 64) of row-set r is row base + n of the [T*H, ...] q / out / lse arrays
+// and exists iff n < nvalid. Decode: base = t*H + 64*chunk. Prefill (H*G = 128): packed
+// row half*64 + n of group g is token g*G + (half*64 + n)/H, head (half*64 + n)%H, i.e.
+// row g*128 + half*64 + n; rows of members past the last token do not exist.
+struct RowsetRows {
+  long long base;
+  int nvalid;
+};
+
+__device__ __forceinline__ RowsetRows rowset_rows(const AttnParams& p, int r) {
+  RowsetRows rr;
   if (p.mode == kModeDecode) {
     const int t = r / p.hchunks;
-    h = (r - t * p.hchunks) * kRowsetRows + n;
-    tok = h < p.H ? t : -1;
+    const int hc = r - t * p.hchunks;
+    rr.base = static_cast<long long>(t) * p.H + hc * kRowsetRows;
+    rr.nvalid = min(kRowsetRows, p.H - hc * kRowsetRows);
   } else {
-    const int g = r >> 1;
-    const int packed = (r & 1) * kRowsetRows + n;
-    const int m = packed / p.H;
-    h = packed - m * p.H;
-    tok = g * p.G + m;
-    if (tok >= p.T) tok = -1;
+    const int g = r >> 1, half = r & 1;
+    rr.base = static_cast<long long>(g) * 128 + half * kRowsetRows;
+    const int members = min(p.G, p.T - g * p.G);
+    rr.nvalid = max(0, min(kRowsetRows, members * p.H - half * kRowsetRows));
   }
+  return rr;
 }
 
 __device__ __forceinline__ uint4 ldg_nc_v4(const void* ptr) {
@@ -195,76 +211,141 @@ __device__ __forceinline__ uint32_t e4m3x2_scaled_f16x2(uint32_t codes16, float 
   return pack_f16x2(f.x * scale, f.y * scale);
 }
 
-// One 128-row tile of an e4m3 cache. Row layout: 512 codes | 4 fp32 scales | 64 bf16 rope.
-// Each thread owns (row = ltid / 2, 32 of the 64 channels of every latent block) and four
-// 16-byte rope chunks: all of its raw bytes are loaded into registers first (so the next
-// tile's HBM reads overlap this tile's MMAs), then each block is converted to f16 (latent:
-// code * scale; rope: bf16 -> f16) into the swizzled operand layout as soon as the previous
-// tile's PV has released it.
-__device__ __forceinline__ void load_tile_fp8(const AttnParams& p, const int* slots, uint8_t* smem, int ltid,
-                                              uint32_t n, uint32_t bar0, int* status, volatile int* abort_flag) {
-  auto bar = [&](int i) -> uint32_t { return bar0 + 8u * static_cast<uint32_t>(i); };
-  const int row = ltid >> 1, hf = ltid & 1;
-  const int slot = slots[row];
-  uint4 raw[8][2];
-  uint4 rope[4];
-  float sc[4];
-  const int chunk = ltid & 7, row0 = ltid >> 3;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int sl = slots[row0 + 32 * k];
-    rope[k] = sl >= 0 ? ldg_nc_v4(p.kv + static_cast<long long>(sl) * p.row_stride + 528 + chunk * 16)
-                      : make_uint4(0, 0, 0, 0);
-  }
-  if (slot >= 0) {
-    const uint8_t* base = p.kv + static_cast<long long>(slot) * p.row_stride;
-#pragma unroll
-    for (int kb = 0; kb < 8; ++kb) {
-      raw[kb][0] = ldg_nc_v4(base + kb * 64 + hf * 32);
-      raw[kb][1] = ldg_nc_v4(base + kb * 64 + hf * 32 + 16);
-    }
-    const uint4 s4 = ldg_nc_v4(base + 512);
-    sc[0] = __uint_as_float(s4.x);
-    sc[1] = __uint_as_float(s4.y);
-    sc[2] = __uint_as_float(s4.z);
-    sc[3] = __uint_as_float(s4.w);
-  } else {
-#pragma unroll
-    for (int kb = 0; kb < 8; ++kb) raw[kb][0] = raw[kb][1] = make_uint4(0, 0, 0, 0);
-    sc[0] = sc[1] = sc[2] = sc[3] = 0.f;
-  }
-#pragma unroll
-  for (int kb = 0; kb < 8; ++kb) {
-    mbar_wait(bar(kBarEmptyV + (kb >> 1)), (n & 1u) ^ 1u, status, abort_flag);
-    const float s = sc[kb >> 1];
-    uint8_t* blk = smem + kOffStage + kb * kBlockBytes;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint4 r = raw[kb][h];
-      const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-      uint32_t o[8];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        o[2 * k] = e4m3x2_scaled_f16x2(w[k] & 0xFFFFu, s);
-        o[2 * k + 1] = e4m3x2_scaled_f16x2(w[k] >> 16, s);
-      }
-      // 16 codes -> 16 bf16 = output chunks 4*hf + 2*h and 4*hf + 2*h + 1
-      *reinterpret_cast<uint4*>(blk + sw128_offset(row, 4 * hf + 2 * h)) = make_uint4(o[0], o[1], o[2], o[3]);
-      *reinterpret_cast<uint4*>(blk + sw128_offset(row, 4 * hf + 2 * h + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
-    }
+// Publishes the cp.async blocks I..N-1 in order as their groups complete (block b was the
+// b-th of N groups committed, so it is done once at most N-1-b groups are pending).
+template <int I, int N>
+__device__ __forceinline__ void publish_cp_blocks(uint32_t bar0) {
+  if constexpr (I < N) {
+    cp_async_wait<N - 1 - I>();
     fence_proxy_async_smem();
-    mbar_arrive(bar(kBarFull + kb));
+    mbar_arrive(bar0 + 8u * static_cast<uint32_t>(kBarFull + I));
+    publish_cp_blocks<I + 1, N>(bar0);
   }
-  mbar_wait(bar(kBarEmptyR), (n & 1u) ^ 1u, status, abort_flag);
-  uint8_t* rblk = smem + kOffStage + 8 * kBlockBytes;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const uint4 r = rope[k];
-    *reinterpret_cast<uint4*>(rblk + sw128_offset(row0 + 32 * k, chunk)) =
-        make_uint4(bf16x2_to_f16x2(r.x), bf16x2_to_f16x2(r.y), bf16x2_to_f16x2(r.z), bf16x2_to_f16x2(r.w));
+}
+
+constexpr int kDeadEntry = -2147483647 - 1;  // an entry past the list's live count
+
+// Loader threads 0..127 read entry tile*128 + ltid of the row-set's list: a position (or a
+// slot when there is no block table) for decode, a union word (mask << 24 | slot) for
+// prefill. Done a tile ahead, so that resolving has a single dependent load left.
+__device__ __forceinline__ int fetch_entry(const AttnParams& p, const Seg& seg, int tile, int ltid) {
+  if (ltid >= kTileRows) return kDeadEntry;
+  const int e = tile * kTileRows + ltid;
+  if (e >= seg.len) return kDeadEntry;
+  if (p.mode == kModeDecode) return __ldg(p.topk + static_cast<long long>(seg.r / p.hchunks) * p.K + e);
+  return __ldg(p.enc + static_cast<long long>(seg.r >> 1) * p.list_stride + e);
+}
+
+// Turns a fetched entry into the slot / mask table entries of buffer `buf`.
+__device__ __forceinline__ void resolve_entry(const AttnParams& p, const Seg& seg, int raw, int ltid, int* slot_tab,
+                                              uint32_t* mask_tab, int& err) {
+  if (ltid >= kTileRows) return;
+  int slot = -1;
+  uint32_t mask = 0xFFFFFFFFu;
+  if (raw != kDeadEntry) {
+    if (p.mode == kModeDecode) {
+      const int t = seg.r / p.hchunks;
+      slot = resolve_position(raw, t, p.topk_len, p.req_of_token, p.block_table, p.num_reqs, p.max_blocks,
+                              p.seq_lens, p.page_size, p.num_pages, &err);
+    } else {
+      const uint32_t w = static_cast<uint32_t>(raw);
+      if (w != 0xFFFFFFFFu) {
+        const int sl = static_cast<int>(w & 0xFFFFFFu);
+        if (static_cast<long long>(sl) < p.num_slots) {
+          slot = sl;
+          mask = w >> 24;
+        } else {
+          err = 1;
+        }
+      }
+    }
   }
-  fence_proxy_async_smem();
-  mbar_arrive(bar(kBarFull + 8));
+  slot_tab[ltid] = slot;
+  mask_tab[ltid] = mask;
+}
+
+// Merge of a row-set split between CTAs c_lo .. c_lo + parts - 1 (stream-K): out = sum_s
+// exp(lse_s - lse) o_s, lse = ln sum_s exp(lse_s), over the parts' normalised partials.
+// Runs after the CTA's own tiles, when all 221 KB of stage and Q memory are free: all 512
+// threads copy every part's rows for a band of channels into shared memory with cp.async
+// (one round trip per band instead of one per load), 64 threads turn the parts' LSEs into
+// weights meanwhile, and the band is then combined from shared memory.
+constexpr int kMaxMergeParts = 128;
+constexpr int kMergeScratchBytes = kOffSlot - kOffStage;  // stage + Q memory
+
+__device__ void merge_rowset(const AttnParams& p, int r, uint8_t* scratch) {
+  const long long nt = p.tiles_per_rowset;
+  const long long first = r * nt;
+  const long long c_lo = streamk_owner(first, p.total_tiles, p.num_ctas);
+  const long long c_hi = streamk_owner(first + nt - 1, p.total_tiles, p.num_ctas);
+  const int parts = static_cast<int>(c_hi - c_lo + 1);
+  const RowsetRows rr = rowset_rows(p, r);
+  int* s_slot = reinterpret_cast<int*>(scratch);                      // [kMaxMergeParts]
+  float* s_w = reinterpret_cast<float*>(scratch + 4 * kMaxMergeParts);  // [parts][64]
+  const int buf_off = 4 * kMaxMergeParts + ((parts * kRowsetRows * 4 + 15) & ~15);
+  float* buf = reinterpret_cast<float*>(scratch + buf_off);            // [parts][64][band]
+  // channel band: widest power-of-two width (<= 512) whose parts x 64 rows fit the buffer
+  int lband = 9;  // log2(band)
+  while (lband > 2 && (static_cast<long long>(parts) * kRowsetRows * 4) << lband > kMergeScratchBytes - buf_off) --lband;
+  const int lvec = lband - 2;  // log2(16-byte vectors per row and band)
+  __syncthreads();             // scratch is free
+  for (int s = threadIdx.x; s < parts; s += blockDim.x) {
+    const long long c = c_lo + s;
+    s_slot[s] = static_cast<int>((streamk_lo(c, p.total_tiles, p.num_ctas) < first) ? 2 * c + 1 : 2 * c);
+  }
+  __syncthreads();
+  // every part's LSE of every row, fetched in parallel into s_w
+  for (int i = threadIdx.x; i < parts * kRowsetRows; i += blockDim.x)
+    s_w[i] = __ldcg(p.part_lse + s_slot[i >> 6] * kRowsetRows + (i & 63));
+  __syncthreads();
+  if (threadIdx.x < kRowsetRows) {  // LSEs -> merge weights, in place
+    const int row = threadIdx.x;
+    float mx = -CUDART_INF_F;
+    for (int s = 0; s < parts; ++s) mx = fmaxf(mx, s_w[s * kRowsetRows + row]);
+    float L = -CUDART_INF_F;
+    if (mx != -CUDART_INF_F) {
+      float tot = 0.f;
+      for (int s = 0; s < parts; ++s) tot += expf(s_w[s * kRowsetRows + row] - mx);
+      L = mx + logf(tot);
+    }
+    for (int s = 0; s < parts; ++s) {
+      const float ls = s_w[s * kRowsetRows + row];
+      s_w[s * kRowsetRows + row] = (L == -CUDART_INF_F || ls == -CUDART_INF_F) ? 0.f : expf(ls - L);
+    }
+    if (p.lse && row < rr.nvalid) p.lse[rr.base + row] = L;
+  }
+  const uint32_t sbuf = smem_u32(buf);
+  const int total = (parts * kRowsetRows) << lvec;
+  for (int c0 = 0; c0 < kVdim; c0 += 1 << lband) {
+    for (int i = threadIdx.x; i < total; i += blockDim.x) {
+      const int pr = i >> lvec;  // part * 64 + row
+      const int v = i & ((1 << lvec) - 1);
+      const float* src = p.part_o + (static_cast<long long>(s_slot[pr >> 6]) * kRowsetRows + (pr & 63)) * kVdim + c0 + 4 * v;
+      cp_async16(sbuf + 16u * static_cast<uint32_t>(i), src, (pr & 63) < rr.nvalid ? 16u : 0u);
+    }
+    cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    // combine: 4 channels (one 16-byte vector) per thread and step
+    for (int i = threadIdx.x; i < (kRowsetRows << lvec); i += blockDim.x) {
+      const int row = i >> lvec, v = i & ((1 << lvec) - 1);
+      if (row >= rr.nvalid) continue;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s = 0; s < parts; ++s) {
+        const float w = s_w[s * kRowsetRows + row];
+        const float4 x = reinterpret_cast<const float4*>(buf)[(((s * kRowsetRows) + row) << lvec) + v];
+        acc.x += w * x.x;
+        acc.y += w * x.y;
+        acc.z += w * x.z;
+        acc.w += w * x.w;
+      }
+      uint2 pk;
+      pk.x = pack_bf16x2(acc.x, acc.y);
+      pk.y = pack_bf16x2(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(p.out + (rr.base + row) * kVdim + c0 + 4 * v) = pk;
+    }
+    __syncthreads();
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_constant__ AttnParams p) {
@@ -282,13 +363,14 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
   const uint32_t bars = sbase + kOffBars;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  volatile int* fixup_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 8);
+  volatile int* npending = reinterpret_cast<volatile int*>(smem + kOffMisc + 12);
+  volatile int* pending = reinterpret_cast<volatile int*>(smem + kOffPending);
   auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const bool f16_mode = p.kv_dtype == SVT_KV_FP8_E4M3;
-  const uint32_t idesc_s = f16_mode ? kIdescS16 : kIdescS;
-  const uint32_t idesc_pv = f16_mode ? kIdescPV16 : kIdescPV;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kBlocks; ++i) mbar_init(bar(kBarFull + i), kLoaderThreads);
@@ -299,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
     mbar_init(bar(kBarQFull), kLoaderThreads);
     mbar_init(bar(kBarQEmpty), 1);
     *abort_flag = 0;
+    *npending = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) {
@@ -317,125 +400,197 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
   if (warp >= kLoaderWarp0) {
     // ------------------------------------------------------------------ loaders
     const int ltid = threadIdx.x - kLoaderWarp0 * 32;
+    const int chunk = ltid & 7;   // 16-byte chunk of a 128-byte block row
+    const int row0 = ltid >> 3;   // rows row0 + 32k, k < 4
     uint32_t n = 0, qn = 0;
     int err = 0;
+    uint32_t resolved = 0xFFFFFFFFu;  // tile counter whose slots are already in their buffer
     while (sched.next(seg)) {
       if (seg.ntile == 0) continue;
-      // Q^T of the row-set: 64 rows x 72 chunks of 16 bytes, zero rows for padding
+      const RowsetRows rr = rowset_rows(p, seg.r);
+      // Q^T of the row-set: 64 rows x 72 chunks, zero rows for padding. bf16: cp.async,
+      // published after the first tile's cp.async blocks are issued; f16 mode: converted.
       mbar_wait(bar(kBarQEmpty), (qn & 1u) ^ 1u, p.status, abort_flag);
       for (int idx = ltid; idx < kRowsetRows * 72; idx += kLoaderThreads) {
         const int row = idx / 72, c = idx - row * 72;
-        int tok, h;
-        rowset_row(p, seg.r, row, tok, h);
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q);
-        uint32_t bytes = 0;
-        if (tok >= 0) {
-          src += (static_cast<long long>(tok) * p.H + h) * (kRow * 2) + c * 16;
-          bytes = 16;
-        }
+        const bool valid = row < rr.nvalid;
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(p.q) + (valid ? (rr.base + row) * (kRow * 2) + c * 16 : 0);
         const uint32_t off = (c >> 3) * kQBlockBytes + sw128_offset(row, c & 7);
         if (f16_mode) {
-          const uint4 v = bytes ? ldg_nc_v4(src) : make_uint4(0, 0, 0, 0);
+          const uint4 v = valid ? ldg_nc_v4(src) : make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4*>(smem + kOffQ + off) =
               make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
         } else {
-          cp_async16(s_q + off, src, bytes);
+          cp_async16(s_q + off, src, valid ? 16u : 0u);
         }
       }
       cp_async_commit();
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      mbar_arrive(bar(kBarQFull));
+      bool q_published = false;
+      if (f16_mode) {
+        fence_proxy_async_smem();
+        mbar_arrive(bar(kBarQFull));
+        q_published = true;
+      }
       ++qn;
 
       for (int i = 0; i < seg.ntile; ++i, ++n) {
         const int buf = n & 1;
-        const int tile = seg.tb + i;
-        // resolve the tile's 128 entries
-        if (ltid < kTileRows) {
-          const int e = tile * kTileRows + ltid;
-          int slot = -1;
-          uint32_t mask = 0xFFFFFFFFu;
-          if (e < seg.len) {
-            if (p.mode == kModeDecode) {
-              const int t = seg.r / p.hchunks;
-              slot = resolve_position(p.topk[static_cast<long long>(t) * p.K + e], t, p.topk_len, p.req_of_token,
-                                      p.block_table, p.num_reqs, p.max_blocks, p.seq_lens, p.page_size,
-                                      p.num_pages, &err);
-            } else {
-              const uint32_t w = static_cast<uint32_t>(p.enc[static_cast<long long>(seg.r >> 1) * p.list_stride + e]);
-              if (w != 0xFFFFFFFFu) {
-                const int s = static_cast<int>(w & 0xFFFFFFu);
-                if (static_cast<long long>(s) < p.num_slots) {
-                  slot = s;
-                  mask = w >> 24;
-                } else {
-                  err = 1;
-                }
-              }
-            }
-          }
-          slot_tab[buf * kTileRows + ltid] = slot;
-          mask_tab[buf * kTileRows + ltid] = mask;
+        int* slots = slot_tab + buf * kTileRows;
+        if (resolved != n) {
+          resolve_entry(p, seg, fetch_entry(p, seg, seg.tb + i, ltid), ltid, slots, mask_tab + buf * kTileRows, err);
+          named_bar_sync(kNamedBarLoaders, kLoaderThreads);
         }
-        named_bar_sync(kNamedBarLoaders, kLoaderThreads);
-        const int chunk = ltid & 7;
-        const int row0 = ltid >> 3;
-        if (p.kv_dtype == SVT_KV_FP8_E4M3) {
-          load_tile_fp8(p, slot_tab + buf * kTileRows, smem, ltid, n, bar(0), p.status, abort_flag);
-          continue;
-        }
-        for (int kb = 0; kb < kBlocks; ++kb) {
-          const int eb = kb < 8 ? kBarEmptyV + (kb >> 1) : kBarEmptyR;
-          mbar_wait(bar(eb), (n & 1u) ^ 1u, p.status, abort_flag);
-          const uint32_t dst_blk = s_stage + kb * kBlockBytes;
+        // The next tile's slots go into the other buffer, last read by the softmax of tile
+        // n-1; that softmax finished before PV(n-1) was issued, and PV(n-1) has completed
+        // once the first EMPTY wait below returns.
+        const bool ahead = i + 1 < seg.ntile;
+        const int raw_next = ahead ? fetch_entry(p, seg, seg.tb + i + 1, ltid) : kDeadEntry;
+        if (!f16_mode) {
+          uint4 reg[kBlocks - kRegBlock0][4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            const int row = row0 + 32 * k;
-            const int slot = slot_tab[buf * kTileRows + row];
-            const uint8_t* src = p.kv + kb * 128 + chunk * 16;
-            uint32_t bytes = 0;
-            if (slot >= 0) {
-              src += static_cast<long long>(slot) * p.row_stride;
-              bytes = 16;
-            }
-            cp_async16(dst_blk + sw128_offset(row, chunk), src, bytes);
+            const int slot = slots[row0 + 32 * k];
+            const uint8_t* src = p.kv + static_cast<long long>(slot < 0 ? 0 : slot) * p.row_stride + chunk * 16;
+#pragma unroll
+            for (int b = 0; b < kBlocks - kRegBlock0; ++b)
+              reg[b][k] = slot >= 0 ? ldg_nc_v4(src + (kRegBlock0 + b) * 128) : make_uint4(0, 0, 0, 0);
           }
-          cp_async_commit();
+#pragma unroll
+          for (int kb = 0; kb < kRegBlock0; ++kb) {
+            mbar_wait(bar(kBarEmptyV + (kb >> 1)), (n & 1u) ^ 1u, p.status, abort_flag);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int row = row0 + 32 * k;
+              const int slot = slots[row];
+              const uint8_t* src = p.kv + static_cast<long long>(slot < 0 ? 0 : slot) * p.row_stride + kb * 128 +
+                                   chunk * 16;
+              cp_async16(s_stage + kb * kBlockBytes + sw128_offset(row, chunk), src, slot >= 0 ? 16u : 0u);
+            }
+            cp_async_commit();
+          }
+          if (!q_published) {
+            cp_async_wait<kRegBlock0>();
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kBarQFull));
+            q_published = true;
+          }
+#pragma unroll
+          for (int b = 0; b < kBlocks - kRegBlock0; ++b) {
+            const int kb = kRegBlock0 + b;
+            mbar_wait(bar(kb < 8 ? kBarEmptyV + (kb >> 1) : kBarEmptyR), (n & 1u) ^ 1u, p.status, abort_flag);
+            uint8_t* blk = smem + kOffStage + kb * kBlockBytes;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) *reinterpret_cast<uint4*>(blk + sw128_offset(row0 + 32 * k, chunk)) = reg[b][k];
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kBarFull + kb));
+          }
+          // resolve the next tile while the cp.async blocks land
+          if (ahead) {
+            resolve_entry(p, seg, raw_next, ltid, slot_tab + (buf ^ 1) * kTileRows, mask_tab + (buf ^ 1) * kTileRows,
+                          err);
+            resolved = n + 1;
+          }
+          publish_cp_blocks<0, kRegBlock0>(bar(0));
+          if (ahead) named_bar_sync(kNamedBarLoaders, kLoaderThreads);
+        } else {
+          // e4m3: thread owns (row = ltid / 2, 32 channels of every latent block) and four
+          // 16-byte rope chunks; all raw bytes are in registers before any block is written.
+          const int row = ltid >> 1, hf = ltid & 1;
+          const int slot = slots[row];
+          uint4 raw[8][2];
+          uint4 rope[4];
+          float sc[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int sl = slots[row0 + 32 * k];
+            rope[k] = sl >= 0 ? ldg_nc_v4(p.kv + static_cast<long long>(sl) * p.row_stride + 528 + chunk * 16)
+                              : make_uint4(0, 0, 0, 0);
+          }
+          if (slot >= 0) {
+            const uint8_t* base = p.kv + static_cast<long long>(slot) * p.row_stride;
+#pragma unroll
+            for (int kb = 0; kb < 8; ++kb) {
+              raw[kb][0] = ldg_nc_v4(base + kb * 64 + hf * 32);
+              raw[kb][1] = ldg_nc_v4(base + kb * 64 + hf * 32 + 16);
+            }
+            const uint4 s4 = ldg_nc_v4(base + 512);
+            sc[0] = __uint_as_float(s4.x);
+            sc[1] = __uint_as_float(s4.y);
+            sc[2] = __uint_as_float(s4.z);
+            sc[3] = __uint_as_float(s4.w);
+          } else {
+#pragma unroll
+            for (int kb = 0; kb < 8; ++kb) raw[kb][0] = raw[kb][1] = make_uint4(0, 0, 0, 0);
+            sc[0] = sc[1] = sc[2] = sc[3] = 0.f;
+          }
+#pragma unroll
+          for (int kb = 0; kb < 8; ++kb) {
+            mbar_wait(bar(kBarEmptyV + (kb >> 1)), (n & 1u) ^ 1u, p.status, abort_flag);
+            if (kb == 0 && ahead) {
+              resolve_entry(p, seg, raw_next, ltid, slot_tab + (buf ^ 1) * kTileRows,
+                            mask_tab + (buf ^ 1) * kTileRows, err);
+              resolved = n + 1;
+            }
+            const float s = sc[kb >> 1];
+            uint8_t* blk = smem + kOffStage + kb * kBlockBytes;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint4 r = raw[kb][h];
+              const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+              uint32_t o[8];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                o[2 * k] = e4m3x2_scaled_f16x2(w[k] & 0xFFFFu, s);
+                o[2 * k + 1] = e4m3x2_scaled_f16x2(w[k] >> 16, s);
+              }
+              // 16 codes -> 16 f16 = output chunks 4*hf + 2*h and 4*hf + 2*h + 1
+              *reinterpret_cast<uint4*>(blk + sw128_offset(row, 4 * hf + 2 * h)) = make_uint4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<uint4*>(blk + sw128_offset(row, 4 * hf + 2 * h + 1)) =
+                  make_uint4(o[4], o[5], o[6], o[7]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(kBarFull + kb));
+          }
+          mbar_wait(bar(kBarEmptyR), (n & 1u) ^ 1u, p.status, abort_flag);
+          uint8_t* rblk = smem + kOffStage + 8 * kBlockBytes;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint4 r = rope[k];
+            *reinterpret_cast<uint4*>(rblk + sw128_offset(row0 + 32 * k, chunk)) =
+                make_uint4(bf16x2_to_f16x2(r.x), bf16x2_to_f16x2(r.y), bf16x2_to_f16x2(r.z), bf16x2_to_f16x2(r.w));
+          }
+          fence_proxy_async_smem();
+          mbar_arrive(bar(kBarFull + 8));
+          if (ahead) named_bar_sync(kNamedBarLoaders, kLoaderThreads);
         }
-        // publish the blocks in order as they land
-        cp_async_wait<8>(); fence_proxy_async_smem(); mbar_arrive(bar(kBarFull + 0));
-        cp_async_wait<7>(); fence_proxy_async_smem(); mbar_arrive(bar(kBarFull + 1));
-        cp_async_wait<6>(); fence_proxy_async_smem(); mbar_arrive(bar(kBarFull + 2));
-        cp_async_wait<5>(); fence_proxy_async_smem(); mbar_arrive(bar(kBarFull + 3));
-        cp_async_wait<4>(); fence_proxy_async_smem(); mbar_arrive(bar(kBarFull + 4));
-        cp_async_wait<3>(); fence_proxy_async_smem(); mbar_arrive(bar(kBarFull + 5));
-        cp_async_wait<2>(); fence_proxy_async_smem(); mbar_arrive(bar(kBarFull + 6));
-        cp_async_wait<1>(); fence_proxy_async_smem(); mbar_arrive(bar(kBarFull + 7));
-        cp_async_wait<0>(); fence_proxy_async_smem(); mbar_arrive(bar(kBarFull + 8));
       }
     }
     cp_async_wait_all();
     if (__any_sync(0xffffffffu, err) && lane == 0) atomicOr(p.status, SVT_DEV_ERR_INDEX_RANGE);
   } else {
     // ------------------------------------------------------------------ softmax + epilogue
-    const int q = warp & 3;        // TMEM lane quadrant: KV rows 32q .. 32q+31
-    const int ch = warp >> 2;      // column half: query rows 32ch .. 32ch+31
+    const int q = warp & 3;    // TMEM lane quadrant: KV rows 32q .. 32q+31
+    const int ch = warp >> 2;  // column half: query rows 32ch .. 32ch+31
     const int kvrow = 32 * q + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
     uint32_t n = 0, qn = 0;
     const bool issuer = (warp == 0 && lane == 0);
     const uint32_t s_p = s_stage + 8 * kBlockBytes;
-    // S^T = K_tile . Q^T for tile number `tn`; `last` releases Q^T after it.
+    const uint32_t idesc_s = f16_mode ? kIdescS16 : kIdescS;
+    const uint32_t idesc_pv = f16_mode ? kIdescPV16 : kIdescPV;
+    // S^T = K_tile . Q^T for tile number `tn` (register-staged blocks first); `last`
+    // releases Q^T after it.
     auto issue_s = [&](uint32_t tn, bool last) {
-      for (int kb = 0; kb < kBlocks; ++kb) {
+#pragma unroll 1
+      for (int j = 0; j < kBlocks; ++j) {
+        const int kb = f16_mode ? j : (j < kBlocks - kRegBlock0 ? kRegBlock0 + j : j - (kBlocks - kRegBlock0));
         mbar_wait(bar(kBarFull + kb), tn & 1u, p.status, abort_flag);
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
           const uint64_t a = smem_desc_sw128(s_stage + kb * kBlockBytes + ks * 32, 16, 1024);
           const uint64_t b = smem_desc_sw128(s_q + kb * kQBlockBytes + ks * 32, 16, 1024);
-          umma_f16(tmem + kTmemS, a, b, idesc_s, (kb | ks) != 0);
+          umma_f16(tmem + kTmemS, a, b, idesc_s, (j | ks) != 0);
         }
       }
       umma_commit(bar(kBarSFull));
@@ -475,6 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
         tc_fence_after();
         issue_s(n, seg.ntile == 1);
       }
+      __syncwarp();  // the rest of warp 0 waits here, not spinning beside the issuing lane
 
       for (int i = 0; i < seg.ntile; ++i, ++n) {
         mbar_wait(bar(kBarSFull), n & 1u, p.status, abort_flag);
@@ -549,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
             tmem_st_wait();
           }
         }
-        // P^T row (this KV row, my 32 query columns) as bf16, into the rope block's space
+        // P^T row (this KV row, my 32 query columns) into the rope block's space
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
@@ -574,6 +730,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
           issue_pv(i > 0);
           if (i + 1 < seg.ntile) issue_s(n + 1, i + 2 == seg.ntile);
         }
+        __syncwarp();
       }
       if (seg.ntile > 0) ++qn;
 
@@ -595,6 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
       }
       red[warp * 32 + lane] = lpart[0];
       named_bar_sync(kNamedBarSoftmax, kSoftmaxThreads);
+      const RowsetRows rr = rowset_rows(p, seg.r);
       if (q == 0) {
         const int col = 32 * ch + lane;
         const float l = red[(4 * ch) * 32 + lane] + red[(4 * ch + 1) * 32 + lane] + red[(4 * ch + 2) * 32 + lane] +
@@ -602,11 +760,9 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
         lfin[col] = l;
         const float lse2 = (l > 0.f) ? (m_ref[col] + __log2f(l)) : -CUDART_INF_F;
         const float lse_nat = lse2 * 0.69314718055994530942f;
-        int tok, h;
-        rowset_row(p, seg.r, col, tok, h);
-        if (tok >= 0) {
+        if (col < rr.nvalid) {
           if (seg.full) {
-            if (p.lse) p.lse[static_cast<long long>(tok) * p.H + h] = lse_nat;
+            if (p.lse) p.lse[rr.base + col] = lse_nat;
           } else {
             p.part_lse[static_cast<long long>(seg.slot) * kRowsetRows + col] = lse_nat;
           }
@@ -619,6 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
         const float l = lfin[32 * ch + c];
         inv[c] = l > 0.f ? 1.0f / l : 0.f;
       }
+      const int nv = rr.nvalid - 32 * ch;  // my columns c < nv exist
 #pragma unroll 1
       for (int mb = 0; mb < 4; ++mb) {
         uint32_t o[32];
@@ -630,21 +787,40 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
           for (int c = 0; c < 32; ++c) o[c] = 0u;
         }
         const int chan = 128 * mb + 32 * q + lane;
+        if (seg.full) {
+          uint16_t* dst = p.out + (rr.base + 32 * ch) * kVdim + chan;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          int tok, h;
-          rowset_row(p, seg.r, 32 * ch + c, tok, h);
-          if (tok < 0) continue;
-          const float v = __uint_as_float(o[c]) * inv[c];
-          if (seg.full) {
-            const uint32_t b = pack_bf16x2(v, 0.f) & 0xFFFFu;
-            p.out[(static_cast<long long>(tok) * p.H + h) * kVdim + chan] = static_cast<uint16_t>(b);
-          } else {
-            p.part_o[(static_cast<long long>(seg.slot) * kRowsetRows + 32 * ch + c) * kVdim + chan] = v;
+          for (int c = 0; c < 32; ++c) {
+            if (c < nv) dst[c * kVdim] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(o[c]) * inv[c], 0.f));
+          }
+        } else {
+          float* dst = p.part_o + (static_cast<long long>(seg.slot) * kRowsetRows + 32 * ch) * kVdim + chan;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            if (c < nv) dst[c * kVdim] = __uint_as_float(o[c]) * inv[c];
           }
         }
       }
       tc_fence_before();
+      if (!seg.full) {
+        // Stream-K: the last CTA to finish a part of this row-set merges all parts.
+        __threadfence();
+        named_bar_sync(kNamedBarSoftmax, kSoftmaxThreads);
+        const long long nt = p.tiles_per_rowset;
+        const long long c_lo = streamk_owner(seg.r * nt, p.total_tiles, p.num_ctas);
+        const long long c_hi = streamk_owner(seg.r * nt + nt - 1, p.total_tiles, p.num_ctas);
+        const int parts = static_cast<int>(c_hi - c_lo + 1);
+        if (threadIdx.x == 0) *fixup_flag = (atomicAdd(p.counters + c_lo, 1) == parts - 1);
+        named_bar_sync(kNamedBarSoftmax, kSoftmaxThreads);
+        if (*fixup_flag) {
+          // merged after this CTA's last tile, by all of its threads
+          if (threadIdx.x == 0) {
+            pending[*npending] = seg.r;
+            *npending = *npending + 1;
+            p.counters[c_lo] = 0;  // ready for the next launch
+          }
+        }
+      }
       named_bar_sync(kNamedBarSoftmax, kSoftmaxThreads);
     }
   }
@@ -653,6 +829,11 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+  const int np = *npending;
+  if (np > 0) {
+    __threadfence();
+    for (int k = 0; k < np; ++k) merge_rowset(p, pending[k], smem + kOffStage);
+  }
 }
 
 }  // namespace

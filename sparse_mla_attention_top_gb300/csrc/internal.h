@@ -15,6 +15,11 @@ constexpr int kVdim = 512;         // V is the first 512 columns
 constexpr int kRowBytesBf16 = 1152;
 constexpr int kRowBytesFp8 = 656;  // 512 e4m3 | 4 fp32 scales | 64 bf16 rope
 constexpr size_t kStatusBytes = 256;  // status header at the start of every workspace
+// Split-merge counters follow the header at a fixed place, so that every call (whatever its
+// shape) uses the same bytes for them and nothing else ever writes there; each call leaves
+// them zero. One counter per CTA bounds the CTAs of a split decode.
+constexpr size_t kCounterBytes = 65536;
+constexpr int kMaxCtas = static_cast<int>(kCounterBytes / sizeof(int));
 
 // Attention kernel geometry (the tcgen05 tile): a tile is 128 KV rows (the MMA M), a
 // row-set is up to 64 query rows sharing one KV list (the MMA N).
@@ -64,6 +69,7 @@ struct AttnParams {
   int num_ctas;
   float* part_o;    // [2 * num_ctas, 64, 512] fp32 (stream-K partial segments)
   float* part_lse;  // [2 * num_ctas, 64]
+  int* counters;    // [num_ctas] parts finished per split row-set, indexed by its first CTA
   int* status;
 };
 
@@ -89,7 +95,6 @@ cudaError_t launch_merge_splits(const float* o_part, const float* lse_part, int 
                                 uint16_t* out, float* lse, cudaStream_t stream);
 
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
-cudaError_t launch_streamk_merge(const AttnParams& p, cudaStream_t stream);
 int attention_smem_bytes();
 
 }  // namespace svt

@@ -77,33 +77,6 @@ __global__ void __launch_bounds__(256) merge_splits_kernel(const float* __restri
       [&](int s) { return o_part + (s * rows + r) * kVdim; }, out + r * kVdim, lse ? lse + r : nullptr);
 }
 
-// Stream-K merge for the attention kernel: row-set r's tiles were spread over CTAs
-// owner(r*n) .. owner(r*n + n - 1); each wrote a partial into slot 2c (its first segment)
-// or 2c + 1 (its last one). Row-sets covered by a single CTA were written directly.
-__global__ void __launch_bounds__(256) streamk_merge_kernel(AttnParams p) {
-  const int r = blockIdx.x;
-  const long long n = p.tiles_per_rowset;
-  const long long first = r * n, last = r * n + n - 1;
-  const long long c_lo = streamk_owner(first, p.total_tiles, p.num_ctas);
-  const long long c_hi = streamk_owner(last, p.total_tiles, p.num_ctas);
-  if (c_lo == c_hi) return;
-  const int S = static_cast<int>(c_hi - c_lo + 1);
-  const int t = r / p.hchunks, hc = r - t * p.hchunks;
-  for (int row = threadIdx.x >> 5; row < kRowsetRows; row += 8) {
-    const int h = hc * kRowsetRows + row;
-    if (h >= p.H) break;
-    auto slot_of = [&](int s) -> long long {
-      const long long c = c_lo + s;
-      return (streamk_lo(c, p.total_tiles, p.num_ctas) < first) ? 2 * c + 1 : 2 * c;
-    };
-    merge_row(
-        S, [&](int s) { return p.part_lse[slot_of(s) * kRowsetRows + row]; },
-        [&](int s) { return p.part_o + (slot_of(s) * kRowsetRows + row) * kVdim; },
-        p.out + (static_cast<long long>(t) * p.H + h) * kVdim,
-        p.lse ? p.lse + static_cast<long long>(t) * p.H + h : nullptr);
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_merge_splits(const float* o_part, const float* lse_part, int S, long long rows, int /*H_rows*/,
@@ -111,12 +84,6 @@ cudaError_t launch_merge_splits(const float* o_part, const float* lse_part, int 
   if (rows == 0) return cudaSuccess;
   const long long blocks = (rows + 7) / 8;
   merge_splits_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(o_part, lse_part, S, rows, out, lse);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_streamk_merge(const AttnParams& p, cudaStream_t stream) {
-  if (p.num_rowsets == 0) return cudaSuccess;
-  streamk_merge_kernel<<<p.num_rowsets, 256, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -66,8 +66,9 @@ __global__ void union_kernel(const int32_t* __restrict__ slots, const int32_t* _
   // 2. bitonic sort, ascending; each thread takes pairs (i, i + j)
   for (int k = 2; k <= npow; k <<= 1) {
     for (int j = k >> 1; j > 0; j >>= 1) {
+      const int lj = __ffs(j) - 1;
       for (int p = tid; p < (npow >> 1); p += nthreads) {
-        const int i = ((p / j) * (j << 1)) + (p % j);
+        const int i = ((p >> lj) << (lj + 1)) | (p & (j - 1));
         const int ixj = i + j;
         const uint32_t a = keys[i], b = keys[ixj];
         const bool up = (i & k) == 0;
@@ -136,7 +137,7 @@ cudaError_t launch_union(const int32_t* slots, const int32_t* topk_len, int T, i
   if (groups == 0) return cudaSuccess;
   const int npow = next_pow2(G * K);
   int threads = npow / 4;
-  threads = threads < 64 ? 64 : (threads > 1024 ? 1024 : threads);
+  threads = threads < 64 ? 64 : (threads > 512 ? 512 : threads);
   const size_t smem = union_smem_bytes(G, K);
   cudaError_t e = cudaFuncSetAttribute(union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        static_cast<int>(smem));

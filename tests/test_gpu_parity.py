@@ -312,3 +312,19 @@ def test_prefill_membership_bit_negative_control(S, dev, ws):
     out2, lse2 = S.sparse_mla_prefill_grouped(to_dev(w.q_bits, dev), w.G, kv_of(w, dev), e, lens, w.K, w.scale, ws=ws)
     assert float((lse2[1] - lse[1]).abs().max()) > LSE_TOL
     assert torch.equal(out2[0], out[0])
+
+
+def test_workspace_reuse_across_shapes_and_repeats(S, dev):
+    # One workspace serves calls of different shapes back to back; the split-merge counters
+    # must start at zero every time (regression: they once shared bytes with partials).
+    ws = S.Workspace(dev)
+    big = W.make_decode(80, T=5, H=64, K=700, ctx_lo=800, ctx_hi=3000, page_size=64)
+    small = W.make_decode(81, T=4, H=16, K=256, ctx_lo=300, ctx_hi=900, page_size=16)
+    ref_b, ref_lse_b, _ = oracle_decode(big)
+    ref_s, ref_lse_s, _ = oracle_decode(small)
+    for w, ref, ref_lse in [(big, ref_b, ref_lse_b), (small, ref_s, ref_lse_s), (big, ref_b, ref_lse_b),
+                            (small, ref_s, ref_lse_s)]:
+        for splits in (0, 3):
+            out, lse = gpu_decode(S, w, dev, ws, num_splits=splits)
+            compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    assert ws.read_status() == 0
