@@ -39,7 +39,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of the decode attention kernel,
 # keyed by the sha256 of the attention source it was measured on (stale -> null).
-TRAFFIC_BY_SOURCE = {}
+TRAFFIC_BY_SOURCE = {
+    # 16-query decode capture (profiles/decode_bf16_attention_ncu.md): 39.22 MB read + 0.56 MB
+    # written, scaled by 64/16 queries to the benchmark's launch
+    "22b323542208fcb1": 4 * (39.224064e6 + 0.557824e6),
+}
 
 
 def parse():
