@@ -143,6 +143,33 @@ SVT_API svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t 
                                  size_t ws_bytes, svt_stream_t stream);
 
 /*
+ * Sparse MLA decode without a caller workspace. The pages have no counterpart for this entry
+ * point; it exists for callers that cannot call cudaMalloc at all, such as a plugin inside a
+ * host application that owns every byte of device memory through its own allocator, or code
+ * that must never trigger the device-wide synchronisation a cudaMalloc can cause.
+ *
+ * Same arguments and results as svt_sparse_mla_decode, without ws / ws_bytes. The scratch it
+ * needs lives in an 8 MiB array inside the library that every GPU loading the library holds
+ * until the process exits. That bounds it: one CTA per query (num_splits = 1) works for any
+ * batch (256 bytes of scratch); a split decode works while
+ * svt_sparse_mla_decode_workspace_size(T, H, K, num_splits) <= 8 MiB (up to 31 CTAs with
+ * partial results). Anything larger returns SVT_ERR_WORKSPACE before any work is enqueued.
+ *   status_out  optional device int32: receives this call's device status bits (the
+ *               SVT_DEV_ERR_* values) when the call's kernels have run; NULL to skip.
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ * with that device current; make that first call before any stream capture. Every call shares
+ * the one array: the call clears its status word and counters first, so calls that follow one
+ * another on a stream are independent, but calls that overlap on the GPU (other streams or
+ * threads) race on it. It calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+SVT_API svt_status svt_sparse_mla_decode_noalloc(const void* q_bf16, int32_t T, int32_t H, const svt_kv_cache* kv,
+                                                 const int32_t* block_table, int32_t num_reqs, int32_t max_blocks,
+                                                 const int32_t* req_of_token, const int32_t* seq_lens,
+                                                 const int32_t* topk, int32_t K, const int32_t* topk_len,
+                                                 float softmax_scale, void* out_bf16, float* lse, int32_t num_splits,
+                                                 int32_t* status_out, svt_stream_t stream);
+
+/*
  * Group union (vLLM PR #63104, Details / Changes: each group of G consecutive queries gets
  * the sorted union of its members' converted KV rows; Tests: empty groups, entries past a
  * query's count, negative rows and rows up to the 24-bit limit; each member keeps to its

@@ -108,6 +108,16 @@ size_t decode_ws_bytes(const DecodePlan& d) {
 
 }  // namespace
 
+namespace svt {
+svt_status set_last_error(svt_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return st;
+}
+}  // namespace svt
+
 extern "C" {
 
 const char* svt_last_error_string(void) { return g_err; }

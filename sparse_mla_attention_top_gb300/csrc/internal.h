@@ -95,6 +95,9 @@ cudaError_t launch_merge_splits(const float* o_part, const float* lse_part, int 
                                 uint16_t* out, float* lse, cudaStream_t stream);
 
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
+
+// Records the message svt_last_error_string() returns on this thread and passes `st` back.
+svt_status set_last_error(svt_status st, const char* fmt, ...);
 int attention_smem_bytes();
 
 }  // namespace svt

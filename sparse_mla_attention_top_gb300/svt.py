@@ -32,6 +32,7 @@ EXPORTED = [
     "svt_resolve_topk_slots", "svt_sparse_mla_decode_workspace_size", "svt_sparse_mla_decode",
     "svt_build_group_union_workspace_size", "svt_build_group_union",
     "svt_sparse_mla_prefill_grouped_workspace_size", "svt_sparse_mla_prefill_grouped", "svt_merge_splits",
+    "svt_sparse_mla_decode_noalloc",
 ]
 
 
@@ -75,6 +76,8 @@ def lib():
         L.svt_sparse_mla_prefill_grouped.argtypes = [P, i32, i32, i32, ctypes.POINTER(_KV), P, P, i32, f32, P, P, P,
                                                      sz, P]
         L.svt_merge_splits.argtypes = [P, P, i32, i32, i32, P, P, P]
+        L.svt_sparse_mla_decode_noalloc.argtypes = [P, i32, i32, ctypes.POINTER(_KV), P, i32, i32, P, P, P, i32, P, f32,
+                                                    P, P, i32, P, P]
         _lib = L
     return _lib
 
