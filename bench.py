@@ -70,34 +70,104 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+    """SM clock and clock-event (throttle) reasons, sampled every 0.2 ms while running.
 
+    Reads through NVML (the driver's libnvidia-ml, read-only queries) so that even a timed
+    region of a few milliseconds gets samples; falls back to nvidia-smi at 200 ms when NVML
+    cannot be loaded."""
+
+    # nvmlClocksEventReason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index: int):
-        self.index = index
+    def __init__(self, cuda_index: int):
+        self.cuda_index = cuda_index
+        self.samples = []  # (sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self.thread = None
         self.proc = None
         self.lines = []
-        self.thread = None
+        self.nvml = None
+        self.handle = None
+
+    def _nvml_open(self) -> bool:
+        import ctypes
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return False
+            h = ctypes.c_void_p()
+            ok = False
+            try:
+                import torch
+                bus = getattr(torch.cuda.get_device_properties(self.cuda_index), "pci_bus_id", None)
+                if isinstance(bus, int):
+                    bus = None
+                if bus:
+                    ok = nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) == 0
+            except Exception:
+                ok = False
+            if not ok:
+                vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+                idx = int(vis.split(",")[self.cuda_index]) if vis and vis.split(",")[0].isdigit() else self.cuda_index
+                ok = nv.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(h)) == 0
+            if not ok:
+                return False
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self.nvml, self.handle = nv, h
+            return True
+        except OSError:
+            return False
+
+    def _nvml_loop(self):
+        import ctypes
+        nv, h = self.nvml, self.handle
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and get_reasons(h, ctypes.byref(rs)) == 0:
+                self.samples.append((float(clk.value), int(rs.value)))
+            time.sleep(0.0002)
 
     def start(self):
+        if self._nvml_open():
+            self.thread = threading.Thread(target=self._nvml_loop, daemon=True)
+            self.thread.start()
+            return
         try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.cuda_index}", f"--query-gpu={self.QUERY}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True, bufsize=1)
         except (FileNotFoundError, OSError):
             self.proc = None
             return
-        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread = threading.Thread(target=self._read_smi, daemon=True)
         self.thread.start()
 
-    def _read(self):
+    def _read_smi(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
     def stop(self):
+        if self.nvml is not None:
+            self._stop.set()
+            self.thread.join(timeout=2)
+            if not self.samples:
+                return None
+            reasons = set()
+            for _, r in self.samples:
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        reasons.add(name)
+            return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                    "reasons": sorted(reasons), "samples": len(self.samples), "source": "nvml, 0.2 ms"}
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -124,22 +194,22 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi, 200 ms"}
 
 
 def dist_setup(args):
+    """Rank layout from torchrun's environment; NCCL on GPUs, gloo where there is no CUDA."""
     import torch
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local if world > 1 else 0)
     if world > 1:
         import torch.distributed as dist
 
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
-    else:
-        torch.cuda.set_device(0)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     return world, rank, local
 
 
@@ -156,9 +226,16 @@ def max_over_ranks(x: float, world: int) -> float:
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_throughput(units_per_rank: int, ms_max: float, world: int) -> float:
+    """Whole-job units per second: every rank processes its own copy of the workload (weak
+    scaling), and the job takes as long as its slowest rank."""
+    return units_per_rank * world / (ms_max / 1000.0)
 
 
 def source_hash() -> str:
@@ -283,7 +360,7 @@ def main():
     ms = max_over_ranks(statistics.mean(times), world)
     ms_med = max_over_ranks(statistics.median(times), world)
     nb = decode_bytes(w)
-    value = w.T * world / (ms / 1000.0)
+    value = replica_throughput(w.T, ms, world)
     achieved = nb["algorithmic"] / (ms / 1000.0) / 1e9
     th = source_hash()
 
@@ -311,7 +388,7 @@ def main():
         et = time_steps(e2e_step, args.steps, flush, stream)
         barrier(world)
         ems = max_over_ranks(statistics.mean(et), world)
-        e2e = {"value": w.T * world / (ems / 1000.0), "unit": UNIT, "ms_per_step": ems,
+        e2e = {"value": replica_throughput(w.T, ems, world), "unit": UNIT, "ms_per_step": ems,
                "h2d_bytes_per_step": q_h.numel() * 2 + topk_h.numel() * 4,
                "d2h_bytes_per_step": out_h.numel() * 2 + lse_h.numel() * 4}
 

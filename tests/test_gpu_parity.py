@@ -328,3 +328,77 @@ def test_workspace_reuse_across_shapes_and_repeats(S, dev):
             out, lse = gpu_decode(S, w, dev, ws, num_splits=splits)
             compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
     assert ws.read_status() == 0
+
+
+# ------------------------------------------------------------- e4m3 grouped prefill
+
+@pytest.mark.parametrize("H,G,T", [(64, 2, 11), (16, 8, 29)])
+def test_prefill_fp8_cache_matches_oracle(S, dev, ws, H, G, T):
+    w = W.make_prefill(100 + G, n_new=T, n_cached=200, H=H, G=G, K=150, page_size=16, kv_dtype=W.KV_FP8_E4M3)
+    slots, enc, lens, out, lse = gpu_prefill(S, w, dev, ws)
+    ref_enc, ref_lens, _ = oracle.group_union(slots.cpu().numpy(), G, w.num_slots)
+    assert np.array_equal(enc.cpu().numpy(), ref_enc)
+    ref, ref_lse, err = oracle.prefill_grouped(w.q_bits, G, w.kv, w.kv_dtype, w.num_slots, ref_enc, ref_lens, w.K,
+                                               w.scale)
+    assert err == 0
+    compare(out, lse, ref, ref_lse, FP8_OUT_TOL)
+    assert ws.read_status() == 0
+
+
+# ------------------------------------------------------------------ CUDA graph replay
+
+def test_decode_and_prefill_replay_from_a_cuda_graph(S, dev):
+    # The grids depend only on the arguments, so a captured step replays with new inputs.
+    w = W.make_decode(110, T=6, H=64, K=400, ctx_lo=500, ctx_hi=3000, page_size=64)
+    ws = S.Workspace(dev).ensure(1 << 24)
+    q = to_dev(w.q_bits, dev)
+    kv = kv_of(w, dev)
+    topk = to_dev(w.topk, dev)
+    bt, seq = to_dev(w.block_table, dev), to_dev(w.seq_lens, dev)
+    out = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+    S.sparse_mla_decode(q, kv, topk, w.scale, block_table=bt, seq_lens=seq, out=out, lse=lse, ws=ws)  # warm
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            S.sparse_mla_decode(q, kv, topk, w.scale, block_table=bt, seq_lens=seq, out=out, lse=lse, ws=ws)
+    w2 = W.make_decode(111, T=6, H=64, K=400, ctx_lo=500, ctx_hi=3000, page_size=64)
+    q.copy_(to_dev(w2.q_bits, dev))  # new queries, same cache and lists
+    g.replay()
+    torch.cuda.synchronize()
+    w2.kv, w2.block_table, w2.seq_lens, w2.topk, w2.num_pages = w.kv, w.block_table, w.seq_lens, w.topk, w.num_pages
+    ref, ref_lse, _ = oracle_decode(w2)
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    g.replay()
+    torch.cuda.synchronize()
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    assert ws.read_status() == 0
+
+
+# --------------------------------------------------------- zigzag-sharded prefill
+
+def test_zigzag_sharded_prefill_reproduces_the_whole_step(S, dev, ws):
+    from sparse_mla_attention_top_gb300.shard import zigzag_split
+
+    w = W.make_prefill(120, n_new=37, n_cached=400, H=64, G=2, K=180, page_size=16)
+    _, _, _, out_all, lse_all = gpu_prefill(S, w, dev, ws)
+    out = torch.zeros_like(out_all)
+    lse = torch.zeros_like(lse_all)
+    for ids in zigzag_split(w.T, 4):  # each rank runs its own rows, no exchange
+        idx = torch.from_numpy(ids).to(dev)
+        qr = to_dev(w.q_bits, dev)[idx].contiguous()
+        tk = to_dev(w.topk, dev)[idx].contiguous()
+        slots = S.resolve_topk_slots(tk, block_table=to_dev(w.block_table, dev), seq_lens=to_dev(w.seq_lens, dev),
+                                     req_of_token=torch.zeros(len(ids), dtype=torch.int32, device=dev),
+                                     page_size=w.page_size, num_pages=w.num_pages, ws=ws)
+        enc, lens = S.build_group_union(slots, w.G, w.num_slots, ws=ws)
+        o, l = S.sparse_mla_prefill_grouped(qr, w.G, kv_of(w, dev), enc, lens, w.K, w.scale, ws=ws)
+        out[idx] = o
+        lse[idx] = l
+    ref, ref_lse, _ = oracle.decode(w.q_bits, w.kv, w.kv_dtype, w.num_pages, w.page_size, w.topk, w.scale,
+                                    block_table=w.block_table, seq_lens=w.seq_lens, req_of_token=w.req_of_token)
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    assert float((out.float() - out_all.float()).abs().max()) <= BF16_OUT_TOL
+    assert ws.read_status() == 0
