@@ -81,6 +81,7 @@ constexpr int kBarSFull = 14;   // S^T ready
 constexpr int kBarPvDone = 16;  // all MMAs of the tile done
 constexpr int kBarQFull = 17;   // Q^T loaded
 constexpr int kBarQEmpty = 18;  // last S^T of the row-set done with Q^T
+constexpr int kBarMerge = 19;   // bulk copies of a merge band landed
 
 constexpr int kTmemCols = 512;
 constexpr int kTmemS = 0;   // S^T: columns 0..63
@@ -236,17 +237,23 @@ __device__ __forceinline__ int fetch_entry(const AttnParams& p, const Seg& seg, 
   return __ldg(p.enc + static_cast<long long>(seg.r >> 1) * p.list_stride + e);
 }
 
-// Turns a fetched entry into the slot / mask table entries of buffer `buf`.
-__device__ __forceinline__ void resolve_entry(const AttnParams& p, const Seg& seg, int raw, int ltid, int* slot_tab,
-                                              uint32_t* mask_tab, int& err) {
+// Turns a fetched entry into its slot / mask table entries, in two steps so that the one
+// dependent load (the page-table entry of a decode position) can be issued early and
+// checked late: resolve_page issues it (prefill words need none), resolve_finish checks
+// and stores.
+__device__ __forceinline__ int resolve_page(const AttnParams& p, const ReqContext& rc, int raw) {
+  if (p.mode != kModeDecode || raw == kDeadEntry) return -1;
+  return page_of(raw, rc, p.max_blocks, p.page_size);
+}
+
+__device__ __forceinline__ void resolve_finish(const AttnParams& p, const ReqContext& rc, int raw, int page, int ltid,
+                                               int* slot_tab, uint32_t* mask_tab, int& err) {
   if (ltid >= kTileRows) return;
   int slot = -1;
   uint32_t mask = 0xFFFFFFFFu;
   if (raw != kDeadEntry) {
     if (p.mode == kModeDecode) {
-      const int t = seg.r / p.hchunks;
-      slot = resolve_position(raw, t, p.topk_len, p.req_of_token, p.block_table, p.num_reqs, p.max_blocks,
-                              p.seq_lens, p.page_size, p.num_pages, &err);
+      slot = slot_of(raw, page, rc, p.block_table != nullptr, p.max_blocks, p.page_size, p.num_pages, &err);
     } else {
       const uint32_t w = static_cast<uint32_t>(raw);
       if (w != 0xFFFFFFFFu) {
@@ -266,14 +273,15 @@ __device__ __forceinline__ void resolve_entry(const AttnParams& p, const Seg& se
 
 // Merge of a row-set split between CTAs c_lo .. c_lo + parts - 1 (stream-K): out = sum_s
 // exp(lse_s - lse) o_s, lse = ln sum_s exp(lse_s), over the parts' normalised partials.
-// Runs after the CTA's own tiles, when all 221 KB of stage and Q memory are free: all 512
-// threads copy every part's rows for a band of channels into shared memory with cp.async
-// (one round trip per band instead of one per load), 64 threads turn the parts' LSEs into
-// weights meanwhile, and the band is then combined from shared memory.
+// Runs after the CTA's own tiles, when all 221 KB of stage and Q memory are free: each
+// part's rows for a band of channels come into shared memory by 1-D bulk copies (one per
+// part and row), the parts' LSEs become weights, and the band is combined from shared
+// memory.
 constexpr int kMaxMergeParts = 128;
 constexpr int kMergeScratchBytes = kOffSlot - kOffStage;  // stage + Q memory
 
-__device__ void merge_rowset(const AttnParams& p, int r, uint8_t* scratch) {
+__device__ void merge_rowset(const AttnParams& p, int r, uint8_t* scratch, uint32_t mbar, uint32_t& phase,
+                             volatile int* abort_flag) {
   const long long nt = p.tiles_per_rowset;
   const long long first = r * nt;
   const long long c_lo = streamk_owner(first, p.total_tiles, p.num_ctas);
@@ -315,17 +323,19 @@ __device__ void merge_rowset(const AttnParams& p, int r, uint8_t* scratch) {
     if (p.lse && row < rr.nvalid) p.lse[rr.base + row] = L;
   }
   const uint32_t sbuf = smem_u32(buf);
-  const int total = (parts * kRowsetRows) << lvec;
+  const uint32_t row_bytes = 4u << lband;  // one part's row within a band
   for (int c0 = 0; c0 < kVdim; c0 += 1 << lband) {
-    for (int i = threadIdx.x; i < total; i += blockDim.x) {
-      const int pr = i >> lvec;  // part * 64 + row
-      const int v = i & ((1 << lvec) - 1);
-      const float* src = p.part_o + (static_cast<long long>(s_slot[pr >> 6]) * kRowsetRows + (pr & 63)) * kVdim + c0 + 4 * v;
-      cp_async16(sbuf + 16u * static_cast<uint32_t>(i), src, (pr & 63) < rr.nvalid ? 16u : 0u);
-    }
-    cp_async_commit();
-    cp_async_wait_all();
+    // one bulk copy per (part, live row): parts x nvalid contiguous runs of row_bytes
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(mbar, static_cast<uint32_t>(parts * rr.nvalid) * row_bytes);
     __syncthreads();
+    for (int i = threadIdx.x; i < parts * kRowsetRows; i += blockDim.x) {
+      const int row = i & (kRowsetRows - 1);
+      if (row >= rr.nvalid) continue;
+      const float* src = p.part_o + (static_cast<long long>(s_slot[i >> 6]) * kRowsetRows + row) * kVdim + c0;
+      bulk_copy_g2s(sbuf + static_cast<uint32_t>(i) * row_bytes, src, row_bytes, mbar);
+    }
+    mbar_wait(mbar, phase, p.status, abort_flag);
+    phase ^= 1u;
     // combine: 4 channels (one 16-byte vector) per thread and step
     for (int i = threadIdx.x; i < (kRowsetRows << lvec); i += blockDim.x) {
       const int row = i >> lvec, v = i & ((1 << lvec) - 1);
@@ -380,6 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
     mbar_init(bar(kBarPvDone), 1);
     mbar_init(bar(kBarQFull), kLoaderThreads);
     mbar_init(bar(kBarQEmpty), 1);
+    mbar_init(bar(kBarMerge), 1);
     *abort_flag = 0;
     *npending = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -408,6 +419,12 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
     while (sched.next(seg)) {
       if (seg.ntile == 0) continue;
       const RowsetRows rr = rowset_rows(p, seg.r);
+      // decode: the query's request and page-table row, once per segment
+      ReqContext rc{nullptr, 0, true};
+      if (p.mode == kModeDecode)
+        rc = request_context(seg.r / p.hchunks, p.req_of_token, p.block_table, p.num_reqs, p.max_blocks, p.seq_lens);
+      // the first tile's entries are fetched before the Q^T loads, so the latencies overlap
+      const int raw_first = (resolved != n) ? fetch_entry(p, seg, seg.tb, ltid) : kDeadEntry;
       // Q^T of the row-set: 64 rows x 72 chunks, zero rows for padding. bf16: cp.async,
       // published after the first tile's cp.async blocks are issued; f16 mode: converted.
       mbar_wait(bar(kBarQEmpty), (qn & 1u) ^ 1u, p.status, abort_flag);
@@ -437,7 +454,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
         const int buf = n & 1;
         int* slots = slot_tab + buf * kTileRows;
         if (resolved != n) {
-          resolve_entry(p, seg, fetch_entry(p, seg, seg.tb + i, ltid), ltid, slots, mask_tab + buf * kTileRows, err);
+          const int raw = i == 0 ? raw_first : fetch_entry(p, seg, seg.tb + i, ltid);
+          resolve_finish(p, rc, raw, resolve_page(p, rc, raw), ltid, slots, mask_tab + buf * kTileRows, err);
           named_bar_sync(kNamedBarLoaders, kLoaderThreads);
         }
         // The next tile's slots go into the other buffer, last read by the softmax of tile
@@ -468,6 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
             }
             cp_async_commit();
           }
+          // the next tile's page-table entries: loads issued now, checked once the blocks are out
+          const int page_next = ahead ? resolve_page(p, rc, raw_next) : -1;
           if (!q_published) {
             cp_async_wait<kRegBlock0>();
             fence_proxy_async_smem();
@@ -484,17 +504,17 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
             fence_proxy_async_smem();
             mbar_arrive(bar(kBarFull + kb));
           }
-          // resolve the next tile while the cp.async blocks land
-          if (ahead) {
-            resolve_entry(p, seg, raw_next, ltid, slot_tab + (buf ^ 1) * kTileRows, mask_tab + (buf ^ 1) * kTileRows,
-                          err);
-            resolved = n + 1;
-          }
           publish_cp_blocks<0, kRegBlock0>(bar(0));
-          if (ahead) named_bar_sync(kNamedBarLoaders, kLoaderThreads);
+          if (ahead) {
+            resolve_finish(p, rc, raw_next, page_next, ltid, slot_tab + (buf ^ 1) * kTileRows,
+                           mask_tab + (buf ^ 1) * kTileRows, err);
+            resolved = n + 1;
+            named_bar_sync(kNamedBarLoaders, kLoaderThreads);
+          }
         } else {
           // e4m3: thread owns (row = ltid / 2, 32 channels of every latent block) and four
           // 16-byte rope chunks; all raw bytes are in registers before any block is written.
+          int page_next = -1;
           const int row = ltid >> 1, hf = ltid & 1;
           const int slot = slots[row];
           uint4 raw[8][2];
@@ -526,11 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
 #pragma unroll
           for (int kb = 0; kb < 8; ++kb) {
             mbar_wait(bar(kBarEmptyV + (kb >> 1)), (n & 1u) ^ 1u, p.status, abort_flag);
-            if (kb == 0 && ahead) {
-              resolve_entry(p, seg, raw_next, ltid, slot_tab + (buf ^ 1) * kTileRows,
-                            mask_tab + (buf ^ 1) * kTileRows, err);
-              resolved = n + 1;
-            }
+            if (kb == 0 && ahead) page_next = resolve_page(p, rc, raw_next);
             const float s = sc[kb >> 1];
             uint8_t* blk = smem + kOffStage + kb * kBlockBytes;
 #pragma unroll
@@ -561,7 +577,12 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
           }
           fence_proxy_async_smem();
           mbar_arrive(bar(kBarFull + 8));
-          if (ahead) named_bar_sync(kNamedBarLoaders, kLoaderThreads);
+          if (ahead) {
+            resolve_finish(p, rc, raw_next, page_next, ltid, slot_tab + (buf ^ 1) * kTileRows,
+                           mask_tab + (buf ^ 1) * kTileRows, err);
+            resolved = n + 1;
+            named_bar_sync(kNamedBarLoaders, kLoaderThreads);
+          }
         }
       }
     }
@@ -668,13 +689,27 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
             : "memory");
         if (any) {
           // exact column maxima of this tile, then move the reference and rescale
-          float mine = -CUDART_INF_F;
+          // column maxima over the warp's 32 KV rows, transposed so that lane c ends with
+          // column c (the first exchange halves into t[], x[] stays intact for P)
+          float t[16];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            const float mx = warp_max_f32(x[c]);
-            if (lane == c) mine = mx;
+          for (int k = 0; k < 16; ++k) {
+            const bool up = (lane & 16) != 0;
+            const float send = up ? x[k] : x[k + 16];
+            const float keep = up ? x[k + 16] : x[k];
+            t[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, 16));
           }
-          red[warp * 32 + lane] = mine;
+#pragma unroll
+          for (int half = 8; half >= 1; half >>= 1) {
+            const bool up = (lane & half) != 0;
+#pragma unroll
+            for (int k = 0; k < half; ++k) {
+              const float send = up ? t[k] : t[k + half];
+              const float keep = up ? t[k + half] : t[k];
+              t[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, half));
+            }
+          }
+          red[warp * 32 + lane] = t[0];
           named_bar_sync(kNamedBarSoftmax, kSoftmaxThreads);
           if (q == 0) {
             const int col = 32 * ch + lane;
@@ -757,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
         const int col = 32 * ch + lane;
         const float l = red[(4 * ch) * 32 + lane] + red[(4 * ch + 1) * 32 + lane] + red[(4 * ch + 2) * 32 + lane] +
                         red[(4 * ch + 3) * 32 + lane];
-        lfin[col] = l;
+        lfin[col] = l > 0.f ? 1.0f / l : 0.f;  // the column's 1 / l, read by every thread below
         const float lse2 = (l > 0.f) ? (m_ref[col] + __log2f(l)) : -CUDART_INF_F;
         const float lse_nat = lse2 * 0.69314718055994530942f;
         if (col < rr.nvalid) {
@@ -772,8 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
       float inv[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float l = lfin[32 * ch + c];
-        inv[c] = l > 0.f ? 1.0f / l : 0.f;
+        inv[c] = lfin[32 * ch + c];
       }
       const int nv = rr.nvalid - 32 * ch;  // my columns c < nv exist
 #pragma unroll 1
@@ -832,7 +866,9 @@ __global__ void __launch_bounds__(kThreads, 1) attention_kernel(const __grid_con
   const int np = *npending;
   if (np > 0) {
     __threadfence();
-    for (int k = 0; k < np; ++k) merge_rowset(p, pending[k], smem + kOffStage);
+    asm volatile("fence.proxy.async.global;" ::: "memory");  // other CTAs' partials, read by bulk copies
+    uint32_t phase = 0;
+    for (int k = 0; k < np; ++k) merge_rowset(p, pending[k], smem + kOffStage, bar(kBarMerge), phase, abort_flag);
   }
 }
 

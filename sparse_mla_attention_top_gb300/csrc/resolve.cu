@@ -27,8 +27,8 @@ __global__ void __launch_bounds__(256) resolve_kernel(const int32_t* __restrict_
     const long long idx = static_cast<long long>(t) * K + j;
     int slot = -1;
     if (j < len) {
-      slot = resolve_position(__ldg(topk + idx), t, topk_len, req_of_token, block_table, num_reqs, max_blocks,
-                              seq_lens, page_size, num_pages, &err);
+      slot = resolve_position(__ldg(topk + idx), t, req_of_token, block_table, num_reqs, max_blocks, seq_lens,
+                              page_size, num_pages, &err);
     }
     slots[idx] = slot;
   }
