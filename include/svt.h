@@ -127,10 +127,10 @@ SVT_API svt_status svt_resolve_topk_slots(const int32_t* topk_pos, int32_t T, in
  *   out_bf16 [T, H, 512] bf16; lse [T, H] fp32 natural-log normaliser, or NULL.
  *            A query with no live entry gets out = 0 and lse = -inf.
  *   num_splits  0 = automatic (persistent CTAs share the whole batch's tiles evenly; a
- *            query whose list is split between CTAs is merged in the same kernel by the
- *            last CTA to finish its part), 1 = one CTA per (query, 64-head chunk), S > 1 =
- *            each query's list cut into S slices ("parallel tiled softmax", the explainer of
- *            arXiv 2511.11581, section 4.5), merged the same way.
+ *            query whose list is split between CTAs is merged by a second kernel that the
+ *            call enqueues right behind the attention kernel), 1 = one CTA per (query,
+ *            64-head chunk), S > 1 = each query's list cut into S slices ("parallel tiled
+ *            softmax", the explainer of arXiv 2511.11581, section 4.5), merged the same way.
  * Workspace: svt_sparse_mla_decode_workspace_size(T, H, K, num_splits) (depends on the
  * current device's SM count when num_splits == 0).
  */
@@ -158,7 +158,7 @@ SVT_API svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t 
  *               SVT_DEV_ERR_* values) when the call's kernels have run; NULL to skip.
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress)
  * with that device current; make that first call before any stream capture. Every call shares
- * the one array: the call clears its status word and counters first, so calls that follow one
+ * the one array: the call clears its status word first, so calls that follow one
  * another on a stream are independent, but calls that overlap on the GPU (other streams or
  * threads) race on it. It calls no cudaMalloc, cudaFree or other allocating routine.
  */

@@ -93,7 +93,7 @@ DecodePlan plan_decode(int T, int H, int K, int num_splits) {
   return d;
 }
 
-// Workspace: status header | split counters (fixed 64 KB) | partial outputs | partial LSEs.
+// Workspace: status header | partial outputs | partial LSEs.
 size_t decode_part_o_bytes(const DecodePlan& d) {
   return round_up(2ull * d.num_ctas * svt::kRowsetRows * svt::kVdim * sizeof(float), 256);
 }
@@ -102,7 +102,7 @@ size_t decode_part_lse_bytes(const DecodePlan& d) {
 }
 size_t decode_ws_bytes(const DecodePlan& d) {
   size_t b = svt::kStatusBytes;
-  if (d.partials) b += svt::kCounterBytes + decode_part_o_bytes(d) + decode_part_lse_bytes(d);
+  if (d.partials) b += decode_part_o_bytes(d) + decode_part_lse_bytes(d);
   return b;
 }
 
@@ -184,11 +184,6 @@ svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const
   if (block_table != nullptr && (num_reqs <= 0 || max_blocks <= 0))
     return fail(SVT_ERR_INVALID_ARG, "num_reqs and max_blocks must be > 0 with a block table");
   const DecodePlan d = plan_decode(T, H, K, num_splits);
-  if (d.partials && static_cast<long long>(d.tiles_per_rowset) * d.num_ctas / d.total_tiles + 2 > 128)
-    return fail(SVT_ERR_UNSUPPORTED, "a query's list would be split into more than 128 parts");
-  if (d.partials && d.num_ctas > svt::kMaxCtas)
-    return fail(SVT_ERR_UNSUPPORTED, "num_splits %d gives %d CTAs; at most %d can split a decode", num_splits,
-                d.num_ctas, svt::kMaxCtas);
   st = check_ws(ws, ws_bytes, decode_ws_bytes(d));
   if (st != SVT_OK) return st;
   if (T == 0) return SVT_OK;
@@ -227,9 +222,8 @@ svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const
   p.status = static_cast<int*>(ws);
   if (d.partials) {
     char* base = static_cast<char*>(ws) + svt::kStatusBytes;
-    p.counters = reinterpret_cast<int*>(base);
-    p.part_o = reinterpret_cast<float*>(base + svt::kCounterBytes);
-    p.part_lse = reinterpret_cast<float*>(base + svt::kCounterBytes + decode_part_o_bytes(d));
+    p.part_o = reinterpret_cast<float*>(base);
+    p.part_lse = reinterpret_cast<float*>(base + decode_part_o_bytes(d));
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (d.num_ctas == 0) {
@@ -240,6 +234,10 @@ svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const
   }
   cudaError_t e = svt::launch_attention(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+  if (d.partials) {
+    e = svt::launch_streamk_merge(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode merge launch");
+  }
   return SVT_OK;
 }
 

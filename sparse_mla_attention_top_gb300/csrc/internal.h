@@ -15,11 +15,6 @@ constexpr int kVdim = 512;         // V is the first 512 columns
 constexpr int kRowBytesBf16 = 1152;
 constexpr int kRowBytesFp8 = 656;  // 512 e4m3 | 4 fp32 scales | 64 bf16 rope
 constexpr size_t kStatusBytes = 256;  // status header at the start of every workspace
-// Split-merge counters follow the header at a fixed place, so that every call (whatever its
-// shape) uses the same bytes for them and nothing else ever writes there; each call leaves
-// them zero. One counter per CTA bounds the CTAs of a split decode.
-constexpr size_t kCounterBytes = 65536;
-constexpr int kMaxCtas = static_cast<int>(kCounterBytes / sizeof(int));
 
 // Attention kernel geometry (the tcgen05 tile): a tile is 128 KV rows (the MMA M), a
 // row-set is up to 64 query rows sharing one KV list (the MMA N).
@@ -69,9 +64,33 @@ struct AttnParams {
   int num_ctas;
   float* part_o;    // [2 * num_ctas, 64, 512] fp32 (stream-K partial segments)
   float* part_lse;  // [2 * num_ctas, 64]
-  int* counters;    // [num_ctas] parts finished per split row-set, indexed by its first CTA
   int* status;
 };
+
+// Query row n (< 64) of row-set r is row base + n of the [T*H, ...] q / out / lse arrays
+// and exists iff n < nvalid. Decode: base = t*H + 64*chunk. Prefill (H*G = 128): packed
+// row half*64 + n of group g is token g*G + (half*64 + n)/H, head (half*64 + n)%H, i.e.
+// row g*128 + half*64 + n; rows of members past the last token do not exist.
+struct RowsetRows {
+  long long base;
+  int nvalid;
+};
+
+__device__ __forceinline__ RowsetRows rowset_rows(const AttnParams& p, int r) {
+  RowsetRows rr;
+  if (p.mode == kModeDecode) {
+    const int t = r / p.hchunks;
+    const int hc = r - t * p.hchunks;
+    rr.base = static_cast<long long>(t) * p.H + hc * kRowsetRows;
+    rr.nvalid = min(kRowsetRows, p.H - hc * kRowsetRows);
+  } else {
+    const int g = r >> 1, half = r & 1;
+    rr.base = static_cast<long long>(g) * 128 + half * kRowsetRows;
+    const int members = min(p.G, p.T - g * p.G);
+    rr.nvalid = max(0, min(kRowsetRows, members * p.H - half * kRowsetRows));
+  }
+  return rr;
+}
 
 // First flattened tile of CTA c under the stream-K split of `total` tiles over n CTAs.
 __host__ __device__ inline long long streamk_lo(long long c, long long total, long long n) {
@@ -80,6 +99,11 @@ __host__ __device__ inline long long streamk_lo(long long c, long long total, lo
 // The CTA whose stream-K range holds flattened tile `pos`.
 __host__ __device__ inline long long streamk_owner(long long pos, long long total, long long n) {
   return ((pos + 1) * n - 1) / total;
+}
+// The partial slot CTA c writes for the row-set whose first flattened tile is `first`: its
+// second one (2c + 1) when its range started inside an earlier row-set, else its first (2c).
+__host__ __device__ inline long long streamk_part_slot(long long c, long long first, long long total, long long n) {
+  return streamk_lo(c, total, n) < first ? 2 * c + 1 : 2 * c;
 }
 
 // Launchers (each returns cudaSuccess or the launch error).
@@ -95,6 +119,9 @@ cudaError_t launch_merge_splits(const float* o_part, const float* lse_part, int 
                                 uint16_t* out, float* lse, cudaStream_t stream);
 
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
+// Merges the partial results of the row-sets a stream-K decode split between CTAs; launched
+// right behind the attention kernel (programmatic dependent launch) and waiting for it.
+cudaError_t launch_streamk_merge(const AttnParams& p, cudaStream_t stream);
 
 // Records the message svt_last_error_string() returns on this thread and passes `st` back.
 svt_status set_last_error(svt_status st, const char* fmt, ...);

@@ -6,7 +6,7 @@
 // normalised output:  lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s.
 //
 // One warp per output row: the slice LSEs are reduced with warp shuffles, then each lane
-// accumulates 16 of the 512 channels. HBM-bound on reading the fp32 partials.
+// accumulates 16 of the 512 channels. Bound by reading the fp32 partials.
 #include <math_constants.h>
 
 #include "device.cuh"
@@ -48,7 +48,7 @@ __device__ __forceinline__ void merge_row(int S, LseOf lse_of, OOf o_of, uint16_
       const float4* o = reinterpret_cast<const float4*>(o_of(s)) + lane * 4;
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
-        const float4 x = o[v];
+        const float4 x = __ldcg(o + v);
         acc[4 * v + 0] += w * x.x;
         acc[4 * v + 1] += w * x.y;
         acc[4 * v + 2] += w * x.z;
@@ -77,7 +77,130 @@ __global__ void __launch_bounds__(256) merge_splits_kernel(const float* __restri
       [&](int s) { return o_part + (s * rows + r) * kVdim; }, out + r * kVdim, lse ? lse + r : nullptr);
 }
 
+// Stream-K decode: a row-set whose tiles span CTAs c_lo..c_hi has one normalised partial per
+// CTA; CTA c_lo's partial sits in its second slot when its range began in an earlier row-set.
+// Row-sets held by a single CTA were written by the attention kernel itself. The kernel is
+// launched behind the attention kernel with programmatic dependent launch, so its CTAs are
+// scheduled on the SMs that attention CTAs leave; griddepcontrol.wait then holds every warp
+// until the attention grid has finished and its writes are visible. A warp takes one half
+// (256 channels) of one row: the parts' LSEs and the first four parts' half-rows come in one
+// trip to L2.
+constexpr int kMergeWarpsPerCta = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// One half (channels 256 half .. +255) of output row `row` of a split row-set whose parts'
+// rows are part_o[part_row(s)], part_lse[part_row(s)]: lane l holds part l's LSE, and the
+// first four parts' half-rows are requested in the same trip.
+template <typename PartRow>
+__device__ __forceinline__ void merge_half_row(const AttnParams& p, int parts, PartRow part_row, int half,
+                                               uint16_t* out_row, float* lse_out) {
+  const int lane = threadIdx.x & 31;
+  const float ls = lane < parts ? __ldcg(p.part_lse + part_row(lane)) : -CUDART_INF_F;
+  const int ch0 = 256 * half + 8 * lane;  // this lane's 8 channels
+  float4 x[4][2];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float4* o = reinterpret_cast<const float4*>(p.part_o + part_row(min(j, parts - 1)) * kVdim + ch0);
+    x[j][0] = __ldcg(o);
+    x[j][1] = __ldcg(o + 1);
+  }
+  // L = ln sum_s exp(lse_s) (parts past 32 folded in by a loop)
+  float mx = ls;
+  for (int s = 32 + lane; s < parts; s += 32) mx = fmaxf(mx, __ldcg(p.part_lse + part_row(s)));
+  mx = warp_allmax(mx);
+  float L = -CUDART_INF_F;
+  if (mx != -CUDART_INF_F) {
+    float tot = ls == -CUDART_INF_F ? 0.f : ex2_approx((ls - mx) * kLog2e);
+    for (int s = 32 + lane; s < parts; s += 32) tot += ex2_approx((__ldcg(p.part_lse + part_row(s)) - mx) * kLog2e);
+    L = mx + logf(warp_allsum(tot));
+  }
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+  if (L != -CUDART_INF_F) {
+    auto weight = [&](int s) -> float {
+      const float lsj = s < 32 ? __shfl_sync(0xffffffffu, ls, s) : __ldcg(p.part_lse + part_row(s));
+      return lsj == -CUDART_INF_F ? 0.f : ex2_approx((lsj - L) * kLog2e);
+    };
+    auto accumulate = [&](float w, const float4(&v)[2]) {
+      acc[0] += w * v[0].x;
+      acc[1] += w * v[0].y;
+      acc[2] += w * v[0].z;
+      acc[3] += w * v[0].w;
+      acc[4] += w * v[1].x;
+      acc[5] += w * v[1].y;
+      acc[6] += w * v[1].z;
+      acc[7] += w * v[1].w;
+    };
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float w = weight(j);  // every lane shuffles; parts past the last weigh nothing
+      if (j < parts) accumulate(w, x[j]);
+    }
+    for (int s = 4; s < parts; ++s) {
+      const float4* o = reinterpret_cast<const float4*>(p.part_o + part_row(s) * kVdim + ch0);
+      const float4 v[2] = {__ldcg(o), __ldcg(o + 1)};
+      accumulate(weight(s), v);
+    }
+  }
+  uint4 packed;
+  packed.x = pack_bf16x2(acc[0], acc[1]);
+  packed.y = pack_bf16x2(acc[2], acc[3]);
+  packed.z = pack_bf16x2(acc[4], acc[5]);
+  packed.w = pack_bf16x2(acc[6], acc[7]);
+  *reinterpret_cast<uint4*>(out_row + ch0) = packed;
+  if (lse_out != nullptr && lane == 0 && half == 0) *lse_out = L;
+}
+
+__global__ void __launch_bounds__(256, 4) streamk_merge_kernel(const __grid_constant__ AttnParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const long long nt = p.tiles_per_rowset;
+  const long long items = static_cast<long long>(p.num_rowsets) * kRowsetRows * 2;
+  const long long nwarps = static_cast<long long>(gridDim.x) * kMergeWarpsPerCta;
+  for (long long it = blockIdx.x * kMergeWarpsPerCta + (threadIdx.x >> 5); it < items; it += nwarps) {
+    const int half = static_cast<int>(it & 1);
+    const int r = static_cast<int>(it >> 7), row = static_cast<int>((it >> 1) & (kRowsetRows - 1));
+    const long long first = r * nt;
+    const long long c_lo = streamk_owner(first, p.total_tiles, p.num_ctas);
+    const long long c_hi = streamk_owner(first + nt - 1, p.total_tiles, p.num_ctas);
+    if (c_lo == c_hi) continue;
+    const RowsetRows rr = rowset_rows(p, r);
+    if (row >= rr.nvalid) continue;
+    const long long slot0 = streamk_part_slot(c_lo, first, p.total_tiles, p.num_ctas);
+    merge_half_row(
+        p, static_cast<int>(c_hi - c_lo + 1),
+        [&](int s) -> long long { return (s == 0 ? slot0 : 2 * (c_lo + s)) * kRowsetRows + row; }, half,
+        p.out + (rr.base + row) * kVdim, p.lse ? p.lse + rr.base + row : nullptr);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_streamk_merge(const AttnParams& p, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  // one wave: as many CTAs as fit at once (register-bound), each warp looping over items
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, streamk_merge_kernel, 256, 0);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const long long warps = static_cast<long long>(p.num_rowsets) * kRowsetRows * 2;
+  long long blocks = (warps + kMergeWarpsPerCta - 1) / kMergeWarpsPerCta;
+  if (blocks > static_cast<long long>(per_sm) * sms) blocks = static_cast<long long>(per_sm) * sms;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, streamk_merge_kernel, p);
+}
 
 cudaError_t launch_merge_splits(const float* o_part, const float* lse_part, int S, long long rows, int /*H_rows*/,
                                 uint16_t* out, float* lse, cudaStream_t stream) {

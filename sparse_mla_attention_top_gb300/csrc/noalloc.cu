@@ -1,7 +1,7 @@
 // Sparse MLA decode for callers that cannot allocate device memory.
 //
-// svt_sparse_mla_decode needs a caller-provided workspace (a status word, split-merge
-// counters and, when a query's list is split between CTAs, partial results). Some callers
+// svt_sparse_mla_decode needs a caller-provided workspace (a status word and, when a query's
+// list is split between CTAs, partial results). Some callers
 // cannot call cudaMalloc at all: a plugin inside a host application that owns every byte of
 // device memory through its own allocator, or code that must never trigger the device-wide
 // synchronisation a cudaMalloc can cause. For them this file keeps the scratch in a
@@ -13,8 +13,8 @@
 
 namespace {
 
-// 8 MiB: the status header, the 64 KiB split counters and partial results for up to 31
-// CTAs (2 slots x 64 rows x 512 fp32 + LSEs each). One CTA per query (num_splits = 1) needs
+// 8 MiB: the status header and partial results for up to 31 CTAs (2 slots x 64 rows x 512
+// fp32 + LSEs each). One CTA per query (num_splits = 1) needs
 // only the 256-byte header, whatever the batch.
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -57,9 +57,9 @@ extern "C" SVT_API svt_status svt_sparse_mla_decode_noalloc(
                                "use num_splits = 1 (no partial results) or split the batch",
                                need, kNoAllocScratchBytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // The array keeps the previous call's bytes: clear the status word and the split counters.
-  const size_t clear = need < svt::kStatusBytes + svt::kCounterBytes ? need : svt::kStatusBytes + svt::kCounterBytes;
-  e = cudaMemsetAsync(scratch, 0, clear, s);
+  // The array keeps the previous call's bytes: clear the status word (partial results are
+  // written before they are read).
+  e = cudaMemsetAsync(scratch, 0, svt::kStatusBytes, s);
   if (e != cudaSuccess) return svt::set_last_error(SVT_ERR_CUDA, "clearing scratch: %s", cudaGetErrorString(e));
   const svt_status st = svt_sparse_mla_decode(q_bf16, T, H, kv, block_table, num_reqs, max_blocks, req_of_token,
                                               seq_lens, topk, K, topk_len, softmax_scale, out_bf16, lse, num_splits,

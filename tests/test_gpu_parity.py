@@ -315,8 +315,8 @@ def test_prefill_membership_bit_negative_control(S, dev, ws):
 
 
 def test_workspace_reuse_across_shapes_and_repeats(S, dev):
-    # One workspace serves calls of different shapes back to back; the split-merge counters
-    # must start at zero every time (regression: they once shared bytes with partials).
+    # One workspace serves calls of different shapes back to back (split and unsplit), so a
+    # call never depends on bytes an earlier call left in it.
     ws = S.Workspace(dev)
     big = W.make_decode(80, T=5, H=64, K=700, ctx_lo=800, ctx_hi=3000, page_size=64)
     small = W.make_decode(81, T=4, H=16, K=256, ctx_lo=300, ctx_hi=900, page_size=16)
