@@ -61,6 +61,7 @@ def _load():
         lib.oracle_merge.argtypes = [P, P, i32, i64, P, P]
         lib.oracle_attend_slots.argtypes = [P, i32, P, i32, i64, P, i32, f64, P, P]
         lib.oracle_fetch_rows.argtypes = [P, i32, i64, P, i32, P]
+        lib.oracle_topk_select.argtypes = [P, i32, i32, i64, P, i32, P]
         lib.oracle_num_threads.restype = i32
         _lib = lib
     return _lib
@@ -200,3 +201,12 @@ def fetch_rows(kv_bytes, kv_dtype, slots, row_stride=None):
     rows = np.empty((len(slots), ROW), np.float64)
     _load().oracle_fetch_rows(_ptr(kv_bytes), kv_dtype, row_stride, _ptr(slots), len(slots), _ptr(rows))
     return rows
+
+
+def topk_select(scores, K, lens=None):
+    """Top-k positions per query row of `scores` [T, N] fp32 (ascending, -1 padded) -> [T, K] int32."""
+    scores = _c(scores, np.float32)
+    T, N = scores.shape
+    out = np.empty((T, K), np.int32)
+    _load().oracle_topk_select(_ptr(scores), T, N, N, _ptr(_c(lens, np.int32)), int(K), _ptr(out))
+    return out

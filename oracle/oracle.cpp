@@ -26,6 +26,10 @@
 //          Blackwell" -- an e4m3 latent cache is a real variant; the pages give no byte
 //          layout, so the layout used here is: 512 e4m3 codes, 4 fp32 scales (one per 128
 //          channels), 64 bf16 rope values (656 bytes per row).
+//   [IDX]  "The Virtual Block Table", Input Knowledge Required, item 3: the DSA indexer
+//          produces top-k sparse indices per token, selecting a subset of KV positions. The
+//          pages name no selection rule beyond "top-k", so the reading used here: per query,
+//          the K largest scores among positions 0..len-1 (-1 padded when fewer exist).
 //
 // Error bits reported by the oracle (its own numbering):
 //   1  an index that is >= 0 but out of range (position past the request's length, page
@@ -394,6 +398,34 @@ void oracle_attend_slots(const double* q /*[n_q,576]*/, int32_t n_q, const uint8
 void oracle_fetch_rows(const uint8_t* kv, int32_t kv_dtype, int64_t row_stride, const int64_t* slots,
                        int32_t n, double* rows /*[n,576]*/) {
   for (int32_t i = 0; i < n; ++i) fetch_row(kv, kv_dtype, row_stride, slots[i], rows + static_cast<int64_t>(i) * kRow);
+}
+
+// Top-k selection [IDX]. Query t's candidates are positions 0..len_t-1 (len_t = lens[t]
+// clamped to [0, N], or N). The K largest scores are kept; equal scores (+0 and -0 are
+// equal) go to the lower position first; a NaN score ranks below every number. The kept
+// positions are written in ascending order to out[t, 0..], the remaining slots get -1.
+void oracle_topk_select(const float* scores, int32_t T, int32_t N, int64_t stride, const int32_t* lens, int32_t K,
+                        int32_t* out) {
+  for (int32_t t = 0; t < T; ++t) {
+    int32_t len = lens ? lens[t] : N;
+    len = len < 0 ? 0 : (len > N ? N : len);
+    const float* row = scores + static_cast<int64_t>(t) * stride;
+    std::vector<int32_t> idx(static_cast<size_t>(len));
+    for (int32_t j = 0; j < len; ++j) idx[static_cast<size_t>(j)] = j;
+    // a ranks before b: a's score is greater, or the scores are equal (both NaN counts as
+    // equal) and a is the lower position
+    auto before = [&](int32_t a, int32_t b) {
+      const double sa = row[a], sb = row[b];
+      const bool na = std::isnan(sa), nb = std::isnan(sb);
+      if (na != nb) return nb;  // the number ranks above the NaN
+      if (!na && sa != sb) return sa > sb;
+      return a < b;
+    };
+    std::sort(idx.begin(), idx.end(), before);
+    const int32_t m = len < K ? len : K;
+    std::sort(idx.begin(), idx.begin() + m);
+    for (int32_t k = 0; k < K; ++k) out[static_cast<int64_t>(t) * K + k] = k < m ? idx[static_cast<size_t>(k)] : -1;
+  }
 }
 
 int32_t oracle_num_threads() {

@@ -19,7 +19,10 @@ for them):
 * prefill lists: query i of the new tokens selects from its causal prefix; when the prefix
   holds at most K positions it takes them all, otherwise it keeps a uniform 70% of its
   predecessor's list and fills the rest with distinct new positions (neighbouring queries
-  overlap, as the pages report for real top-k).
+  overlap, as the pages report for real top-k);
+* indexer scores (the input of top-k selection): fp32 N(0, 1) values rounded to bf16
+  precision, so equal scores occur as they do for a low-precision indexer, one row per
+  query over its context (contexts as for the decode batch).
 """
 
 from __future__ import annotations
@@ -297,3 +300,29 @@ def dense_check() -> DecodeWorkload:
     w = make_decode(6, T=1, H=16, K=4096, ctx_lo=4096, ctx_hi=4096, page_size=64, kv_dtype=KV_BF16,
                     name="dense_check_h16_ctx4096_p64")
     return w
+
+
+@dataclass
+class TopkWorkload:
+    """Indexer scores for top-k selection: query t's candidates are positions 0..lens[t]-1."""
+    name: str
+    T: int
+    N: int
+    K: int
+    scores: np.ndarray  # [T, N] float32
+    lens: np.ndarray    # [T] int32
+    seed: int
+
+
+def make_topk(seed: int, T: int, K: int, ctx_lo: int, ctx_hi: int) -> TopkWorkload:
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(ctx_lo, ctx_hi + 1, size=T).astype(np.int32)
+    N = int(lens.max())
+    scores = bf16_bits_to_f32(f32_to_bf16_bits(rng.standard_normal((T, N), dtype=np.float32)))
+    return TopkWorkload(name=f"topk_t{T}_k{K}_ctx{ctx_lo}-{ctx_hi}", T=T, N=N, K=K, scores=scores, lens=lens,
+                        seed=seed)
+
+
+def topk_batch(T: int = 64) -> TopkWorkload:
+    """The decode batch's selection: 64 queries, contexts 8K-32K, K = 2048."""
+    return make_topk(7, T=T, K=2048, ctx_lo=8192, ctx_hi=32768)

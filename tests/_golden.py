@@ -70,3 +70,23 @@ def union_cases():
 def encode(mask: int, slot: int) -> int:
     """(mask << 24) | slot as a signed int32 value."""
     return int(np.array([(mask << 24) | slot], np.uint32).view(np.int32)[0])
+
+
+def topk_cases():
+    """Hand-worked top-k selections: dicts with K, scores (float32), len (int or None), expect."""
+    cases, cur = [], None
+    for line in _lines("topk_small.txt"):
+        tok = line.split()
+        if tok[0] == "case":
+            cur = {"name": tok[1]}
+        elif tok[0] == "K":
+            cur["K"] = int(tok[1])
+        elif tok[0] == "scores":
+            cur["scores"] = np.array([float(v) for v in tok[1:]], np.float32)
+        elif tok[0] == "len":
+            cur["len"] = None if tok[1] == "all" else int(tok[1])
+        elif tok[0] == "expect":
+            cur["expect"] = np.array([int(v) for v in tok[1:]], np.int32)
+        elif tok[0] == "end":
+            cases.append(cur)
+    return cases

@@ -460,3 +460,58 @@ def test_generators_hold_their_stated_shapes():
     assert all(max(s) <= 2100 + i for i, s in enumerate(live))  # causal prefix only
     overlap = np.mean([len(live[i] & live[i - 1]) / 64 for i in range(1, 40)])
     assert 0.65 <= overlap <= 0.8
+
+
+# ----------------------------------------------------------------------------- top-k selection
+
+
+@pytest.mark.parametrize("case", _golden.topk_cases(), ids=lambda c: c["name"])
+def test_topk_hand_worked_cases(case):
+    lens = None if case["len"] is None else np.array([case["len"]], np.int32)
+    got = oracle.topk_select(case["scores"][None, :], case["K"], lens=lens)[0]
+    assert np.array_equal(got, case["expect"]), (got, case["expect"])
+
+
+def _topk_by_rank_count(row, K, length):
+    """Position j is kept iff fewer than K candidates outrank it (greater score, or an equal
+    score at a lower position; NaN below every number): a quadratic count, written apart
+    from the oracle's sorts."""
+    def beats(a, b):
+        xa, xb = row[a], row[b]
+        if np.isnan(xa) or np.isnan(xb):
+            if np.isnan(xa) and np.isnan(xb):
+                return a < b
+            return np.isnan(xb)
+        return xa > xb or (xa == xb and a < b)
+    kept = [j for j in range(length) if sum(beats(i, j) for i in range(length) if i != j) < K]
+    return np.array(kept + [-1] * (K - len(kept)), np.int32)
+
+
+def test_topk_matches_rank_counting_on_random_rows_with_ties():
+    rng = np.random.default_rng(11)
+    for trial in range(60):
+        n = int(rng.integers(1, 40))
+        K = int(rng.integers(1, 20))
+        # few distinct values, some NaN / infinities / signed zeros, so ties are common
+        pool = np.array([0.0, -0.0, 1.0, -1.0, 2.5, np.inf, -np.inf, np.nan], np.float32)
+        row = rng.choice(pool, size=n).astype(np.float32)
+        length = int(rng.integers(0, n + 1))
+        got = oracle.topk_select(row[None, :], K, lens=np.array([length], np.int32))[0]
+        assert np.array_equal(got, _topk_by_rank_count(row, K, length)), (trial, row, K, length, got)
+
+
+def test_topk_output_invariants():
+    rng = np.random.default_rng(12)
+    T, N, K = 6, 300, 64
+    scores = rng.standard_normal((T, N)).astype(np.float32)
+    lens = np.array([0, 1, 63, 64, 65, 300], np.int32)
+    out = oracle.topk_select(scores, K, lens=lens)
+    for t in range(T):
+        m = min(K, int(lens[t]))
+        kept = out[t, :m]
+        assert np.all(out[t, m:] == -1)
+        assert np.all(np.diff(kept) > 0) and (m == 0 or (kept[0] >= 0 and kept[-1] < lens[t]))
+        if 0 < m < lens[t]:
+            # every kept score is at least every dropped one
+            dropped = np.setdiff1d(np.arange(lens[t]), kept)
+            assert scores[t, kept].min() >= scores[t, dropped].max()
