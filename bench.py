@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["svt", "reference"], default="svt")
     ap.add_argument("--no-prefill", action="store_true", help="skip the grouped-prefill line item")
+    ap.add_argument("--no-topk", action="store_true", help="skip the top-k selection line item")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--decode-T", type=int, default=64, help="decode batch size (64 = the benchmark workload)")
@@ -343,7 +344,7 @@ def main():
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     # one attention kernel per decode call, plus the split merge when any query's list is split
     # between CTAs (the workspace then holds partial results beyond the status header)
-    ws_need = S.lib().svt_sparse_mla_decode_workspace_size(w.T, w.H, w.K, 0)
+    ws_need = S.svt.lib().svt_sparse_mla_decode_workspace_size(w.T, w.H, w.K, 0)
     launches_per_step = 2 if ws_need > 256 else 1
 
     def step():
@@ -394,6 +395,27 @@ def main():
         e2e = {"value": replica_throughput(w.T, ems, world), "unit": UNIT, "ms_per_step": ems,
                "h2d_bytes_per_step": q_h.numel() * 2 + topk_h.numel() * 4,
                "d2h_bytes_per_step": out_h.numel() * 2 + lse_h.numel() * 4}
+
+    # ---- top-k selection line item (the indexer's last step, on the decode batch's contexts)
+    topk_item = None
+    if not args.no_topk:
+        tw = W.topk_batch(args.decode_T)
+        t_scores = torch.from_numpy(tw.scores).to(dev)
+        t_lens = torch.from_numpy(tw.lens).to(dev)
+        t_out = torch.empty((tw.T, tw.K), dtype=torch.int32, device=dev)
+
+        def topk_step():
+            S.topk_select(t_scores, tw.K, lens=t_lens, out=t_out)
+
+        for _ in range(max(3, args.warmup)):
+            topk_step()
+        torch.cuda.synchronize()
+        tt = time_steps(topk_step, max(3, args.steps // 2), flush, stream)
+        t_ms = statistics.mean(tt)
+        t_bytes = float(tw.lens.astype(np.int64).sum() * 4 + tw.T * tw.K * 4)  # scores read once, lists written
+        topk_item = {"workload": tw.name, "ms": round(t_ms, 4), "queries_per_s": tw.T / (t_ms / 1e3),
+                     "algorithmic_bytes": t_bytes, "gbs": t_bytes / (t_ms / 1e3) / 1e9,
+                     "frac_of_hbm_peak": t_bytes / (t_ms / 1e3) / 1e9 / hbm_peak}
 
     # ---- grouped prefill line item (union + attention)
     prefill = None
@@ -462,6 +484,7 @@ def main():
                          "algorithmic_bytes": nb["algorithmic"], "peak_source": peak_src, "source_hash": th},
             "clocks": clk, "gpu_launches": launches_per_step * args.steps, "e2e": e2e, "cpu_baseline": cpu,
             "prefill": prefill,
+            "topk": topk_item,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

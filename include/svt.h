@@ -219,6 +219,22 @@ SVT_API svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T,
 SVT_API svt_status svt_merge_splits(const float* o_part, const float* lse_part, int32_t S, int32_t T, int32_t H,
                             void* out_bf16, float* lse, svt_stream_t stream);
 
+/*
+ * Top-k selection, the last step of the indexer that produces the lists above ("The Virtual
+ * Block Table", Input Knowledge Required, item 3: the DSA indexer produces top-k sparse
+ * indices per token; the pages name no selection rule, so this is the reading used here).
+ * For each query t the candidates are positions 0..len_t-1; the K largest scores are kept.
+ * Equal scores (+0 and -0 are equal) go to the lower position first; a NaN score ranks
+ * below every number.
+ *   scores    [T, N] fp32, row t starting at scores + t * stride (stride >= N elements).
+ *   lens      [T] int32 candidates per query, clamped to [0, N]; NULL means N for all.
+ *   topk_out  [T, K] int32: the kept positions in ascending order, then -1 up to K (the
+ *             -1-padded list svt_resolve_topk_slots and svt_sparse_mla_decode take).
+ * K >= 1. No workspace; the call only enqueues one kernel.
+ */
+SVT_API svt_status svt_topk_select(const float* scores, int32_t T, int32_t N, int64_t stride, const int32_t* lens,
+                                   int32_t K, int32_t* topk_out, svt_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

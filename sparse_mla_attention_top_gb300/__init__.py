@@ -17,4 +17,5 @@ from .svt import (  # noqa: F401
     resolve_topk_slots,
     sparse_mla_decode,
     sparse_mla_prefill_grouped,
+    topk_select,
 )

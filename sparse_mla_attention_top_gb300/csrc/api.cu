@@ -328,4 +328,16 @@ svt_status svt_merge_splits(const float* o_part, const float* lse_part, int32_t 
   return SVT_OK;
 }
 
+svt_status svt_topk_select(const float* scores, int32_t T, int32_t N, int64_t stride, const int32_t* lens, int32_t K,
+                           int32_t* topk_out, svt_stream_t stream) {
+  if (T < 0 || N < 0) return fail(SVT_ERR_INVALID_ARG, "T and N must be >= 0");
+  if (K < 1) return fail(SVT_ERR_INVALID_ARG, "K must be >= 1");
+  if (stride < N) return fail(SVT_ERR_INVALID_ARG, "stride %lld is below N %d", static_cast<long long>(stride), N);
+  if (T == 0) return SVT_OK;
+  if (topk_out == nullptr || (N > 0 && scores == nullptr)) return fail(SVT_ERR_INVALID_ARG, "null array argument");
+  cudaError_t e = svt::launch_topk(scores, T, N, stride, lens, K, topk_out, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "top-k launch");
+  return SVT_OK;
+}
+
 }  // extern "C"

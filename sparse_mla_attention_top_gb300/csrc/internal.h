@@ -118,6 +118,9 @@ cudaError_t launch_union(const int32_t* slots, const int32_t* topk_len, int T, i
 cudaError_t launch_merge_splits(const float* o_part, const float* lse_part, int S, long long rows, int H_rows,
                                 uint16_t* out, float* lse, cudaStream_t stream);
 
+cudaError_t launch_topk(const float* scores, int T, int N, long long stride, const int32_t* lens, int K, int32_t* out,
+                        cudaStream_t stream);
+
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
 // Merges the partial results of the row-sets a stream-K decode split between CTAs; launched
 // right behind the attention kernel (programmatic dependent launch) and waiting for it.

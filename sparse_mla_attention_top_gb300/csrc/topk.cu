@@ -1,0 +1,224 @@
+// Top-k selection, the last step of the indexer that feeds the sparse path ("The Virtual
+// Block Table: Reusing Triton MLA for Sparse Attention on Blackwell GPUs", Input Knowledge
+// Required, item 3: the DSA indexer produces top-k sparse indices per token). For query t
+// the candidates are positions 0..len_t-1; the K largest scores are kept (equal scores go
+// to the lower position, +0 equals -0, NaN ranks below every number) and written in
+// ascending position order, then -1 up to K.
+//
+// One CTA per query. Scores become order-preserving 32-bit keys (NaN -> 0, the lowest),
+// kept in shared memory when the row fits. A most-significant-digit-first radix select
+// (four 8-bit digits, per-warp shared histograms) finds the K-th largest key exactly and
+// how many keys equal to it are kept; one ordered pass then compacts the kept positions
+// with warp ballots and a block-wide scan, so the output is ascending by construction.
+#include <cstdint>
+
+#include "internal.h"
+
+namespace svt {
+
+namespace {
+
+constexpr int kTopkThreads = 1024;
+constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kKeysInSmemMax = 46 * 1024;  // 184 KB of keys; longer rows are read from global memory
+
+// Order-preserving key: larger score -> larger key; equal scores (with -0 == +0) -> equal
+// keys; NaN -> 0, below the key of -inf (0x007FFFFF).
+__device__ __forceinline__ uint32_t score_key(float x) {
+  if (x != x) return 0u;
+  uint32_t u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0u;  // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+constexpr int kBatch = 8;  // positions per thread per compaction round
+
+struct TopkShared {
+  uint32_t hist[256];
+  uint32_t cnt[kBatch * kTopkWarps];  // per-(batch slot, warp) counts of the current round
+  uint32_t off[kBatch * kTopkWarps];  // their exclusive prefix in position order
+  uint32_t total;
+  uint32_t digit, above;
+};
+
+// keys + per-warp histograms (dynamic) + the block's scalars (static) within 227 KB
+static_assert(kKeysInSmemMax * 4 + kTopkWarps * 256 * 4 + sizeof(TopkShared) <= 232448, "top-k smem budget");
+
+// Exclusive prefix of sh.cnt (256 values in position order) into sh.off, total into
+// sh.total; run by warp 0, lane l taking values 8l .. 8l + 7.
+__device__ __forceinline__ void scan_counts(TopkShared& sh, int lane) {
+  uint32_t v[8], tot = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    v[i] = sh.cnt[8 * lane + i];
+    tot += v[i];
+  }
+  uint32_t incl = tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  uint32_t acc = incl - tot;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    sh.off[8 * lane + i] = acc;
+    acc += v[i];
+  }
+  if (lane == 31) sh.total = incl;
+}
+
+__global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ scores, int N, long long stride,
+                                                             const int32_t* __restrict__ lens, int K,
+                                                             int32_t* __restrict__ out) {
+  extern __shared__ uint32_t dyn_smem[];
+  uint32_t* warp_hist = dyn_smem;                   // [32 warps][256 bins]
+  uint32_t* keys_smem = dyn_smem + kTopkWarps * 256;  // the row's keys, when they fit
+  __shared__ TopkShared sh;
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int len = lens ? lens[t] : N;
+  len = len < 0 ? 0 : (len > N ? N : len);
+  const float* row = scores + static_cast<long long>(t) * stride;
+  int32_t* dst = out + static_cast<long long>(t) * K;
+
+  if (len <= K) {  // every candidate is kept
+    for (int j = tid; j < K; j += kTopkThreads) dst[j] = j < len ? j : -1;
+    return;
+  }
+  const bool in_smem = len <= kKeysInSmemMax;
+  if (in_smem) {
+    // eight loads in flight per thread, then their keys
+#pragma unroll 1
+    for (int j0 = 0; j0 < len; j0 += 8 * kTopkThreads) {
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u * kTopkThreads + tid;
+        v[u] = j < len ? __ldg(row + j) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u * kTopkThreads + tid;
+        if (j < len) keys_smem[j] = score_key(v[u]);
+      }
+    }
+  }
+
+  // radix select: find thr = the K-th largest key, and `need` = how many keys equal to thr
+  // are kept (the ones at the lowest positions)
+  uint32_t prefix = 0, prefix_mask = 0;
+  uint32_t rank = static_cast<uint32_t>(K);  // 1-based rank still to find among the matching keys
+  uint32_t* my_hist = warp_hist + warp * 256;
+#pragma unroll 1
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int b = lane; b < 256; b += 32) my_hist[b] = 0;
+    __syncthreads();
+    // one histogram per warp, so warps never contend with each other
+    for (int j = tid; j < len; j += kTopkThreads) {
+      const uint32_t k = in_smem ? keys_smem[j] : score_key(__ldg(row + j));
+      if ((k & prefix_mask) == prefix) atomicAdd(&my_hist[(k >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (tid < 256) {
+      uint32_t c = 0;
+#pragma unroll 8
+      for (int w = 0; w < kTopkWarps; ++w) c += warp_hist[w * 256 + tid];
+      sh.hist[tid] = c;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // bins from the top: lane l owns bins 255 - 8l .. 248 - 8l
+      uint32_t c[8], tot = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        c[i] = sh.hist[255 - 8 * lane - i];
+        tot += c[i];
+      }
+      uint32_t incl = tot;  // inclusive prefix over lanes (higher bins first)
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += v;
+      }
+      const uint32_t excl = incl - tot;
+      // the lane whose range contains the rank-th key
+      if (excl < rank && rank <= incl) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (acc < rank && rank <= acc + c[i]) {
+            sh.digit = 255u - 8u * lane - i;
+            sh.above = acc;
+          }
+          acc += c[i];
+        }
+      }
+    }
+    __syncthreads();
+    prefix |= sh.digit << shift;
+    prefix_mask |= 255u << shift;
+    rank -= sh.above;
+  }
+  const uint32_t thr = prefix;
+  const uint32_t need = rank;  // keys equal to thr to keep, lowest positions first
+
+  // ordered compaction: kept = key > thr, or key == thr among the first `need` equal ones.
+  // A round covers kBatch x 1024 positions: slot u of thread (warp, lane) is position
+  // j0 + 1024 u + 32 warp + lane, so (u, warp, lane) is position order.
+  uint32_t base_out = 0, base_eq = 0;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+#pragma unroll 1
+  for (int j0 = 0; j0 < len; j0 += kBatch * kTopkThreads) {
+    uint32_t key[kBatch], eq_b[kBatch], kept_b[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = j0 + u * kTopkThreads + tid;
+      key[u] = j < len ? (in_smem ? keys_smem[j] : score_key(__ldg(row + j))) : 0u;
+      eq_b[u] = __ballot_sync(0xffffffffu, j < len && key[u] == thr);
+      if (lane == 0) sh.cnt[u * kTopkWarps + warp] = __popc(eq_b[u]);
+    }
+    __syncthreads();
+    if (warp == 0) scan_counts(sh, lane);
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = j0 + u * kTopkThreads + tid;
+      const bool eq = (eq_b[u] >> lane) & 1u;
+      const uint32_t eq_before = base_eq + sh.off[u * kTopkWarps + warp] + __popc(eq_b[u] & lt_mask);
+      const bool kept = (j < len && key[u] > thr) || (eq && eq_before < need);
+      kept_b[u] = __ballot_sync(0xffffffffu, kept);
+    }
+    base_eq += sh.total;
+    __syncthreads();  // the equal-key offsets are read
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u)
+      if (lane == 0) sh.cnt[u * kTopkWarps + warp] = __popc(kept_b[u]);
+    __syncthreads();
+    if (warp == 0) scan_counts(sh, lane);
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const uint32_t pos = base_out + sh.off[u * kTopkWarps + warp] + __popc(kept_b[u] & lt_mask);
+      // exactly K are kept; the bound is a guard
+      if (((kept_b[u] >> lane) & 1u) && pos < static_cast<uint32_t>(K)) dst[pos] = j0 + u * kTopkThreads + tid;
+    }
+    base_out += sh.total;
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const float* scores, int T, int N, long long stride, const int32_t* lens, int K, int32_t* out,
+                        cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  const int smem_keys = (N < kKeysInSmemMax ? N : kKeysInSmemMax);
+  const size_t smem = (static_cast<size_t>(kTopkWarps) * 256 + smem_keys) * sizeof(uint32_t);
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  topk_kernel<<<T, kTopkThreads, smem, stream>>>(scores, N, stride, lens, K, out);
+  return cudaGetLastError();
+}
+
+}  // namespace svt

@@ -32,6 +32,7 @@ EXPORTED = [
     "svt_resolve_topk_slots", "svt_sparse_mla_decode_workspace_size", "svt_sparse_mla_decode",
     "svt_build_group_union_workspace_size", "svt_build_group_union",
     "svt_sparse_mla_prefill_grouped_workspace_size", "svt_sparse_mla_prefill_grouped", "svt_merge_splits",
+    "svt_topk_select",
     "svt_sparse_mla_decode_noalloc",
 ]
 
@@ -76,6 +77,7 @@ def lib():
         L.svt_sparse_mla_prefill_grouped.argtypes = [P, i32, i32, i32, ctypes.POINTER(_KV), P, P, i32, f32, P, P, P,
                                                      sz, P]
         L.svt_merge_splits.argtypes = [P, P, i32, i32, i32, P, P, P]
+        L.svt_topk_select.argtypes = [P, i32, i32, i64, P, i32, P, P]
         L.svt_sparse_mla_decode_noalloc.argtypes = [P, i32, i32, ctypes.POINTER(_KV), P, i32, i32, P, P, P, i32, P, f32,
                                                     P, P, i32, P, P]
         _lib = L
@@ -255,3 +257,19 @@ def merge_splits(o_part, lse_part, *, out=None, lse=None, return_lse: bool = Tru
     _check(lib().svt_merge_splits(_ptr(o_part), _ptr(lse_part), S, T, H, _ptr(out),
                                   _ptr(lse), _stream()), "svt_merge_splits")
     return out, lse
+
+
+def topk_select(scores, K: int, *, lens=None, out=None):
+    """svt_topk_select: scores [T, N] fp32 (rows may be strided) -> [T, K] int32 positions,
+    ascending, -1 padded."""
+    if scores.dtype != torch.float32 or scores.dim() != 2 or scores.stride(1) != 1:
+        raise TypeError("scores must be a [T, N] fp32 tensor with unit column stride")
+    T, N = scores.shape
+    if lens is not None:
+        lens = _i32(lens, "lens")
+    if out is None:
+        out = torch.empty((T, K), dtype=torch.int32, device=scores.device)
+    stride = scores.stride(0) if T > 1 else N  # a single row's stride is meaningless (can be 0)
+    _check(lib().svt_topk_select(_ptr(scores), T, N, stride, _ptr(lens), int(K), _ptr(out), _stream()),
+           "svt_topk_select")
+    return out

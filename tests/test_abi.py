@@ -125,6 +125,15 @@ def test_resolve_and_merge_reject_bad_arguments(L):
     assert st == svt.SVT_ERR_INVALID_ARG
 
 
+def test_topk_rejects_bad_arguments(L):
+    P = ctypes.c_void_p
+    assert L.svt_topk_select(P(0x20000), 4, 100, 100, None, 0, P(0x30000), None) == svt.SVT_ERR_INVALID_ARG  # K 0
+    assert L.svt_topk_select(P(0x20000), 4, 100, 99, None, 8, P(0x30000), None) == svt.SVT_ERR_INVALID_ARG  # stride
+    assert L.svt_topk_select(None, 4, 100, 100, None, 8, P(0x30000), None) == svt.SVT_ERR_INVALID_ARG
+    assert L.svt_topk_select(P(0x20000), -1, 100, 100, None, 8, P(0x30000), None) == svt.SVT_ERR_INVALID_ARG
+    assert L.svt_topk_select(None, 0, 100, 100, None, 8, None, None) == svt.SVT_OK  # nothing to do
+
+
 def test_workspace_sizes(L):
     assert L.svt_resolve_workspace_size() == 256
     assert L.svt_build_group_union_workspace_size(8192, 2048, 2) >= 256
