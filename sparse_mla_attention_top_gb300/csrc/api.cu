@@ -308,7 +308,8 @@ svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T, int32_t
   if (sms <= 0) sms = 1;
   p.num_ctas = p.num_rowsets < sms ? p.num_rowsets : sms;
   p.status = static_cast<int*>(ws);
-  cudaError_t e = svt::launch_attention(p, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = kv->dtype == SVT_KV_BF16 ? svt::launch_prefill(p, reinterpret_cast<cudaStream_t>(stream))
+                                           : svt::launch_attention(p, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
   return SVT_OK;
 }

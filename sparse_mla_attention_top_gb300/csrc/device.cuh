@@ -49,6 +49,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One non-blocking test of the phase (the thread is never suspended).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase of `bar` with the given parity to complete. Bounded: after
 // kWaitLimitNs it records SVT_DEV_ERR_TIMEOUT, raises the CTA's abort flag and returns
 // false; once the abort flag is up every later wait returns at once, so each role runs its
@@ -100,6 +113,11 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Makes `bar` receive one arrival when every cp.async this thread issued so far has landed
+// (the barrier's count includes this arrival; the thread does not wait).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 
 // Orders this thread's generic-proxy shared-memory writes (st.shared, completed cp.async)
 // before later async-proxy reads of them (tcgen05.mma operands).

@@ -122,6 +122,9 @@ cudaError_t launch_topk(const float* scores, int T, int N, long long stride, con
                         cudaStream_t stream);
 
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
+// Grouped prefill over a bf16 cache with two 64-row half-tile stages (e4m3 caches use
+// launch_attention).
+cudaError_t launch_prefill(const AttnParams& p, cudaStream_t stream);
 // Merges the partial results of the row-sets a stream-K decode split between CTAs; launched
 // right behind the attention kernel (programmatic dependent launch) and waiting for it.
 cudaError_t launch_streamk_merge(const AttnParams& p, cudaStream_t stream);

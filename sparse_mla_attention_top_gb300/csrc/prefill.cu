@@ -1,0 +1,571 @@
+// Grouped sparse MLA prefill (bf16 cache) on tcgen05 tensor cores, with two shared-memory
+// stages of 64-row half-tiles so that gathering, the two contractions and the softmax
+// overlap.
+//
+// What it computes (vLLM PR #63104, Overview: 2/4/8 consecutive queries share one 128-row
+// tile over the sorted union of their top-k rows; each row sees only the union entries whose
+// membership bit is its query's; bench script: 512 latent + 64 rope, K is the whole row, V
+// its first 512 columns): for each of the 64 packed query rows of a row-set (half of a
+// group's 128) and the group's union list,
+//   s_j = scale * q . k_j,  out = softmax(s) . V,  lse = ln sum_j exp(s_j)
+// over the live entries of the row (membership bit set).
+//
+// GB300 design. A half-tile is 64 union entries; per half-tile
+//   S^T[64 x 64]   = K_half[64 x 576] . Q^T     (M = 64: 36 MMAs of K = 16)
+//   O^T[512 x 64] += V_half^T[512 x 64] . P^T   (4 M-blocks of 128 channels x 4 MMAs)
+// S^T is double-buffered in TMEM (M = 64 layout: rows in lanes 0-15 of each 32-lane
+// quadrant), O^T takes 4 x 64 columns. While the softmax works on half-tile g, the tensor
+// cores run PV(g-1) and S(g+1) and the loaders' cp.async rows of half-tile g+2... land in the
+// stage PV(g) frees, so the serial chain S -> softmax -> PV of a single-stage pipeline is
+// gone; the M = 64 S^T costs the same cycles per MMA as M = 128, which is the price.
+//
+// Warp roles (512 threads):
+//   warps 0-7   softmax + epilogue: warp w reads TMEM quadrant w % 4 (KV rows 16 (w % 4) +
+//               lane, lanes 0-15) and query columns 32 (w / 4) .. + 31; online softmax in
+//               fp32 with a lazily moved reference maximum; P^T goes into the stage's rope
+//               block; each thread keeps its row's share of the column sums.
+//   warp 8      S^T issuer (lane 0), warp 9 PV issuer (lane 0): an MMA issue blocks while the
+//               tensor pipe's queue is full, so one thread issuing both would hold PV behind
+//               the next S^T; each thread commits its own MMAs.
+//   warps 10-15 loaders: resolve the next half-tile's union words and load its 64 rows into
+//               registers (24 x 16 bytes per thread) while both stages are busy; the moment
+//               PV frees a stage, they store it there, so a half-tile's gather latency is
+//               hidden behind the previous stage cycle.
+// Persistent CTAs take whole row-sets round-robin.
+#include <cuda_fp16.h>
+#include <math_constants.h>
+
+#include "device.cuh"
+#include "internal.h"
+
+namespace svt {
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kSmThreads = 256;  // warps 0-7
+constexpr int kSIssuerWarp = 8;   // issues S^T
+constexpr int kPvIssuerWarp = 9;  // issues PV
+constexpr int kLdWarp0 = 10;
+constexpr int kLdThreads = 192;  // warps 10-15
+constexpr int kHalf = 64;        // KV rows per half-tile
+constexpr int kBlocks = 9;
+constexpr int kBlk = kHalf * 128;  // 8 KB: 64 rows x 64 bf16
+constexpr int kStageBytes = kBlocks * kBlk;
+constexpr int kQBlk = kRowsetRows * 128;  // 8 KB
+constexpr float kTau = 8.0f;
+constexpr int kHalfChunks = kHalf * kBlocks * 8;  // 16-byte chunks of a half-tile: 4608
+constexpr int kChunksPerLoader = kHalfChunks / kLdThreads;  // 24
+static_assert(kHalfChunks % kLdThreads == 0, "");
+
+// shared memory map (offsets from a 1024-aligned base)
+constexpr int kOffQ = 0;
+constexpr int kOffStage = kOffQ + kBlocks * kQBlk;      // 73728: stage s at + s * kStageBytes
+constexpr int kSlotRing = 4;                           // resolved half-tiles in flight
+constexpr int kOffSlot = kOffStage + 2 * kStageBytes;  // 221184: int[4][64]
+constexpr int kOffMask = kOffSlot + kSlotRing * kHalf * 4;  // uint[4][64]
+constexpr int kOffMref = kOffMask + kSlotRing * kHalf * 4;  // float[64]
+constexpr int kOffAlpha = kOffMref + kRowsetRows * 4;  // float[64]
+constexpr int kOffRed = kOffAlpha + kRowsetRows * 4;   // float[8][32]
+constexpr int kOffLfin = kOffRed + 8 * 32 * 4;         // float[64]
+constexpr int kOffBars = kOffLfin + kRowsetRows * 4;   // uint64[16]
+constexpr int kOffMisc = kOffBars + 16 * 8;            // tmem base, abort flag
+constexpr int kSmemUsed = kOffMisc + 16;
+constexpr int kSmemBytes = kSmemUsed + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory map exceeds 227 KB");
+
+// barriers (stage / buffer pairs at +0, +1)
+constexpr int kBarQFull = 0;   // loaders' Q^T copies landed (cp.async arrivals)
+constexpr int kBarQEmpty = 1;  // last S^T of the row-set issued and done
+constexpr int kBarFull = 2;    // 2: a half-tile's rows landed in stage s
+constexpr int kBarEmpty = 4;   // 2: PV done with stage s
+constexpr int kBarSFull = 6;   // 2: S^T buffer b ready
+constexpr int kBarPready = 8;  // 2: P^T of the half-tile in stage s written
+constexpr int kBarPvDone = 10; // 2: PV of the half-tile in stage s done
+constexpr int kBarOFree = 12;  // the row-set's epilogue has read O^T
+
+constexpr int kTmemCols = 512;
+constexpr int kTmemS = 0;    // S^T buffer b: columns 64 b .. + 63 (lanes 0-15 of each quadrant)
+constexpr int kTmemO = 128;  // O^T M-block mb: columns 128 + 64 mb .. + 63
+
+constexpr int kNamedBarSm = 1;
+constexpr int kNamedBarLd = 2;
+
+constexpr uint32_t kIdescS = idesc_f32acc(64, 64, 0, 0, kFmtBf16);
+constexpr uint32_t kIdescPV = idesc_f32acc(128, 64, 1, 1, kFmtBf16);
+
+// The CTA's row-sets (round-robin) and each one's union length.
+struct RowsetWalk {
+  int next;
+  __device__ bool advance(const AttnParams& p, int& r, int& len) {
+    if (next >= p.num_rowsets) return false;
+    r = next;
+    next += p.num_ctas;
+    const int l = p.lens[r >> 1];
+    len = l < 0 ? 0 : (l > p.list_stride ? p.list_stride : l);
+    return true;
+  }
+};
+
+__device__ __forceinline__ int halves_of(int len) { return (len + kHalf - 1) / kHalf; }
+
+// Prefill: which query columns of 32-column half h of row-set half `rpar` a KV row is live
+// for, given its membership bits mk. Column c is packed row 64 rpar + 32 h + c, member
+// (64 rpar + 32 h + c) / H (H >= 16, so a half spans at most two members).
+__device__ __forceinline__ uint32_t live_columns(uint32_t mk, int rpar, int h, int H) {
+  const int packed0 = rpar * kRowsetRows + 32 * h;
+  const int lo = packed0 / H, hi = (packed0 + 31) / H;
+  const uint32_t split_hi = (hi != lo) ? (0xFFFFFFFFu << (H - (packed0 - lo * H))) : 0u;
+  return (((mk >> lo) & 1u) ? ~split_hi : 0u) | (((mk >> hi) & 1u) ? split_hi : 0u);
+}
+
+// Transposed reductions over the warp's 32 lanes: lane c ends with column c (v consumed).
+__device__ __forceinline__ float warp_column_max(float (&v)[32], int lane) {
+#pragma unroll
+  for (int half = 16; half >= 1; half >>= 1) {
+    const bool up = (lane & half) != 0;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float send = up ? v[k] : v[k + half];
+      const float keep = up ? v[k + half] : v[k];
+      v[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, half));
+    }
+  }
+  return v[0];
+}
+__device__ __forceinline__ float warp_column_sum(float (&v)[32], int lane) {
+#pragma unroll
+  for (int half = 16; half >= 1; half >>= 1) {
+    const bool up = (lane & half) != 0;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float send = up ? v[k] : v[k + half];
+      const float keep = up ? v[k + half] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+    }
+  }
+  return v[0];
+}
+
+constexpr int kDeadEntry = -2147483647 - 1;
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* ptr) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(ptr));
+  return v;
+}
+
+// ---------------------------------------------------------------------------------- loaders
+// Walks the CTA's half-tiles in order across row-sets (skipping empty row-sets).
+struct HalfCursor {
+  RowsetWalk walk;
+  int r, len, nh, i;
+  __device__ bool next(const AttnParams& p) {
+    while (++i >= nh) {
+      if (!walk.advance(p, r, len)) return false;
+      nh = halves_of(len);
+      i = -1;
+    }
+    return true;
+  }
+};
+
+__device__ void loader_role(const AttnParams& p, uint8_t* smem, uint32_t bars, volatile int* abort_flag) {
+  const int ltid = static_cast<int>(threadIdx.x) - kLdWarp0 * 32;
+  const uint32_t sbase = smem_u32(smem);
+  int* slot_tab = reinterpret_cast<int*>(smem + kOffSlot);
+  uint32_t* mask_tab = reinterpret_cast<uint32_t*>(smem + kOffMask);
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+  const uint8_t* qb = reinterpret_cast<const uint8_t*>(p.q);
+  int err = 0;
+  uint32_t qk = 0;
+  HalfCursor cur{{static_cast<int>(blockIdx.x)}, 0, 0, 0, 0};
+  if (!cur.next(p)) return;
+
+  // entry ltid (< 64) of the cursor's half-tile -> slot / mask table k % 4
+  auto resolve = [&](uint32_t k) {
+    if (ltid < kHalf) {
+      const int e = cur.i * kHalf + ltid;
+      const int raw = e < cur.len ? __ldg(p.enc + static_cast<long long>(cur.r >> 1) * p.list_stride + e) : kDeadEntry;
+      int slot = -1;
+      uint32_t mask = 0;
+      const uint32_t w = static_cast<uint32_t>(raw);
+      if (raw != kDeadEntry && w != 0xFFFFFFFFu) {
+        const int sl = static_cast<int>(w & 0xFFFFFFu);
+        if (static_cast<long long>(sl) < p.num_slots) {
+          slot = sl;
+          mask = w >> 24;
+        } else {
+          err = 1;
+        }
+      }
+      slot_tab[(k % kSlotRing) * kHalf + ltid] = slot;
+      mask_tab[(k % kSlotRing) * kHalf + ltid] = mask;
+    }
+    named_bar_sync(kNamedBarLd, kLdThreads);
+  };
+  // Q^T of the cursor's row-set, once the previous row-set's last S^T is done with the old one
+  auto load_q = [&]() {
+    mbar_wait(bar(kBarQEmpty), (qk & 1u) ^ 1u, p.status, abort_flag);
+    const RowsetRows rr = rowset_rows(p, cur.r);
+    for (int idx = ltid; idx < kRowsetRows * 72; idx += kLdThreads) {
+      const int row = idx / 72, c = idx - row * 72;
+      const bool valid = row < rr.nvalid;
+      const uint8_t* src = qb + (valid ? (rr.base + row) * (kRow * 2) + c * 16 : 0);
+      cp_async16(sbase + kOffQ + (c >> 3) * kQBlk + sw128_offset(row, c & 7), src, valid ? 16u : 0u);
+    }
+    cp_async_arrive_noinc(bar(kBarQFull));
+    ++qk;
+  };
+  uint4 v[kChunksPerLoader];
+  auto issue = [&](uint32_t k) {
+    const int* slots = slot_tab + (k % kSlotRing) * kHalf;
+#pragma unroll
+    for (int u = 0; u < kChunksPerLoader; ++u) {
+      const int idx = ltid + u * kLdThreads;
+      const int blk = idx >> 9, row = (idx >> 3) & (kHalf - 1), chunk = idx & 7;
+      const int slot = slots[row];
+      v[u] = slot >= 0 ? ldg_nc_v4(p.kv + static_cast<long long>(slot) * p.row_stride + blk * 128 + chunk * 16)
+                       : make_uint4(0, 0, 0, 0);
+    }
+  };
+
+  resolve(0);
+  issue(0);
+  load_q();
+  for (uint32_t g = 0;; ++g) {
+    const uint32_t st = g & 1u;
+    // stage st is free once PV of the half-tile two back is done
+    mbar_wait(bar(kBarEmpty + st), ((g >> 1) & 1u) ^ 1u, p.status, abort_flag);
+    uint8_t* stage = smem + kOffStage + st * kStageBytes;
+#pragma unroll
+    for (int u = 0; u < kChunksPerLoader; ++u) {
+      const int idx = ltid + u * kLdThreads;
+      const int blk = idx >> 9, row = (idx >> 3) & (kHalf - 1), chunk = idx & 7;
+      *reinterpret_cast<uint4*>(stage + blk * kBlk + sw128_offset(row, chunk)) = v[u];
+    }
+    fence_proxy_async_smem();
+    mbar_arrive(bar(kBarFull + st));
+    if (*abort_flag) break;
+    // the next half-tile: resolve it and put its rows in flight; a new row-set also needs Q^T
+    const int prev_r = cur.r;
+    if (!cur.next(p)) break;
+    resolve(g + 1);
+    issue(g + 1);
+    if (cur.r != prev_r) load_q();
+  }
+  cp_async_wait_all();
+  if (__any_sync(0xffffffffu, err) && (threadIdx.x & 31) == 0) atomicOr(p.status, SVT_DEV_ERR_INDEX_RANGE);
+}
+
+// ---------------------------------------------------------------------------------- issuers
+// S^T(g) into TMEM buffer g % 2 from stage g % 2, once the stage holds half-tile g and the
+// softmax is done with the buffer's previous contents (half-tile g - 2).
+__device__ void s_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars,
+                              volatile int* abort_flag) {
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+  uint32_t g = 0, qk = 0;
+  RowsetWalk walk{static_cast<int>(blockIdx.x)};
+  int r, len;
+  while (walk.advance(p, r, len)) {
+    const int nh = halves_of(len);
+    if (nh == 0) continue;
+    mbar_wait(bar(kBarQFull), qk & 1u, p.status, abort_flag);
+    ++qk;
+    for (int i = 0; i < nh; ++i, ++g) {
+      const uint32_t b = g & 1u;
+      if (g >= 2) mbar_wait(bar(kBarPready + b), ((g - 2) >> 1) & 1u, p.status, abort_flag);
+      mbar_wait(bar(kBarFull + b), (g >> 1) & 1u, p.status, abort_flag);
+      tc_fence_after();
+      const uint32_t stage = sbase + kOffStage + b * kStageBytes;
+#pragma unroll 1
+      for (int kb = 0; kb < kBlocks; ++kb) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t a = smem_desc_sw128(stage + kb * kBlk + ks * 32, 16, 1024);
+          const uint64_t bq = smem_desc_sw128(sbase + kOffQ + kb * kQBlk + ks * 32, 16, 1024);
+          umma_f16(tmem + kTmemS + 64 * b, a, bq, kIdescS, (kb | ks) != 0);
+        }
+      }
+      umma_commit(bar(kBarSFull + b));
+      if (i == nh - 1) umma_commit(bar(kBarQEmpty));
+    }
+  }
+}
+
+// PV(g) from stage g % 2 and P^T, once the softmax has written P^T(g) (and, for a row-set's
+// first half-tile, once the previous row-set's epilogue has read O^T).
+__device__ void pv_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars,
+                               volatile int* abort_flag) {
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+  uint32_t g = 0, qk = 0;
+  RowsetWalk walk{static_cast<int>(blockIdx.x)};
+  int r, len;
+  while (walk.advance(p, r, len)) {
+    const int nh = halves_of(len);
+    if (nh == 0) continue;
+    if (qk > 0) mbar_wait(bar(kBarOFree), (qk - 1) & 1u, p.status, abort_flag);
+    ++qk;
+    for (int i = 0; i < nh; ++i, ++g) {
+      const uint32_t b = g & 1u;
+      mbar_wait(bar(kBarPready + b), (g >> 1) & 1u, p.status, abort_flag);
+      tc_fence_after();
+      const uint32_t stage = sbase + kOffStage + b * kStageBytes;
+      const uint32_t pt = stage + 8 * kBlk;
+#pragma unroll
+      for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t a = smem_desc_sw128(stage + (2 * mb) * kBlk + ks * 2048, kBlk, 1024);
+          const uint64_t bp = smem_desc_sw128(pt + ks * 2048, kQBlk, 1024);
+          umma_f16(tmem + kTmemO + 64 * mb, a, bp, kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
+        }
+      }
+      umma_commit(bar(kBarEmpty + b));
+      umma_commit(bar(kBarPvDone + b));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------- softmax
+__device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars,
+                             volatile int* abort_flag) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3, ch = warp >> 2;
+  const int kvrow = 16 * q + lane;  // valid for lane < 16
+  const bool row_lane = lane < 16;
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
+  const int* slot_tab = reinterpret_cast<const int*>(smem + kOffSlot);
+  const uint32_t* mask_tab = reinterpret_cast<const uint32_t*>(smem + kOffMask);
+  float* m_ref = reinterpret_cast<float*>(smem + kOffMref);
+  float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
+  float* red = reinterpret_cast<float*>(smem + kOffRed);
+  float* lfin = reinterpret_cast<float*>(smem + kOffLfin);
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+  uint32_t g = 0;
+  RowsetWalk walk{static_cast<int>(blockIdx.x)};
+  int r, len;
+  float lpart[32];
+  while (walk.advance(p, r, len)) {
+    const int nh = halves_of(len);
+    const int rpar = r & 1;
+    if (threadIdx.x < kRowsetRows) m_ref[threadIdx.x] = -CUDART_INF_F;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) lpart[c] = 0.f;
+    named_bar_sync(kNamedBarSm, kSmThreads);
+    for (int i = 0; i < nh; ++i, ++g) {
+      const uint32_t b = g & 1u;
+      mbar_wait(bar(kBarSFull + b), (g >> 1) & 1u, p.status, abort_flag);
+      tc_fence_after();
+      float x[32];
+      {
+        uint32_t sv[32];
+        tmem_ld32(lane_base + kTmemS + 64 * b + 32 * ch, sv);
+        tmem_ld_wait();
+        uint32_t live = 0;
+        if (row_lane) {
+          const uint32_t k = (g % kSlotRing) * kHalf + kvrow;
+          if (slot_tab[k] >= 0) live = live_columns(mask_tab[k], rpar, ch, p.H);
+        }
+#pragma unroll
+        for (int c = 0; c < 32; ++c) x[c] = ((live >> c) & 1u) ? __uint_as_float(sv[c]) * p.scale_log2 : -CUDART_INF_F;
+      }
+      bool exceed = false;
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 m4 = reinterpret_cast<const float4*>(m_ref)[8 * ch + c4];
+        exceed |= x[4 * c4] > m4.x + kTau;
+        exceed |= x[4 * c4 + 1] > m4.y + kTau;
+        exceed |= x[4 * c4 + 2] > m4.z + kTau;
+        exceed |= x[4 * c4 + 3] > m4.w + kTau;
+      }
+      int any;
+      asm volatile(
+          "{\n\t.reg .pred pi, po;\n\t"
+          "setp.ne.u32 pi, %1, 0;\n\t"
+          "bar.red.or.pred po, %2, %3, pi;\n\t"
+          "selp.u32 %0, 1, 0, po;\n\t}"
+          : "=r"(any)
+          : "r"(static_cast<uint32_t>(exceed)), "r"(kNamedBarSm), "r"(kSmThreads)
+          : "memory");
+      if (any) {
+        // exact column maxima of this half-tile, then move the reference and rescale
+        {
+          float v[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) v[c] = x[c];
+          red[warp * 32 + lane] = warp_column_max(v, lane);
+        }
+        named_bar_sync(kNamedBarSm, kSmThreads);
+        if (threadIdx.x < kRowsetRows) {
+          const int col = threadIdx.x, h = col >> 5, c = col & 31;
+          const float mt = fmaxf(fmaxf(red[(4 * h + 0) * 32 + c], red[(4 * h + 1) * 32 + c]),
+                                 fmaxf(red[(4 * h + 2) * 32 + c], red[(4 * h + 3) * 32 + c]));
+          const float mo = m_ref[col];
+          const float mn = fmaxf(mo, mt);
+          alpha_s[col] = (mo == -CUDART_INF_F) ? 0.f : ex2_approx(mo - mn);
+          m_ref[col] = mn;
+        }
+        named_bar_sync(kNamedBarSm, kSmThreads);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) lpart[c] *= alpha_s[32 * ch + c];
+        if (i > 0) {
+          // O^T holds every PV so far once the previous half-tile's PV is done
+          const uint32_t gp = g - 1;
+          mbar_wait(bar(kBarPvDone + (gp & 1u)), (gp >> 1) & 1u, p.status, abort_flag);
+          tc_fence_after();
+#pragma unroll 1
+          for (int part = 0; part < 8; ++part) {  // 4 M-blocks x my 32 columns in halves
+            uint32_t o[16];
+            const int c0 = 16 * (part & 1);
+            const uint32_t ta = lane_base + kTmemO + 64 * (part >> 1) + 32 * ch + c0;
+            tmem_ld16(ta, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha_s[32 * ch + c0 + c]);
+            tmem_st16(ta, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P^T row (this KV row, my 32 query columns) into the stage's rope block
+      uint32_t pk[16];
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 m4 = reinterpret_cast<const float4*>(m_ref)[8 * ch + c4];
+        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+        float pq[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int c = 4 * c4 + j;
+          pq[j] = (x[c] > -CUDART_INF_F) ? ex2_approx(x[c] - mm[j]) : 0.f;
+          lpart[c] += pq[j];
+        }
+        pk[2 * c4] = pack_bf16x2(pq[0], pq[1]);
+        pk[2 * c4 + 1] = pack_bf16x2(pq[2], pq[3]);
+      }
+      if (row_lane) {
+        uint8_t* prow = smem + kOffStage + b * kStageBytes + 8 * kBlk;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          *reinterpret_cast<uint4*>(prow + sw128_offset(kvrow, 4 * ch + k)) =
+              make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(kBarPready + b));
+    }
+
+    // ------------------------------------------------------------------ epilogue
+    if (nh > 0) {
+      const uint32_t gp = g - 1;
+      mbar_wait(bar(kBarPvDone + (gp & 1u)), (gp >> 1) & 1u, p.status, abort_flag);
+      tc_fence_after();
+    }
+    const RowsetRows rr = rowset_rows(p, r);
+    red[warp * 32 + lane] = warp_column_sum(lpart, lane);  // this warp's 16 rows, column 32 ch + lane
+    named_bar_sync(kNamedBarSm, kSmThreads);
+    if (threadIdx.x < kRowsetRows) {
+      const int col = threadIdx.x, h = col >> 5, c = col & 31;
+      const float l = (red[(4 * h + 0) * 32 + c] + red[(4 * h + 1) * 32 + c]) +
+                      (red[(4 * h + 2) * 32 + c] + red[(4 * h + 3) * 32 + c]);
+      lfin[col] = l > 0.f ? 1.0f / l : 0.f;
+      const float lse2 = (l > 0.f) ? (m_ref[col] + __log2f(l)) : -CUDART_INF_F;
+      if (col < rr.nvalid && p.lse) p.lse[rr.base + col] = lse2 * 0.69314718055994530942f;
+    }
+    named_bar_sync(kNamedBarSm, kSmThreads);
+    float inv[32];
+#pragma unroll
+    for (int c4 = 0; c4 < 8; ++c4) {
+      const float4 v = reinterpret_cast<const float4*>(lfin)[8 * ch + c4];
+      inv[4 * c4] = v.x;
+      inv[4 * c4 + 1] = v.y;
+      inv[4 * c4 + 2] = v.z;
+      inv[4 * c4 + 3] = v.w;
+    }
+    const int nv = rr.nvalid - 32 * ch;  // my columns c < nv exist
+#pragma unroll 1
+    for (int mb = 0; mb < 4; ++mb) {
+      uint32_t o[32];
+      if (nh > 0) {
+        tmem_ld32(lane_base + kTmemO + 64 * mb + 32 * ch, o);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) o[c] = 0u;
+      }
+      uint16_t* dst = p.out + (rr.base + 32 * ch) * kVdim + 128 * mb + 32 * q + lane;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        if (c < nv) dst[c * kVdim] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(o[c]) * inv[c], 0.f));
+      }
+    }
+    tc_fence_before();
+    if (nh > 0) mbar_arrive(bar(kBarOFree));
+    named_bar_sync(kNamedBarSm, kSmThreads);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t bars = smem_u32(smem) + kOffBars;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+    mbar_init(bar(kBarQFull), kLdThreads);
+    mbar_init(bar(kBarQEmpty), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kBarFull + s), kLdThreads);
+      mbar_init(bar(kBarEmpty + s), 1);
+      mbar_init(bar(kBarSFull + s), 1);
+      mbar_init(bar(kBarPready + s), kSmThreads);
+      mbar_init(bar(kBarPvDone + s), 1);
+    }
+    mbar_init(bar(kBarOFree), kSmThreads);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp >= kLdWarp0) {
+    loader_role(p, smem, bars, abort_flag);
+  } else if (warp == kSIssuerWarp) {
+    if ((threadIdx.x & 31) == 0) s_issuer_role(p, smem, tmem, bars, abort_flag);
+    __syncwarp();
+  } else if (warp == kPvIssuerWarp) {
+    if ((threadIdx.x & 31) == 0) pv_issuer_role(p, smem, tmem, bars, abort_flag);
+    __syncwarp();
+  } else {
+    softmax_role(p, smem, tmem, bars, abort_flag);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const AttnParams& p, cudaStream_t stream) {
+  if (p.num_ctas == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  prefill_kernel<<<p.num_ctas, kThreads, kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace svt
