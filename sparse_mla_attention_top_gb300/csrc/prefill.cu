@@ -20,17 +20,21 @@
 // gone; the M = 64 S^T costs the same cycles per MMA as M = 128, which is the price.
 //
 // Warp roles (512 threads):
-//   warps 0-7   softmax + epilogue: warp w reads TMEM quadrant w % 4 (KV rows 16 (w % 4) +
-//               lane, lanes 0-15) and query columns 32 (w / 4) .. + 31; online softmax in
-//               fp32 with a lazily moved reference maximum; P^T goes into the stage's rope
-//               block; each thread keeps its row's share of the column sums.
+//   warps 0-7   softmax + epilogue: warp w reads the 16 rows of TMEM quadrant w % 4 (KV rows
+//               16 (w % 4) ..) and query columns 32 (w / 4) .. + 31 with the 16-lane load
+//               shape, two threads per row (even / odd columns); online softmax in fp32 with
+//               a lazily moved reference maximum; P^T goes into the stage's rope block; each
+//               thread keeps its share of the column sums.
 //   warp 8      S^T issuer (lane 0), warp 9 PV issuer (lane 0): an MMA issue blocks while the
 //               tensor pipe's queue is full, so one thread issuing both would hold PV behind
 //               the next S^T; each thread commits its own MMAs.
-//   warps 10-15 loaders: resolve the next half-tile's union words and load its 64 rows into
-//               registers (24 x 16 bytes per thread) while both stages are busy; the moment
-//               PV frees a stage, they store it there, so a half-tile's gather latency is
-//               hidden behind the previous stage cycle.
+//   warps 10-15 loaders: resolve the union words of the half-tile after next, and the moment
+//               PV frees a stage, cp.async the next half-tile's 64 rows into it (24 x 16
+//               bytes per thread; Full completes as the copies land). A group's two
+//               row-sets run side by side and neighbouring groups' unions overlap, so most
+//               rows come from L2 and copying them straight into shared memory beats
+//               staging them through registers, which costs the shared SRAM three passes
+//               per byte (L1 fill, read, store) next to the tensor cores' operand reads.
 // Persistent CTAs take whole row-sets round-robin.
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -119,41 +123,31 @@ __device__ __forceinline__ uint32_t live_columns(uint32_t mk, int rpar, int h, i
   return (((mk >> lo) & 1u) ? ~split_hi : 0u) | (((mk >> hi) & 1u) ? split_hi : 0u);
 }
 
-// Transposed reductions over the warp's 32 lanes: lane c ends with column c (v consumed).
-__device__ __forceinline__ float warp_column_max(float (&v)[32], int lane) {
+// Column reduction over the 16 rows a warp holds in the .16x64b layout: v[i] is column
+// 2 i + parity of this thread's row, and the 16 threads of one parity ((lane >> 1) & 1) hold
+// the same columns. Each step pairs threads across one of lane bits 4, 3, 2, 0 and halves
+// the values kept (16 -> 8 -> 4 -> 2 -> 1), so the thread ends with column 2 idx + parity,
+// idx = 8 b4 + 4 b3 + 2 b2 + b0 of its lane bits (v is consumed).
+template <bool kMax>
+__device__ __forceinline__ float rows16_column_reduce(float (&v)[16], int lane, int& idx) {
+  constexpr int kBits[4] = {16, 8, 4, 1};
 #pragma unroll
-  for (int half = 16; half >= 1; half >>= 1) {
-    const bool up = (lane & half) != 0;
-#pragma unroll
-    for (int k = 0; k < half; ++k) {
-      const float send = up ? v[k] : v[k + half];
-      const float keep = up ? v[k + half] : v[k];
-      v[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, half));
-    }
-  }
-  return v[0];
-}
-__device__ __forceinline__ float warp_column_sum(float (&v)[32], int lane) {
-#pragma unroll
-  for (int half = 16; half >= 1; half >>= 1) {
-    const bool up = (lane & half) != 0;
+  for (int st = 0; st < 4; ++st) {
+    const int half = 8 >> st;
+    const bool up = (lane & kBits[st]) != 0;
 #pragma unroll
     for (int k = 0; k < half; ++k) {
       const float send = up ? v[k] : v[k + half];
       const float keep = up ? v[k + half] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+      const float got = __shfl_xor_sync(0xffffffffu, send, kBits[st]);
+      v[k] = kMax ? fmaxf(keep, got) : keep + got;
     }
   }
+  idx = 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + (lane & 1);
   return v[0];
 }
 
 constexpr int kDeadEntry = -2147483647 - 1;
-
-__device__ __forceinline__ uint4 ldg_nc_v4(const void* ptr) {
-  uint4 v;
-  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(ptr));
-  return v;
-}
 
 // ---------------------------------------------------------------------------------- loaders
 // Walks the CTA's half-tiles in order across row-sets (skipping empty row-sets).
@@ -182,11 +176,11 @@ __device__ void loader_role(const AttnParams& p, uint8_t* smem, uint32_t bars, v
   HalfCursor cur{{static_cast<int>(blockIdx.x)}, 0, 0, 0, 0};
   if (!cur.next(p)) return;
 
-  // entry ltid (< 64) of the cursor's half-tile -> slot / mask table k % 4
-  auto resolve = [&](uint32_t k) {
+  // entry ltid (< 64) of half-tile c -> slot / mask table k % 4
+  auto resolve = [&](const HalfCursor& c, uint32_t k) {
     if (ltid < kHalf) {
-      const int e = cur.i * kHalf + ltid;
-      const int raw = e < cur.len ? __ldg(p.enc + static_cast<long long>(cur.r >> 1) * p.list_stride + e) : kDeadEntry;
+      const int e = c.i * kHalf + ltid;
+      const int raw = e < c.len ? __ldg(p.enc + static_cast<long long>(c.r >> 1) * p.list_stride + e) : kDeadEntry;
       int slot = -1;
       uint32_t mask = 0;
       const uint32_t w = static_cast<uint32_t>(raw);
@@ -217,41 +211,34 @@ __device__ void loader_role(const AttnParams& p, uint8_t* smem, uint32_t bars, v
     cp_async_arrive_noinc(bar(kBarQFull));
     ++qk;
   };
-  uint4 v[kChunksPerLoader];
-  auto issue = [&](uint32_t k) {
+  // half-tile k's rows into stage st with cp.async (zero-filled for dead entries); Full(st)
+  // gets this thread's arrival once its copies have landed
+  auto fill = [&](uint32_t k, uint32_t st) {
     const int* slots = slot_tab + (k % kSlotRing) * kHalf;
+    const uint32_t stage = sbase + kOffStage + st * kStageBytes;
 #pragma unroll
     for (int u = 0; u < kChunksPerLoader; ++u) {
       const int idx = ltid + u * kLdThreads;
       const int blk = idx >> 9, row = (idx >> 3) & (kHalf - 1), chunk = idx & 7;
       const int slot = slots[row];
-      v[u] = slot >= 0 ? ldg_nc_v4(p.kv + static_cast<long long>(slot) * p.row_stride + blk * 128 + chunk * 16)
-                       : make_uint4(0, 0, 0, 0);
+      const uint8_t* src = p.kv + (slot >= 0 ? static_cast<long long>(slot) * p.row_stride + blk * 128 + chunk * 16 : 0);
+      cp_async16(stage + blk * kBlk + sw128_offset(row, chunk), src, slot >= 0 ? 16u : 0u);
     }
+    cp_async_arrive_noinc(bar(kBarFull + st));
   };
 
-  resolve(0);
-  issue(0);
+  HalfCursor ahead = cur;
+  resolve(ahead, 0);
+  if (ahead.next(p)) resolve(ahead, 1);
   load_q();
   for (uint32_t g = 0;; ++g) {
     const uint32_t st = g & 1u;
-    // stage st is free once PV of the half-tile two back is done
     mbar_wait(bar(kBarEmpty + st), ((g >> 1) & 1u) ^ 1u, p.status, abort_flag);
-    uint8_t* stage = smem + kOffStage + st * kStageBytes;
-#pragma unroll
-    for (int u = 0; u < kChunksPerLoader; ++u) {
-      const int idx = ltid + u * kLdThreads;
-      const int blk = idx >> 9, row = (idx >> 3) & (kHalf - 1), chunk = idx & 7;
-      *reinterpret_cast<uint4*>(stage + blk * kBlk + sw128_offset(row, chunk)) = v[u];
-    }
-    fence_proxy_async_smem();
-    mbar_arrive(bar(kBarFull + st));
+    fill(g, st);
     if (*abort_flag) break;
-    // the next half-tile: resolve it and put its rows in flight; a new row-set also needs Q^T
     const int prev_r = cur.r;
     if (!cur.next(p)) break;
-    resolve(g + 1);
-    issue(g + 1);
+    if (ahead.next(p)) resolve(ahead, g + 2);
     if (cur.r != prev_r) load_q();
   }
   cp_async_wait_all();
@@ -277,6 +264,7 @@ __device__ void s_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem,
       const uint32_t b = g & 1u;
       if (g >= 2) mbar_wait(bar(kBarPready + b), ((g - 2) >> 1) & 1u, p.status, abort_flag);
       mbar_wait(bar(kBarFull + b), (g >> 1) & 1u, p.status, abort_flag);
+      fence_proxy_async_smem();
       tc_fence_after();
       const uint32_t stage = sbase + kOffStage + b * kStageBytes;
 #pragma unroll 1
@@ -334,8 +322,10 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
                              volatile int* abort_flag) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3, ch = warp >> 2;
-  const int kvrow = 16 * q + lane;  // valid for lane < 16
-  const bool row_lane = lane < 16;
+  // .16x64b layout of the quadrant's 16 rows: this thread's KV row and column parity (its
+  // columns are 32 ch + 2 i + cp, i < 16; lane ^ 2 holds the other parity of the same row)
+  const int kvrow = 16 * q + (lane >> 2) + 8 * (lane & 1);
+  const int cp = (lane >> 1) & 1;
   const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
   const int* slot_tab = reinterpret_cast<const int*>(smem + kOffSlot);
   const uint32_t* mask_tab = reinterpret_cast<const uint32_t*>(smem + kOffMask);
@@ -347,39 +337,36 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
   uint32_t g = 0;
   RowsetWalk walk{static_cast<int>(blockIdx.x)};
   int r, len;
-  float lpart[32];
+  float lpart[16];
   while (walk.advance(p, r, len)) {
     const int nh = halves_of(len);
     const int rpar = r & 1;
     if (threadIdx.x < kRowsetRows) m_ref[threadIdx.x] = -CUDART_INF_F;
 #pragma unroll
-    for (int c = 0; c < 32; ++c) lpart[c] = 0.f;
+    for (int c = 0; c < 16; ++c) lpart[c] = 0.f;
     named_bar_sync(kNamedBarSm, kSmThreads);
     for (int i = 0; i < nh; ++i, ++g) {
       const uint32_t b = g & 1u;
       mbar_wait(bar(kBarSFull + b), (g >> 1) & 1u, p.status, abort_flag);
       tc_fence_after();
-      float x[32];
+      float x[16];
       {
-        uint32_t sv[32];
-        tmem_ld32(lane_base + kTmemS + 64 * b + 32 * ch, sv);
+        uint32_t sv[16];
+        tmem_ld_16x64b_x16(lane_base + kTmemS + 64 * b + 32 * ch, sv);
         tmem_ld_wait();
-        uint32_t live = 0;
-        if (row_lane) {
-          const uint32_t k = (g % kSlotRing) * kHalf + kvrow;
-          if (slot_tab[k] >= 0) live = live_columns(mask_tab[k], rpar, ch, p.H);
-        }
+        const uint32_t k = (g % kSlotRing) * kHalf + kvrow;
+        const uint32_t live = slot_tab[k] >= 0 ? live_columns(mask_tab[k], rpar, ch, p.H) >> cp : 0u;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) x[c] = ((live >> c) & 1u) ? __uint_as_float(sv[c]) * p.scale_log2 : -CUDART_INF_F;
+        for (int c = 0; c < 16; ++c)
+          x[c] = ((live >> (2 * c)) & 1u) ? __uint_as_float(sv[c]) * p.scale_log2 : -CUDART_INF_F;
       }
+      // a float4 of m_ref covers columns 4 c4 .. + 3 of the warp's 32: x[2 c4] and x[2 c4 + 1]
       bool exceed = false;
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
         const float4 m4 = reinterpret_cast<const float4*>(m_ref)[8 * ch + c4];
-        exceed |= x[4 * c4] > m4.x + kTau;
-        exceed |= x[4 * c4 + 1] > m4.y + kTau;
-        exceed |= x[4 * c4 + 2] > m4.z + kTau;
-        exceed |= x[4 * c4 + 3] > m4.w + kTau;
+        exceed |= x[2 * c4] > (cp ? m4.y : m4.x) + kTau;
+        exceed |= x[2 * c4 + 1] > (cp ? m4.w : m4.z) + kTau;
       }
       int any;
       asm volatile(
@@ -393,10 +380,12 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
       if (any) {
         // exact column maxima of this half-tile, then move the reference and rescale
         {
-          float v[32];
+          float v[16];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) v[c] = x[c];
-          red[warp * 32 + lane] = warp_column_max(v, lane);
+          for (int c = 0; c < 16; ++c) v[c] = x[c];
+          int idx;
+          const float m = rows16_column_reduce<true>(v, lane, idx);
+          red[warp * 32 + 2 * idx + cp] = m;
         }
         named_bar_sync(kNamedBarSm, kSmThreads);
         if (threadIdx.x < kRowsetRows) {
@@ -410,7 +399,7 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
         }
         named_bar_sync(kNamedBarSm, kSmThreads);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) lpart[c] *= alpha_s[32 * ch + c];
+        for (int c = 0; c < 16; ++c) lpart[c] *= alpha_s[32 * ch + 2 * c + cp];
         if (i > 0) {
           // O^T holds every PV so far once the previous half-tile's PV is done
           const uint32_t gp = g - 1;
@@ -430,29 +419,34 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
           tmem_st_wait();
         }
       }
-      // P^T row (this KV row, my 32 query columns) into the stage's rope block
-      uint32_t pk[16];
+      // P^T row (this KV row, 16 query columns) into the stage's rope block. The two threads of
+      // a row swap halves so that each holds 16 consecutive columns: cp = 0 writes columns
+      // 32 ch + 0..15, cp = 1 columns 32 ch + 16..31 (two 16-byte chunks each).
+      float pq[16];
 #pragma unroll
       for (int c4 = 0; c4 < 8; ++c4) {
         const float4 m4 = reinterpret_cast<const float4*>(m_ref)[8 * ch + c4];
-        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-        float pq[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int c = 4 * c4 + j;
-          pq[j] = (x[c] > -CUDART_INF_F) ? ex2_approx(x[c] - mm[j]) : 0.f;
-          lpart[c] += pq[j];
-        }
-        pk[2 * c4] = pack_bf16x2(pq[0], pq[1]);
-        pk[2 * c4 + 1] = pack_bf16x2(pq[2], pq[3]);
+        const float m0 = cp ? m4.y : m4.x, m1 = cp ? m4.w : m4.z;
+        pq[2 * c4] = (x[2 * c4] > -CUDART_INF_F) ? ex2_approx(x[2 * c4] - m0) : 0.f;
+        pq[2 * c4 + 1] = (x[2 * c4 + 1] > -CUDART_INF_F) ? ex2_approx(x[2 * c4 + 1] - m1) : 0.f;
+        lpart[2 * c4] += pq[2 * c4];
+        lpart[2 * c4 + 1] += pq[2 * c4 + 1];
       }
-      if (row_lane) {
-        uint8_t* prow = smem + kOffStage + b * kStageBytes + 8 * kBlk;
+      uint32_t w[8];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          *reinterpret_cast<uint4*>(prow + sw128_offset(kvrow, 4 * ch + k)) =
-              make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
-        }
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = pack_bf16x2(pq[2 * j], pq[2 * j + 1]);      // columns 4 j + cp, 4 j + 2 + cp
+        const uint32_t hi = pack_bf16x2(pq[8 + 2 * j], pq[9 + 2 * j]);  // 16 more
+        const uint32_t own = cp ? hi : lo;
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, cp ? lo : hi, 2);
+        const uint32_t ev = cp ? recv : own, od = cp ? own : recv;  // even / odd columns
+        w[2 * j] = __byte_perm(ev, od, 0x5410);
+        w[2 * j + 1] = __byte_perm(ev, od, 0x7632);
+      }
+      {
+        uint8_t* prow = smem + kOffStage + b * kStageBytes + 8 * kBlk;
+        *reinterpret_cast<uint4*>(prow + sw128_offset(kvrow, 4 * ch + 2 * cp)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(prow + sw128_offset(kvrow, 4 * ch + 2 * cp + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -466,7 +460,11 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
       tc_fence_after();
     }
     const RowsetRows rr = rowset_rows(p, r);
-    red[warp * 32 + lane] = warp_column_sum(lpart, lane);  // this warp's 16 rows, column 32 ch + lane
+    {
+      int idx;
+      const float l = rows16_column_reduce<false>(lpart, lane, idx);  // this warp's 16 rows
+      red[warp * 32 + 2 * idx + cp] = l;
+    }
     named_bar_sync(kNamedBarSm, kSmThreads);
     if (threadIdx.x < kRowsetRows) {
       const int col = threadIdx.x, h = col >> 5, c = col & 31;
