@@ -37,12 +37,13 @@ UNIT = "queries/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the decode attention kernel,
-# keyed by the sha256 of the attention source it was measured on (stale -> null).
+# dram__bytes_read.sum + dram__bytes_write.sum of one decode call (attention_kernel and
+# streamk_merge_kernel), keyed by the hash of their sources it was measured on (stale -> null).
 TRAFFIC_BY_SOURCE = {
-    # 16-query decode capture (profiles/decode_bf16_attention_ncu.md): 39.22 MB read + 0.56 MB
-    # written, scaled by 64/16 queries to the benchmark's launch
-    "22b323542208fcb1": 4 * (39.224064e6 + 0.557824e6),
+    # full-size capture (profiles/decode_bf16_attention_ncu.md, ncu --cache-control none after
+    # bench.py's own L2 flush): attention 158.43 MB read + 62.22 MB written, merge 0.85 MB read
+    # + 0.51 MB written
+    "3981f9e5af6ede67": (158.43 + 62.22 + 0.85 + 0.51) * 1e6,
 }
 
 
@@ -240,9 +241,11 @@ def replica_throughput(units_per_rank: int, ms_max: float, world: int) -> float:
 
 
 def source_hash() -> str:
+    """Hash of the sources of the two decode kernels the roofline line times together."""
     h = hashlib.sha256()
-    with open(os.path.join(ROOT, "sparse_mla_attention_top_gb300", "csrc", "attention.cu"), "rb") as f:
-        h.update(f.read())
+    for name in ("attention.cu", "merge.cu"):
+        with open(os.path.join(ROOT, "sparse_mla_attention_top_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 

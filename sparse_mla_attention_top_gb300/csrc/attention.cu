@@ -37,10 +37,10 @@
 //               Group 0 also resolves list entries to slots two tiles ahead: one thread walks
 //               the CTA's schedule and posts each tile's descriptor in a ring of four.
 // Persistent CTAs walk a static schedule: stream-K over (row-set, tile) for decode, whole
-// row-sets round-robin for grouped prefill. A row-set split between CTAs is merged inside
-// the kernel by the last CTA to finish its part (an atomic count per split row-set, kept
-// in the workspace at the index of the row-set's first CTA, which no other split row-set
-// shares).
+// row-sets round-robin for grouped prefill. Each part of a row-set split between CTAs is
+// written as fp32 partial rows and a partial LSE (slot 2c or 2c + 1 of CTA c); the merge
+// kernel, launched behind this one with programmatic dependent launch, combines them
+// (merge.cu). A row-set no CTA boundary cuts is finished here.
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
