@@ -60,7 +60,8 @@ svt_status check_ws(void* ws, size_t ws_bytes, size_t need) {
   return SVT_OK;
 }
 
-// Decode launch shape: (number of CTAs, partial slots needed).
+// Decode launch shape: (number of CTAs, partial slots needed). The work unit is unit_rows
+// list entries: 64 (a half-tile) for the bf16 kernel, 128 (a tile) for the e4m3 kernel.
 struct DecodePlan {
   int rowsets, hchunks, tiles_per_rowset;
   long long total_tiles;
@@ -68,11 +69,11 @@ struct DecodePlan {
   bool partials;
 };
 
-DecodePlan plan_decode(int T, int H, int K, int num_splits) {
+DecodePlan plan_decode(int T, int H, int K, int num_splits, int unit_rows) {
   DecodePlan d{};
   d.hchunks = (H + svt::kRowsetRows - 1) / svt::kRowsetRows;
   d.rowsets = T * d.hchunks;
-  d.tiles_per_rowset = (K + svt::kTileRows - 1) / svt::kTileRows;
+  d.tiles_per_rowset = (K + unit_rows - 1) / unit_rows;
   d.total_tiles = static_cast<long long>(d.rowsets) * d.tiles_per_rowset;
   if (d.total_tiles == 0) {
     d.num_ctas = 0;
@@ -105,6 +106,8 @@ size_t decode_ws_bytes(const DecodePlan& d) {
   if (d.partials) b += decode_part_o_bytes(d) + decode_part_lse_bytes(d);
   return b;
 }
+
+int decode_unit_rows(svt_kv_dtype dtype) { return dtype == SVT_KV_BF16 ? svt::kTileRows / 2 : svt::kTileRows; }
 
 }  // namespace
 
@@ -165,7 +168,10 @@ svt_status svt_resolve_topk_slots(const int32_t* topk_pos, int32_t T, int32_t K,
 
 size_t svt_sparse_mla_decode_workspace_size(int32_t T, int32_t H, int32_t K, int32_t num_splits) {
   if (T < 0 || H <= 0 || K < 0 || num_splits < 0) return svt::kStatusBytes;
-  return decode_ws_bytes(plan_decode(T, H, K, num_splits));
+  // the cache dtype is not an argument: enough for either kernel's plan
+  const size_t a = decode_ws_bytes(plan_decode(T, H, K, num_splits, decode_unit_rows(SVT_KV_BF16)));
+  const size_t b = decode_ws_bytes(plan_decode(T, H, K, num_splits, decode_unit_rows(SVT_KV_FP8_E4M3)));
+  return a > b ? a : b;
 }
 
 svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const svt_kv_cache* kv,
@@ -183,7 +189,7 @@ svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const
   if (st != SVT_OK) return st;
   if (block_table != nullptr && (num_reqs <= 0 || max_blocks <= 0))
     return fail(SVT_ERR_INVALID_ARG, "num_reqs and max_blocks must be > 0 with a block table");
-  const DecodePlan d = plan_decode(T, H, K, num_splits);
+  const DecodePlan d = plan_decode(T, H, K, num_splits, decode_unit_rows(kv->dtype));
   st = check_ws(ws, ws_bytes, decode_ws_bytes(d));
   if (st != SVT_OK) return st;
   if (T == 0) return SVT_OK;
@@ -232,7 +238,7 @@ svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const
     p.total_tiles = d.rowsets;
     p.num_ctas = d.rowsets;
   }
-  cudaError_t e = svt::launch_attention(p, s);
+  cudaError_t e = kv->dtype == SVT_KV_BF16 ? svt::launch_attention_bf16(p, s) : svt::launch_attention(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
   if (d.partials) {
     e = svt::launch_streamk_merge(p, s);
@@ -308,7 +314,7 @@ svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T, int32_t
   if (sms <= 0) sms = 1;
   p.num_ctas = p.num_rowsets < sms ? p.num_rowsets : sms;
   p.status = static_cast<int*>(ws);
-  cudaError_t e = kv->dtype == SVT_KV_BF16 ? svt::launch_prefill(p, reinterpret_cast<cudaStream_t>(stream))
+  cudaError_t e = kv->dtype == SVT_KV_BF16 ? svt::launch_attention_bf16(p, reinterpret_cast<cudaStream_t>(stream))
                                            : svt::launch_attention(p, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
   return SVT_OK;

@@ -1,0 +1,733 @@
+// Sparse MLA attention over a bf16 cache on tcgen05 tensor cores, decode and grouped
+// prefill, with two shared-memory stages of 64-row half-tiles so that gathering, the two
+// contractions and the softmax overlap.
+//
+// What it computes, per query row of a row-set and the row-set's KV list:
+//   s_j = scale * q . k_j,  out = softmax(s) . V,  lse = ln sum_j exp(s_j)
+// over the live entries of the list, with k_j the whole 576-wide cache row and V its first
+// 512 columns (vLLM PR #63104, bench script: 512 latent + 64 rope). Decode: a row-set is one
+// query's heads (up to 64) and the list its top-k positions, resolved to cache slots through
+// the block table ("The Virtual Block Table: Reusing Triton MLA for Sparse Attention on
+// Blackwell GPUs", The Investigation: slot = table[req, pos / P] * P + pos % P; The
+// Breakthrough: with no table the list already holds slots). Grouped prefill: a row-set is
+// half of a group's 128 packed rows and the list the group's union, each row seeing only the
+// entries whose membership bit is its query's (vLLM PR #63104, Overview).
+//
+// GB300 design. A half-tile is 64 list entries; per half-tile
+//   S^T[64 x 64]   = K_half[64 x 576] . Q^T     (M = 64: 36 MMAs of K = 16)
+//   O^T[512 x 64] += V_half^T[512 x 64] . P^T   (4 M-blocks of 128 channels x 4 MMAs)
+// S^T is double-buffered in TMEM (M = 64 layout: rows in lanes 0-15 of each 32-lane
+// quadrant), O^T takes 4 x 64 columns. While the softmax works on half-tile g, the tensor
+// cores run PV(g-1) and S(g+1) and the rows of half-tile g+2 land by cp.async in the stage
+// PV(g) frees, so the serial chain S -> softmax -> PV of a single stage is broken; the M = 64
+// S^T costs the same cycles per MMA as M = 128, which is the price.
+//
+// Work: persistent CTAs walk segments (a row-set and a range of its half-tiles). Decode uses
+// stream-K over (row-set, half-tile) so every SM gets the same number of half-tiles; a
+// row-set cut by a CTA boundary leaves fp32 partial rows and a partial LSE per part, which
+// the merge kernel (merge.cu) combines. Grouped prefill takes whole row-sets round-robin.
+//
+// Warp roles (512 threads):
+//   warps 0-7   softmax + epilogue: warp w reads the 16 rows of TMEM quadrant w % 4 (KV rows
+//               16 (w % 4) ..) and query columns 32 (w / 4) .. + 31 with the 16-lane load
+//               shape, two threads per row (even / odd columns); online softmax in fp32 with
+//               a lazily moved reference maximum; P^T goes into the stage's rope block; each
+//               thread keeps its share of the column sums.
+//   warp 8      S^T issuer (lane 0), warp 9 PV issuer (lane 0): an MMA issue blocks while the
+//               tensor pipe's queue is full, so one thread issuing both would hold PV behind
+//               the next S^T; each thread commits its own MMAs.
+//   warps 10-11 resolvers: one list entry per thread, up to four half-tiles ahead, into a
+//               ring of slot / mask tables. A decode entry takes two dependent reads (the
+//               entry, then its page-table word); the entry read of the next half-tile is
+//               issued with the page read of the current one.
+//   warps 12-15 fillers: the moment PV frees a stage, cp.async the next half-tile's 64 rows
+//               into it (36 x 16 bytes per thread, dead rows zero-filled; Full completes as
+//               the copies land), and Q^T at each segment start. Copying straight into shared
+//               memory keeps the shared SRAM to one pass per byte; staging through registers
+//               costs three (L1 fill, read, store) next to the tensor cores' operand reads.
+// Every wait is bounded (mbar_wait); the status word records range errors and timeouts.
+#include <climits>
+
+#include <cuda_fp16.h>
+#include <math_constants.h>
+
+#include "device.cuh"
+#include "internal.h"
+#include "resolve_entry.cuh"
+
+namespace svt {
+
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kSmThreads = 256;   // warps 0-7
+constexpr int kSIssuerWarp = 8;   // issues S^T
+constexpr int kPvIssuerWarp = 9;  // issues PV
+constexpr int kResWarp0 = 10;
+constexpr int kResThreads = 64;   // warps 10-11: one list entry each
+constexpr int kFillWarp0 = 12;
+constexpr int kFillThreads = 128;  // warps 12-15
+constexpr int kFillWarps = kFillThreads / 32;
+constexpr int kHalf = 64;          // KV rows per half-tile
+constexpr int kBlocks = 9;
+constexpr int kBlk = kHalf * 128;  // 8 KB: 64 rows x 64 bf16
+constexpr int kStageBytes = kBlocks * kBlk;
+constexpr int kQBlk = kRowsetRows * 128;  // 8 KB
+constexpr float kTau = 8.0f;
+constexpr int kHalfChunks = kHalf * kBlocks * 8;            // 16-byte chunks of a half-tile: 4608
+constexpr int kChunksPerFiller = kHalfChunks / kFillThreads;  // 36
+static_assert(kHalfChunks % kFillThreads == 0, "");
+static_assert(kFillThreads == 128 && kChunksPerFiller == 4 * kBlocks, "the fill loop's row / block mapping");
+static_assert(kResThreads == kHalf, "one resolver thread per entry");
+
+// shared memory map (offsets from a 1024-aligned base)
+constexpr int kOffQ = 0;
+constexpr int kOffStage = kOffQ + kBlocks * kQBlk;      // 73728: stage s at + s * kStageBytes
+constexpr int kSlotRing = 4;                           // resolved half-tiles in flight
+constexpr int kOffSlot = kOffStage + 2 * kStageBytes;  // 221184: int[4][64]
+constexpr int kOffMask = kOffSlot + kSlotRing * kHalf * 4;  // uint[4][64]
+constexpr int kOffMref = kOffMask + kSlotRing * kHalf * 4;  // float[64]
+constexpr int kOffAlpha = kOffMref + kRowsetRows * 4;  // float[64]
+constexpr int kOffRed = kOffAlpha + kRowsetRows * 4;   // float[8][32]
+constexpr int kOffLfin = kOffRed + 8 * 32 * 4;         // float[64]
+constexpr int kOffBars = kOffLfin + kRowsetRows * 4;   // uint64[kNumBars]
+constexpr int kOffMisc = kOffBars + 24 * 8;            // tmem base, abort flag
+constexpr int kSmemUsed = kOffMisc + 16;
+constexpr int kSmemBytes = kSmemUsed + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory map exceeds 227 KB");
+
+// barriers (stage / buffer pairs at +0, +1; slot ring entries at +0 .. +3)
+constexpr int kBarQFull = 0;        // the fillers' Q^T copies landed (cp.async arrivals)
+constexpr int kBarQEmpty = 1;       // last S^T of the segment issued and done
+constexpr int kBarFull = 2;         // 2: a half-tile's rows landed in stage s
+constexpr int kBarEmpty = 4;        // 2: PV done with stage s
+constexpr int kBarSFull = 6;        // 2: S^T buffer b ready
+constexpr int kBarPready = 8;       // 2: P^T of the half-tile in stage s written
+constexpr int kBarPvDone = 10;      // 2: PV of the half-tile in stage s done
+constexpr int kBarOFree = 12;       // the segment's epilogue has read O^T
+constexpr int kBarSlotsReady = 13;  // 4: ring entry k % 4 holds half-tile k's slots
+constexpr int kBarSlotFree = 17;    // 4: softmax and fillers are done with ring entry k % 4
+constexpr int kNumBars = 21;
+static_assert(kNumBars * 8 <= kOffMisc - kOffBars, "barrier block");
+constexpr int kSlotFreeArrivals = kSmThreads / 32 + kFillWarps;  // one per softmax / filler warp
+
+constexpr int kTmemCols = 512;
+constexpr int kTmemS = 0;    // S^T buffer b: columns 64 b .. + 63 (lanes 0-15 of each quadrant)
+constexpr int kTmemO = 128;  // O^T M-block mb: columns 128 + 64 mb .. + 63
+
+constexpr int kNamedBarSm = 1;
+
+constexpr uint32_t kIdescS = idesc_f32acc(64, 64, 0, 0, kFmtBf16);
+constexpr uint32_t kIdescPV = idesc_f32acc(128, 64, 1, 1, kFmtBf16);
+
+constexpr int kDeadEntry = -2147483647 - 1;  // an entry past the list's live count
+
+__device__ __forceinline__ int halves_of(int len) { return (len + kHalf - 1) / kHalf; }
+
+// One stretch of a CTA's work: half-tiles i0 .. i0 + n - 1 of row-set r (only those with
+// live entries; a segment may have none and then only writes its epilogue).
+struct Seg {
+  int r;
+  int i0;
+  int n;
+  int len;   // live entries of the row-set's list
+  int full;  // the segment covers the whole row-set: final output, else a partial
+  int slot;  // the partial slot (stream-K)
+};
+
+// The CTA's segments in order; every role walks its own copy.
+struct SegWalk {
+  long long pos, lo, hi;  // stream-K range in half-tiles
+  int next_rowset, idx;
+
+  __device__ void init(const AttnParams& p) {
+    idx = 0;
+    if (p.sched == kSchedStreamK) {
+      lo = streamk_lo(blockIdx.x, p.total_tiles, p.num_ctas);
+      hi = streamk_lo(blockIdx.x + 1ll, p.total_tiles, p.num_ctas);
+      pos = lo;
+    } else {
+      next_rowset = blockIdx.x;
+    }
+  }
+
+  __device__ static int list_len(const AttnParams& p, int r) {
+    if (p.mode == kModeDecode) {
+      const int t = r / p.hchunks;
+      const int len = p.topk_len ? p.topk_len[t] : p.K;
+      return len < 0 ? 0 : (len > p.K ? p.K : len);
+    }
+    const int len = p.lens[r >> 1];
+    return len < 0 ? 0 : (len > p.list_stride ? p.list_stride : len);
+  }
+
+  __device__ bool next(const AttnParams& p, Seg& s) {
+    if (p.sched == kSchedStreamK) {
+      if (pos >= hi) return false;
+      const long long nt = p.tiles_per_rowset;
+      const long long r = pos / nt;
+      const long long i0 = pos - r * nt;
+      long long te = hi - r * nt;
+      if (te > nt) te = nt;
+      pos = r * nt + te;
+      s.r = static_cast<int>(r);
+      s.i0 = static_cast<int>(i0);
+      s.full = (i0 == 0 && te == nt);
+      const bool multi = (lo / nt) != ((hi - 1) / nt);
+      s.slot = static_cast<int>(2ll * blockIdx.x + ((multi && idx > 0) ? 1 : 0));
+      ++idx;
+      s.len = list_len(p, s.r);
+      const long long live = halves_of(s.len);
+      const long long end = te < live ? te : live;
+      s.n = end > i0 ? static_cast<int>(end - i0) : 0;
+      return true;
+    }
+    if (next_rowset >= p.num_rowsets) return false;
+    s.r = next_rowset;
+    next_rowset += p.num_ctas;
+    s.i0 = 0;
+    s.full = 1;
+    s.slot = 0;
+    s.len = list_len(p, s.r);
+    s.n = halves_of(s.len);
+    return true;
+  }
+};
+
+// Prefill: which query columns of 32-column half h of row-set half `rpar` a KV row is live
+// for, given its membership bits mk. Column c is packed row 64 rpar + 32 h + c, member
+// (64 rpar + 32 h + c) / H (H >= 16, so a half spans at most two members).
+__device__ __forceinline__ uint32_t live_columns(uint32_t mk, int rpar, int h, int H) {
+  const int packed0 = rpar * kRowsetRows + 32 * h;
+  const int lo = packed0 / H, hi = (packed0 + 31) / H;
+  const uint32_t split_hi = (hi != lo) ? (0xFFFFFFFFu << (H - (packed0 - lo * H))) : 0u;
+  return (((mk >> lo) & 1u) ? ~split_hi : 0u) | (((mk >> hi) & 1u) ? split_hi : 0u);
+}
+
+// Column reduction over the 16 rows a warp holds in the .16x64b layout: v[i] is column
+// 2 i + parity of this thread's row, and the 16 threads of one parity ((lane >> 1) & 1) hold
+// the same columns. Each step pairs threads across one of lane bits 4, 3, 2, 0 and halves
+// the values kept (16 -> 8 -> 4 -> 2 -> 1), so the thread ends with column 2 idx + parity,
+// idx = 8 b4 + 4 b3 + 2 b2 + b0 of its lane bits (v is consumed).
+template <bool kMax>
+__device__ __forceinline__ float rows16_column_reduce(float (&v)[16], int lane, int& idx) {
+  constexpr int kBits[4] = {16, 8, 4, 1};
+#pragma unroll
+  for (int st = 0; st < 4; ++st) {
+    const int half = 8 >> st;
+    const bool up = (lane & kBits[st]) != 0;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float send = up ? v[k] : v[k + half];
+      const float keep = up ? v[k + half] : v[k];
+      const float got = __shfl_xor_sync(0xffffffffu, send, kBits[st]);
+      v[k] = kMax ? fmaxf(keep, got) : keep + got;
+    }
+  }
+  idx = 8 * ((lane >> 4) & 1) + 4 * ((lane >> 3) & 1) + 2 * ((lane >> 2) & 1) + (lane & 1);
+  return v[0];
+}
+
+// ---------------------------------------------------------------------------------- resolvers
+// Half-tile k's 64 entries -> slot / mask ring entry k % 4 (waiting until the softmax and
+// the fillers are done with half-tile k - 4), then SlotsReady(k % 4).
+__device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars, volatile int* abort_flag) {
+  const int ltid = static_cast<int>(threadIdx.x) - kResWarp0 * 32;
+  int* slot_tab = reinterpret_cast<int*>(smem + kOffSlot);
+  uint32_t* mask_tab = reinterpret_cast<uint32_t*>(smem + kOffMask);
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+  const bool decode = p.mode == kModeDecode;
+  const bool has_table = p.block_table != nullptr;
+  int err = 0;
+  uint32_t k = 0;
+  SegWalk walk;
+  walk.init(p);
+  Seg s;
+  bool live = true;
+  while (live && walk.next(p, s)) {
+    if (s.n == 0) continue;
+    // the segment's list and, for decode, its request's block-table row and length
+    const int32_t* list;
+    ReqContext rc{nullptr, INT_MAX, true};
+    if (decode) {
+      const int t = s.r / p.hchunks;
+      list = p.topk + static_cast<long long>(t) * p.K;
+      if (has_table) {
+        const int req = p.req_of_token ? __ldg(p.req_of_token + t) : t;
+        rc.ok = req >= 0 && req < p.num_reqs;
+        if (rc.ok) {
+          rc.bt_row = p.block_table + static_cast<long long>(req) * p.max_blocks;
+          if (p.seq_lens != nullptr) rc.seq_len = __ldg(p.seq_lens + req);
+        }
+      }
+    } else {
+      list = p.enc + static_cast<long long>(s.r >> 1) * p.list_stride;
+    }
+    auto entry = [&](int i) -> int {
+      const int e = (s.i0 + i) * kHalf + ltid;
+      return e < s.len ? __ldg(list + e) : kDeadEntry;
+    };
+    int raw = entry(0);
+    for (int i = 0; i < s.n; ++i, ++k) {
+      // the next half-tile's entry read goes out together with this one's page read
+      const int raw_next = i + 1 < s.n ? entry(i + 1) : kDeadEntry;
+      int slot = -1;
+      uint32_t mask = 0xFFFFFFFFu;
+      if (decode) {
+        if (raw != kDeadEntry) {
+          const int phys = page_of(raw, rc, p.max_blocks, p.page_size);
+          slot = slot_of(raw, phys, rc, has_table, p.max_blocks, p.page_size, p.num_pages, &err);
+        }
+      } else {
+        mask = 0;
+        const uint32_t w = static_cast<uint32_t>(raw);
+        if (raw != kDeadEntry && w != 0xFFFFFFFFu) {
+          const int sl = static_cast<int>(w & 0xFFFFFFu);
+          if (static_cast<long long>(sl) < p.num_slots) {
+            slot = sl;
+            mask = w >> 24;
+          } else {
+            err = 1;
+          }
+        }
+      }
+      const uint32_t e = k % kSlotRing;
+      if (k >= kSlotRing && !mbar_wait(bar(kBarSlotFree + e), ((k / kSlotRing) - 1) & 1u, p.status, abort_flag)) {
+        live = false;
+        break;
+      }
+      slot_tab[e * kHalf + ltid] = slot;
+      mask_tab[e * kHalf + ltid] = mask;
+      mbar_arrive(bar(kBarSlotsReady + e));
+      raw = raw_next;
+    }
+  }
+  if (__any_sync(0xffffffffu, err) && (threadIdx.x & 31) == 0) atomicOr(p.status, SVT_DEV_ERR_INDEX_RANGE);
+}
+
+// ---------------------------------------------------------------------------------- fillers
+__device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, volatile int* abort_flag) {
+  const int ftid = static_cast<int>(threadIdx.x) - kFillWarp0 * 32;
+  const int lane = threadIdx.x & 31;
+  const uint32_t sbase = smem_u32(smem);
+  const int* slot_tab = reinterpret_cast<const int*>(smem + kOffSlot);
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+  const uint8_t* qb = reinterpret_cast<const uint8_t*>(p.q);
+  uint32_t g = 0, qk = 0;
+  SegWalk walk;
+  walk.init(p);
+  Seg s;
+  bool live = true;
+  while (live && walk.next(p, s)) {
+    if (s.n == 0) continue;
+    for (int i = 0; i < s.n; ++i, ++g) {
+      const uint32_t st = g & 1u, e = g % kSlotRing;
+      // half-tile g's slots, and its stage free (PV of half-tile g - 2 done)
+      if (!mbar_wait(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, p.status, abort_flag) ||
+          !mbar_wait(bar(kBarEmpty + st), ((g >> 1) & 1u) ^ 1u, p.status, abort_flag)) {
+        live = false;
+        break;
+      }
+      // chunk ftid + 128 u is block u / 4, row ftid / 8 + 16 (u % 4), 16-byte column ftid % 8:
+      // a thread touches four rows, so their slots are read once and the 36 copies go out
+      // back to back
+      const int* slots = slot_tab + e * kHalf;
+      const uint32_t stage = sbase + kOffStage + st * kStageBytes;
+      const int chunk = ftid & 7;
+      const uint8_t* src[4];
+      uint32_t dst[4], nbytes[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int row = (ftid >> 3) + 16 * j;
+        const int slot = slots[row];
+        src[j] = p.kv + (slot >= 0 ? static_cast<long long>(slot) * p.row_stride + chunk * 16 : 0);
+        nbytes[j] = slot >= 0 ? 16u : 0u;
+        dst[j] = stage + sw128_offset(row, chunk);
+      }
+#pragma unroll
+      for (int blk = 0; blk < kBlocks; ++blk) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) cp_async16(dst[j] + blk * kBlk, src[j] + (nbytes[j] ? blk * 128 : 0), nbytes[j]);
+      }
+      cp_async_arrive_noinc(bar(kBarFull + st));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarSlotFree + e));
+      if (i == 0) {
+        // Q^T of the segment's row-set, once the previous segment's last S^T is done with it
+        if (!mbar_wait(bar(kBarQEmpty), (qk & 1u) ^ 1u, p.status, abort_flag)) {
+          live = false;
+          break;
+        }
+        const RowsetRows rr = rowset_rows(p, s.r);
+        for (int idx = ftid; idx < kRowsetRows * 72; idx += kFillThreads) {
+          const int row = idx / 72, c = idx - row * 72;
+          const bool valid = row < rr.nvalid;
+          const uint8_t* src = qb + (valid ? (rr.base + row) * (kRow * 2) + c * 16 : 0);
+          cp_async16(sbase + kOffQ + (c >> 3) * kQBlk + sw128_offset(row, c & 7), src, valid ? 16u : 0u);
+        }
+        cp_async_arrive_noinc(bar(kBarQFull));
+        ++qk;
+      }
+    }
+  }
+  cp_async_wait_all();
+}
+
+// ---------------------------------------------------------------------------------- issuers
+// S^T(g) into TMEM buffer g % 2 from stage g % 2, once the stage holds half-tile g and the
+// softmax is done with the buffer's previous contents (half-tile g - 2).
+__device__ void s_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars,
+                              volatile int* abort_flag) {
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+  uint32_t g = 0, qk = 0;
+  SegWalk walk;
+  walk.init(p);
+  Seg s;
+  while (walk.next(p, s)) {
+    if (s.n == 0) continue;
+    if (!mbar_wait(bar(kBarQFull), qk & 1u, p.status, abort_flag)) return;
+    ++qk;
+    for (int i = 0; i < s.n; ++i, ++g) {
+      const uint32_t b = g & 1u;
+      if (g >= 2 && !mbar_wait(bar(kBarPready + b), ((g - 2) >> 1) & 1u, p.status, abort_flag)) return;
+      if (!mbar_wait(bar(kBarFull + b), (g >> 1) & 1u, p.status, abort_flag)) return;
+      fence_proxy_async_smem();  // cp.async data (generic proxy) -> MMA operand reads
+      tc_fence_after();
+      const uint32_t stage = sbase + kOffStage + b * kStageBytes;
+#pragma unroll 1
+      for (int kb = 0; kb < kBlocks; ++kb) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t a = smem_desc_sw128(stage + kb * kBlk + ks * 32, 16, 1024);
+          const uint64_t bq = smem_desc_sw128(sbase + kOffQ + kb * kQBlk + ks * 32, 16, 1024);
+          umma_f16(tmem + kTmemS + 64 * b, a, bq, kIdescS, (kb | ks) != 0);
+        }
+      }
+      umma_commit(bar(kBarSFull + b));
+      if (i == s.n - 1) umma_commit(bar(kBarQEmpty));
+    }
+  }
+}
+
+// PV(g) from stage g % 2 and P^T, once the softmax has written P^T(g) (and, for a segment's
+// first half-tile, once the previous segment's epilogue has read O^T).
+__device__ void pv_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars,
+                               volatile int* abort_flag) {
+  const uint32_t sbase = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+  uint32_t g = 0, qk = 0;
+  SegWalk walk;
+  walk.init(p);
+  Seg s;
+  while (walk.next(p, s)) {
+    if (s.n == 0) continue;
+    if (qk > 0 && !mbar_wait(bar(kBarOFree), (qk - 1) & 1u, p.status, abort_flag)) return;
+    ++qk;
+    for (int i = 0; i < s.n; ++i, ++g) {
+      const uint32_t b = g & 1u;
+      if (!mbar_wait(bar(kBarPready + b), (g >> 1) & 1u, p.status, abort_flag)) return;
+      tc_fence_after();
+      const uint32_t stage = sbase + kOffStage + b * kStageBytes;
+      const uint32_t pt = stage + 8 * kBlk;
+#pragma unroll
+      for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t a = smem_desc_sw128(stage + (2 * mb) * kBlk + ks * 2048, kBlk, 1024);
+          const uint64_t bp = smem_desc_sw128(pt + ks * 2048, kQBlk, 1024);
+          umma_f16(tmem + kTmemO + 64 * mb, a, bp, kIdescPV, (i > 0 || ks > 0) ? 1u : 0u);
+        }
+      }
+      umma_commit(bar(kBarEmpty + b));
+      umma_commit(bar(kBarPvDone + b));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------- softmax
+__device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars,
+                             volatile int* abort_flag) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q = warp & 3, ch = warp >> 2;
+  // .16x64b layout of the quadrant's 16 rows: this thread's KV row and column parity (its
+  // columns are 32 ch + 2 i + cp, i < 16; lane ^ 2 holds the other parity of the same row)
+  const int kvrow = 16 * q + (lane >> 2) + 8 * (lane & 1);
+  const int cp = (lane >> 1) & 1;
+  const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q) << 16);
+  const int* slot_tab = reinterpret_cast<const int*>(smem + kOffSlot);
+  const uint32_t* mask_tab = reinterpret_cast<const uint32_t*>(smem + kOffMask);
+  float* m_ref = reinterpret_cast<float*>(smem + kOffMref);
+  float* alpha_s = reinterpret_cast<float*>(smem + kOffAlpha);
+  float* red = reinterpret_cast<float*>(smem + kOffRed);
+  float* lfin = reinterpret_cast<float*>(smem + kOffLfin);
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+  const bool decode = p.mode == kModeDecode;
+  uint32_t g = 0;
+  SegWalk walk;
+  walk.init(p);
+  Seg s;
+  float lpart[16];
+  while (walk.next(p, s)) {
+    const int nh = s.n;
+    const int rpar = s.r & 1;
+    if (threadIdx.x < kRowsetRows) m_ref[threadIdx.x] = -CUDART_INF_F;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) lpart[c] = 0.f;
+    named_bar_sync(kNamedBarSm, kSmThreads);
+    for (int i = 0; i < nh; ++i, ++g) {
+      const uint32_t b = g & 1u;
+      const uint32_t e = g % kSlotRing;
+      mbar_wait(bar(kBarSFull + b), (g >> 1) & 1u, p.status, abort_flag);
+      mbar_wait(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, p.status, abort_flag);
+      tc_fence_after();
+      float x[16];
+      {
+        uint32_t sv[16];
+        tmem_ld_16x64b_x16(lane_base + kTmemS + 64 * b + 32 * ch, sv);
+        const uint32_t k = e * kHalf + kvrow;
+        const int slot = slot_tab[k];
+        const uint32_t mk = mask_tab[k];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBarSlotFree + e));  // the ring entry is read
+        const uint32_t live = slot < 0 ? 0u : (decode ? 0xFFFFFFFFu : live_columns(mk, rpar, ch, p.H) >> cp);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          x[c] = ((live >> (2 * c)) & 1u) ? __uint_as_float(sv[c]) * p.scale_log2 : -CUDART_INF_F;
+      }
+      // a float4 of m_ref covers columns 4 c4 .. + 3 of the warp's 32: x[2 c4] and x[2 c4 + 1]
+      bool exceed = false;
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 m4 = reinterpret_cast<const float4*>(m_ref)[8 * ch + c4];
+        exceed |= x[2 * c4] > (cp ? m4.y : m4.x) + kTau;
+        exceed |= x[2 * c4 + 1] > (cp ? m4.w : m4.z) + kTau;
+      }
+      int any;
+      asm volatile(
+          "{\n\t.reg .pred pi, po;\n\t"
+          "setp.ne.u32 pi, %1, 0;\n\t"
+          "bar.red.or.pred po, %2, %3, pi;\n\t"
+          "selp.u32 %0, 1, 0, po;\n\t}"
+          : "=r"(any)
+          : "r"(static_cast<uint32_t>(exceed)), "r"(kNamedBarSm), "r"(kSmThreads)
+          : "memory");
+      if (any) {
+        // exact column maxima of this half-tile, then move the reference and rescale
+        {
+          float v[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) v[c] = x[c];
+          int idx;
+          const float m = rows16_column_reduce<true>(v, lane, idx);
+          red[warp * 32 + 2 * idx + cp] = m;
+        }
+        named_bar_sync(kNamedBarSm, kSmThreads);
+        if (threadIdx.x < kRowsetRows) {
+          const int col = threadIdx.x, h = col >> 5, c = col & 31;
+          const float mt = fmaxf(fmaxf(red[(4 * h + 0) * 32 + c], red[(4 * h + 1) * 32 + c]),
+                                 fmaxf(red[(4 * h + 2) * 32 + c], red[(4 * h + 3) * 32 + c]));
+          const float mo = m_ref[col];
+          const float mn = fmaxf(mo, mt);
+          alpha_s[col] = (mo == -CUDART_INF_F) ? 0.f : ex2_approx(mo - mn);
+          m_ref[col] = mn;
+        }
+        named_bar_sync(kNamedBarSm, kSmThreads);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) lpart[c] *= alpha_s[32 * ch + 2 * c + cp];
+        if (i > 0) {
+          // O^T holds every PV so far once the previous half-tile's PV is done
+          const uint32_t gp = g - 1;
+          mbar_wait(bar(kBarPvDone + (gp & 1u)), (gp >> 1) & 1u, p.status, abort_flag);
+          tc_fence_after();
+#pragma unroll 1
+          for (int part = 0; part < 8; ++part) {  // 4 M-blocks x my 32 columns in halves
+            uint32_t o[16];
+            const int c0 = 16 * (part & 1);
+            const uint32_t ta = lane_base + kTmemO + 64 * (part >> 1) + 32 * ch + c0;
+            tmem_ld16(ta, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 16; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha_s[32 * ch + c0 + c]);
+            tmem_st16(ta, o);
+          }
+          tmem_st_wait();
+        }
+      }
+      // P^T row (this KV row, 16 query columns) into the stage's rope block. The two threads of
+      // a row swap halves so that each holds 16 consecutive columns: cp = 0 writes columns
+      // 32 ch + 0..15, cp = 1 columns 32 ch + 16..31 (two 16-byte chunks each).
+      float pq[16];
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 m4 = reinterpret_cast<const float4*>(m_ref)[8 * ch + c4];
+        const float m0 = cp ? m4.y : m4.x, m1 = cp ? m4.w : m4.z;
+        pq[2 * c4] = (x[2 * c4] > -CUDART_INF_F) ? ex2_approx(x[2 * c4] - m0) : 0.f;
+        pq[2 * c4 + 1] = (x[2 * c4 + 1] > -CUDART_INF_F) ? ex2_approx(x[2 * c4 + 1] - m1) : 0.f;
+        lpart[2 * c4] += pq[2 * c4];
+        lpart[2 * c4 + 1] += pq[2 * c4 + 1];
+      }
+      uint32_t w[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t lo = pack_bf16x2(pq[2 * j], pq[2 * j + 1]);      // columns 4 j + cp, 4 j + 2 + cp
+        const uint32_t hi = pack_bf16x2(pq[8 + 2 * j], pq[9 + 2 * j]);  // 16 more
+        const uint32_t own = cp ? hi : lo;
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, cp ? lo : hi, 2);
+        const uint32_t ev = cp ? recv : own, od = cp ? own : recv;  // even / odd columns
+        w[2 * j] = __byte_perm(ev, od, 0x5410);
+        w[2 * j + 1] = __byte_perm(ev, od, 0x7632);
+      }
+      {
+        uint8_t* prow = smem + kOffStage + b * kStageBytes + 8 * kBlk;
+        *reinterpret_cast<uint4*>(prow + sw128_offset(kvrow, 4 * ch + 2 * cp)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(prow + sw128_offset(kvrow, 4 * ch + 2 * cp + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(bar(kBarPready + b));
+    }
+
+    // ------------------------------------------------------------------ epilogue
+    if (nh > 0) {
+      const uint32_t gp = g - 1;
+      mbar_wait(bar(kBarPvDone + (gp & 1u)), (gp >> 1) & 1u, p.status, abort_flag);
+      tc_fence_after();
+    }
+    const RowsetRows rr = rowset_rows(p, s.r);
+    {
+      int idx;
+      const float l = rows16_column_reduce<false>(lpart, lane, idx);  // this warp's 16 rows
+      red[warp * 32 + 2 * idx + cp] = l;
+    }
+    named_bar_sync(kNamedBarSm, kSmThreads);
+    if (threadIdx.x < kRowsetRows) {
+      const int col = threadIdx.x, h = col >> 5, c = col & 31;
+      const float l = (red[(4 * h + 0) * 32 + c] + red[(4 * h + 1) * 32 + c]) +
+                      (red[(4 * h + 2) * 32 + c] + red[(4 * h + 3) * 32 + c]);
+      lfin[col] = l > 0.f ? 1.0f / l : 0.f;
+      const float lse2 = (l > 0.f) ? (m_ref[col] + __log2f(l)) : -CUDART_INF_F;
+      const float lse_nat = lse2 * 0.69314718055994530942f;
+      if (col < rr.nvalid) {
+        if (s.full) {
+          if (p.lse) p.lse[rr.base + col] = lse_nat;
+        } else {
+          p.part_lse[static_cast<long long>(s.slot) * kRowsetRows + col] = lse_nat;
+        }
+      }
+    }
+    named_bar_sync(kNamedBarSm, kSmThreads);
+    float inv[32];
+#pragma unroll
+    for (int c4 = 0; c4 < 8; ++c4) {
+      const float4 v = reinterpret_cast<const float4*>(lfin)[8 * ch + c4];
+      inv[4 * c4] = v.x;
+      inv[4 * c4 + 1] = v.y;
+      inv[4 * c4 + 2] = v.z;
+      inv[4 * c4 + 3] = v.w;
+    }
+    const int nv = rr.nvalid - 32 * ch;  // my columns c < nv exist
+    // thread (quadrant q, lane) holds channel 128 mb + 32 q + lane of query columns 32 ch + c
+#pragma unroll 1
+    for (int mb = 0; mb < 4; ++mb) {
+      uint32_t o[32];
+      if (nh > 0) {
+        tmem_ld32(lane_base + kTmemO + 64 * mb + 32 * ch, o);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) o[c] = 0u;
+      }
+      const int chan = 128 * mb + 32 * q + lane;
+      if (s.full) {
+        uint16_t* dst = p.out + (rr.base + 32 * ch) * kVdim + chan;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if (c < nv) dst[c * kVdim] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(o[c]) * inv[c], 0.f));
+        }
+      } else {
+        // a part of a split row-set: its normalised rows in fp32 for the merge
+        float* dst = p.part_o + (static_cast<long long>(s.slot) * kRowsetRows + 32 * ch) * kVdim + chan;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          if (c < nv) dst[c * kVdim] = __uint_as_float(o[c]) * inv[c];
+        }
+      }
+    }
+    tc_fence_before();
+    if (nh > 0) mbar_arrive(bar(kBarOFree));
+    named_bar_sync(kNamedBarSm, kSmThreads);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) bf16_attention_kernel(const __grid_constant__ AttnParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const uint32_t bars = smem_u32(smem) + kOffBars;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  const int warp = threadIdx.x >> 5;
+  // a dependent launch (the split merge) may be scheduled on SMs as this grid's CTAs exit
+  if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) {
+    auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+    mbar_init(bar(kBarQFull), kFillThreads);
+    mbar_init(bar(kBarQEmpty), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar(kBarFull + s), kFillThreads);
+      mbar_init(bar(kBarEmpty + s), 1);
+      mbar_init(bar(kBarSFull + s), 1);
+      mbar_init(bar(kBarPready + s), kSmThreads);
+      mbar_init(bar(kBarPvDone + s), 1);
+    }
+    mbar_init(bar(kBarOFree), kSmThreads);
+    for (int e = 0; e < kSlotRing; ++e) {
+      mbar_init(bar(kBarSlotsReady + e), kResThreads);
+      mbar_init(bar(kBarSlotFree + e), kSlotFreeArrivals);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp >= kFillWarp0) {
+    filler_role(p, smem, bars, abort_flag);
+  } else if (warp >= kResWarp0) {
+    resolver_role(p, smem, bars, abort_flag);
+  } else if (warp == kSIssuerWarp) {
+    if ((threadIdx.x & 31) == 0) s_issuer_role(p, smem, tmem, bars, abort_flag);
+    __syncwarp();
+  } else if (warp == kPvIssuerWarp) {
+    if ((threadIdx.x & 31) == 0) pv_issuer_role(p, smem, tmem, bars, abort_flag);
+    __syncwarp();
+  } else {
+    softmax_role(p, smem, tmem, bars, abort_flag);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+int bf16_attention_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_attention_bf16(const AttnParams& p, cudaStream_t stream) {
+  if (p.num_ctas == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(bf16_attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  bf16_attention_kernel<<<p.num_ctas, kThreads, kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace svt

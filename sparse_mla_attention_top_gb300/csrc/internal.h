@@ -121,10 +121,11 @@ cudaError_t launch_merge_splits(const float* o_part, const float* lse_part, int 
 cudaError_t launch_topk(const float* scores, int T, int N, long long stride, const int32_t* lens, int K, int32_t* out,
                         cudaStream_t stream);
 
+// Decode and grouped prefill over an e4m3 cache (128-row tiles staged through registers).
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
-// Grouped prefill over a bf16 cache with two 64-row half-tile stages (e4m3 caches use
-// launch_attention).
-cudaError_t launch_prefill(const AttnParams& p, cudaStream_t stream);
+// Decode and grouped prefill over a bf16 cache (two stages of 64-row half-tiles; decode
+// work units are half-tiles).
+cudaError_t launch_attention_bf16(const AttnParams& p, cudaStream_t stream);
 // Merges the partial results of the row-sets a stream-K decode split between CTAs; launched
 // right behind the attention kernel (programmatic dependent launch) and waiting for it.
 cudaError_t launch_streamk_merge(const AttnParams& p, cudaStream_t stream);
