@@ -161,25 +161,25 @@ struct SegWalk {
     return len < 0 ? 0 : (len > p.list_stride ? p.list_stride : len);
   }
 
-  __device__ bool next(const AttnParams& p, Seg& s) {
+  // The next segment's row-set and half-tile range (te = one past its last half-tile); the
+  // list length is filled in by with_len, so that a caller can put other reads in flight
+  // before it waits for the length.
+  __device__ bool next_range(const AttnParams& p, Seg& s, int& te) {
     if (p.sched == kSchedStreamK) {
       if (pos >= hi) return false;
       const long long nt = p.tiles_per_rowset;
       const long long r = pos / nt;
       const long long i0 = pos - r * nt;
-      long long te = hi - r * nt;
-      if (te > nt) te = nt;
-      pos = r * nt + te;
+      long long e = hi - r * nt;
+      if (e > nt) e = nt;
+      pos = r * nt + e;
       s.r = static_cast<int>(r);
       s.i0 = static_cast<int>(i0);
-      s.full = (i0 == 0 && te == nt);
+      s.full = (i0 == 0 && e == nt);
       const bool multi = (lo / nt) != ((hi - 1) / nt);
       s.slot = static_cast<int>(2ll * blockIdx.x + ((multi && idx > 0) ? 1 : 0));
       ++idx;
-      s.len = list_len(p, s.r);
-      const long long live = halves_of(s.len);
-      const long long end = te < live ? te : live;
-      s.n = end > i0 ? static_cast<int>(end - i0) : 0;
+      te = static_cast<int>(e);
       return true;
     }
     if (next_rowset >= p.num_rowsets) return false;
@@ -188,8 +188,20 @@ struct SegWalk {
     s.i0 = 0;
     s.full = 1;
     s.slot = 0;
-    s.len = list_len(p, s.r);
-    s.n = halves_of(s.len);
+    te = INT_MAX;
+    return true;
+  }
+  // s.len and s.n (half-tiles of the range that hold live entries) from the list length
+  __device__ static void with_len(Seg& s, int len, int te) {
+    s.len = len;
+    const int live = halves_of(len);
+    const int end = te < live ? te : live;
+    s.n = end > s.i0 ? end - s.i0 : 0;
+  }
+  __device__ bool next(const AttnParams& p, Seg& s) {
+    int te;
+    if (!next_range(p, s, te)) return false;
+    with_len(s, list_len(p, s.r), te);
     return true;
   }
 };
@@ -244,30 +256,41 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
   walk.init(p);
   Seg s;
   bool live = true;
-  while (live && walk.next(p, s)) {
-    if (s.n == 0) continue;
-    // the segment's list and, for decode, its request's block-table row and length
+  int te;
+  while (live && walk.next_range(p, s, te)) {
+    // first round of reads, all independent: the list length, the request id and the
+    // segment's first entry (read speculatively below K, dropped below if past the length)
     const int32_t* list;
-    ReqContext rc{nullptr, INT_MAX, true};
+    int len_raw, req = 0, raw;
+    const int e0 = s.i0 * kHalf + ltid;
     if (decode) {
       const int t = s.r / p.hchunks;
       list = p.topk + static_cast<long long>(t) * p.K;
-      if (has_table) {
-        const int req = p.req_of_token ? __ldg(p.req_of_token + t) : t;
-        rc.ok = req >= 0 && req < p.num_reqs;
-        if (rc.ok) {
-          rc.bt_row = p.block_table + static_cast<long long>(req) * p.max_blocks;
-          if (p.seq_lens != nullptr) rc.seq_len = __ldg(p.seq_lens + req);
-        }
-      }
+      len_raw = p.topk_len ? __ldg(p.topk_len + t) : p.K;
+      if (has_table) req = p.req_of_token ? __ldg(p.req_of_token + t) : t;
+      raw = e0 < p.K ? __ldg(list + e0) : kDeadEntry;
     } else {
       list = p.enc + static_cast<long long>(s.r >> 1) * p.list_stride;
+      len_raw = __ldg(p.lens + (s.r >> 1));
+      raw = e0 < p.list_stride ? __ldg(list + e0) : kDeadEntry;
+    }
+    const int cap = decode ? p.K : p.list_stride;
+    SegWalk::with_len(s, len_raw < 0 ? 0 : (len_raw > cap ? cap : len_raw), te);
+    if (s.n == 0) continue;
+    if (e0 >= s.len) raw = kDeadEntry;
+    // the request's block-table row and length (second round, with the page reads below)
+    ReqContext rc{nullptr, INT_MAX, true};
+    if (decode && has_table) {
+      rc.ok = req >= 0 && req < p.num_reqs;
+      if (rc.ok) {
+        rc.bt_row = p.block_table + static_cast<long long>(req) * p.max_blocks;
+        if (p.seq_lens != nullptr) rc.seq_len = __ldg(p.seq_lens + req);
+      }
     }
     auto entry = [&](int i) -> int {
       const int e = (s.i0 + i) * kHalf + ltid;
       return e < s.len ? __ldg(list + e) : kDeadEntry;
     };
-    int raw = entry(0);
     for (int i = 0; i < s.n; ++i, ++k) {
       // the next half-tile's entry read goes out together with this one's page read
       const int raw_next = i + 1 < s.n ? entry(i + 1) : kDeadEntry;
@@ -275,7 +298,14 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
       uint32_t mask = 0xFFFFFFFFu;
       if (decode) {
         if (raw != kDeadEntry) {
-          const int phys = page_of(raw, rc, p.max_blocks, p.page_size);
+          // the page word is read before the length check (in bounds of the table row
+          // either way), so that it travels with the request's length; slot_of drops it
+          // when a check fails
+          int phys = -1;
+          if (rc.bt_row != nullptr && raw >= 0) {
+            const int page = raw / p.page_size;
+            if (page < p.max_blocks) phys = __ldg(rc.bt_row + page);
+          }
           slot = slot_of(raw, phys, rc, has_table, p.max_blocks, p.page_size, p.num_pages, &err);
         }
       } else {
@@ -291,6 +321,9 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
           }
         }
       }
+      // the row is wanted a few half-tiles from now: start its trip from HBM into L2 here, so
+      // that the fill, when its stage frees, waits for L2 rather than for DRAM
+      if (slot >= 0) prefetch_l2_bulk(p.kv + static_cast<long long>(slot) * p.row_stride, kRowBytesBf16);
       const uint32_t e = k % kSlotRing;
       if (k >= kSlotRing && !mbar_wait(bar(kBarSlotFree + e), ((k / kSlotRing) - 1) & 1u, p.status, abort_flag)) {
         live = false;
@@ -314,12 +347,28 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, v
   auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
   const uint8_t* qb = reinterpret_cast<const uint8_t*>(p.q);
   uint32_t g = 0, qk = 0;
+  // Q^T of segment s's row-set, once the previous segment's last S^T is done with it
+  auto load_q = [&](const Seg& s) -> bool {
+    if (!mbar_wait(bar(kBarQEmpty), (qk & 1u) ^ 1u, p.status, abort_flag)) return false;
+    const RowsetRows rr = rowset_rows(p, s.r);
+    for (int idx = ftid; idx < kRowsetRows * 72; idx += kFillThreads) {
+      const int row = idx / 72, c = idx - row * 72;
+      const bool valid = row < rr.nvalid;
+      const uint8_t* src = qb + (valid ? (rr.base + row) * (kRow * 2) + c * 16 : 0);
+      cp_async16(sbase + kOffQ + (c >> 3) * kQBlk + sw128_offset(row, c & 7), src, valid ? 16u : 0u);
+    }
+    cp_async_arrive_noinc(bar(kBarQFull));
+    ++qk;
+    return true;
+  };
   SegWalk walk;
   walk.init(p);
   Seg s;
   bool live = true;
   while (live && walk.next(p, s)) {
     if (s.n == 0) continue;
+    // the first segment's Q^T needs no wait: it goes out before the first rows' slots exist
+    if (g == 0 && !load_q(s)) break;
     for (int i = 0; i < s.n; ++i, ++g) {
       const uint32_t st = g & 1u, e = g % kSlotRing;
       // half-tile g's slots, and its stage free (PV of half-tile g - 2 done)
@@ -352,21 +401,10 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, v
       cp_async_arrive_noinc(bar(kBarFull + st));
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarSlotFree + e));
-      if (i == 0) {
-        // Q^T of the segment's row-set, once the previous segment's last S^T is done with it
-        if (!mbar_wait(bar(kBarQEmpty), (qk & 1u) ^ 1u, p.status, abort_flag)) {
-          live = false;
-          break;
-        }
-        const RowsetRows rr = rowset_rows(p, s.r);
-        for (int idx = ftid; idx < kRowsetRows * 72; idx += kFillThreads) {
-          const int row = idx / 72, c = idx - row * 72;
-          const bool valid = row < rr.nvalid;
-          const uint8_t* src = qb + (valid ? (rr.base + row) * (kRow * 2) + c * 16 : 0);
-          cp_async16(sbase + kOffQ + (c >> 3) * kQBlk + sw128_offset(row, c & 7), src, valid ? 16u : 0u);
-        }
-        cp_async_arrive_noinc(bar(kBarQFull));
-        ++qk;
+      // a later segment's Q^T goes out after its first rows (their stage frees first)
+      if (i == 0 && g > 0 && !load_q(s)) {
+        live = false;
+        break;
       }
     }
   }

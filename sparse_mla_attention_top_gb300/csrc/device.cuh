@@ -119,6 +119,12 @@ __device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// Asks L2 to fetch `bytes` (a multiple of 16) at a 16-byte aligned global address; no data
+// comes back to the SM and nothing waits for it.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
 // Orders this thread's generic-proxy shared-memory writes (st.shared, completed cp.async)
 // before later async-proxy reads of them (tcgen05.mma operands).
 __device__ __forceinline__ void fence_proxy_async_smem() {
