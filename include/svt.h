@@ -152,7 +152,7 @@ SVT_API svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t 
  * needs lives in an 8 MiB array inside the library that every GPU loading the library holds
  * until the process exits. That bounds it: one CTA per query (num_splits = 1) works for any
  * batch (256 bytes of scratch); a split decode works while
- * svt_sparse_mla_decode_workspace_size(T, H, K, num_splits) <= 8 MiB (up to 31 CTAs with
+ * svt_sparse_mla_decode_workspace_size(T, H, K, num_splits) <= 8 MiB (up to 63 CTAs with
  * partial results). Anything larger returns SVT_ERR_WORKSPACE before any work is enqueued.
  *   status_out  optional device int32: receives this call's device status bits (the
  *               SVT_DEV_ERR_* values) when the call's kernels have run; NULL to skip.

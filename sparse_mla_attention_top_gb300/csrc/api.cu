@@ -96,7 +96,7 @@ DecodePlan plan_decode(int T, int H, int K, int num_splits, int unit_rows) {
 
 // Workspace: status header | partial outputs | partial LSEs.
 size_t decode_part_o_bytes(const DecodePlan& d) {
-  return round_up(2ull * d.num_ctas * svt::kRowsetRows * svt::kVdim * sizeof(float), 256);
+  return round_up(2ull * d.num_ctas * svt::kRowsetRows * svt::kVdim * sizeof(uint16_t), 256);
 }
 size_t decode_part_lse_bytes(const DecodePlan& d) {
   return round_up(2ull * d.num_ctas * svt::kRowsetRows * sizeof(float), 256);
@@ -228,7 +228,7 @@ svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const
   p.status = static_cast<int*>(ws);
   if (d.partials) {
     char* base = static_cast<char*>(ws) + svt::kStatusBytes;
-    p.part_o = reinterpret_cast<float*>(base);
+    p.part_o = reinterpret_cast<uint16_t*>(base);
     p.part_lse = reinterpret_cast<float*>(base + decode_part_o_bytes(d));
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

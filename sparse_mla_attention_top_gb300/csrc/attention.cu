@@ -38,8 +38,8 @@
 //               the CTA's schedule and posts each tile's descriptor in a ring of four.
 // Persistent CTAs walk a static schedule: stream-K over (row-set, tile) for decode, whole
 // row-sets round-robin for grouped prefill. Each part of a row-set split between CTAs is
-// written as fp32 partial rows and a partial LSE (slot 2c or 2c + 1 of CTA c); the merge
-// kernel, launched behind this one with programmatic dependent launch, combines them
+// written as normalised fp16 rows and an fp32 partial LSE (slot 2c or 2c + 1 of CTA c); the
+// merge kernel, launched behind this one with programmatic dependent launch, combines them
 // (merge.cu). A row-set no CTA boundary cuts is finished here.
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -869,10 +869,10 @@ __device__ __forceinline__ void softmax_role(const AttnParams& p, uint8_t* smem,
               if (c < nv) dst[c * kVdim] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(o[c]) * inv[c], 0.f));
             }
           } else {
-            float* dst = p.part_o + (static_cast<long long>(seg.slot) * kRowsetRows + 32 * h) * kVdim + chan;
+            uint16_t* dst = p.part_o + (static_cast<long long>(seg.slot) * kRowsetRows + 32 * h) * kVdim + chan;
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-              if (c < nv) dst[c * kVdim] = __uint_as_float(o[c]) * inv[c];
+              if (c < nv) dst[c * kVdim] = f32_to_f16_bits(__uint_as_float(o[c]) * inv[c]);
             }
           }
         }
@@ -895,7 +895,7 @@ __device__ __forceinline__ void softmax_role(const AttnParams& p, uint8_t* smem,
 }
 
 // The CTA's last segment: O^T from TMEM, scaled by 1 / l, into out (bf16) or the partial
-// slot (fp32), by all 16 warps. Warp w reads TMEM lane quadrant w % 4 (channels 32 (w % 4) +
+// slot (fp16), by all 16 warps. Warp w reads TMEM lane quadrant w % 4 (channels 32 (w % 4) +
 // lane of each M-block) and query columns 16 (w / 4) .. + 15.
 __device__ __forceinline__ void final_store(const AttnParams& p, const Seg& seg, const float* lfin, uint32_t tmem) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -931,10 +931,10 @@ __device__ __forceinline__ void final_store(const AttnParams& p, const Seg& seg,
         if (c < nv) dst[c * kVdim] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(o[c]) * inv[c], 0.f));
       }
     } else {
-      float* dst = p.part_o + (static_cast<long long>(seg.slot) * kRowsetRows + c0) * kVdim + chan;
+      uint16_t* dst = p.part_o + (static_cast<long long>(seg.slot) * kRowsetRows + c0) * kVdim + chan;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
-        if (c < nv) dst[c * kVdim] = __uint_as_float(o[c]) * inv[c];
+        if (c < nv) dst[c * kVdim] = f32_to_f16_bits(__uint_as_float(o[c]) * inv[c]);
       }
     }
   }

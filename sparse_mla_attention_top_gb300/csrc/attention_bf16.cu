@@ -24,8 +24,9 @@
 //
 // Work: persistent CTAs walk segments (a row-set and a range of its half-tiles). Decode uses
 // stream-K over (row-set, half-tile) so every SM gets the same number of half-tiles; a
-// row-set cut by a CTA boundary leaves fp32 partial rows and a partial LSE per part, which
-// the merge kernel (merge.cu) combines. Grouped prefill takes whole row-sets round-robin.
+// row-set cut by a CTA boundary leaves, per part, its normalised rows in fp16 and an fp32
+// partial LSE, which the merge kernel (merge.cu) combines. Grouped prefill takes whole
+// row-sets round-robin.
 //
 // Warp roles (512 threads):
 //   warps 0-7   softmax + epilogue: warp w reads the 16 rows of TMEM quadrant w % 4 (KV rows
@@ -363,6 +364,19 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, v
   };
   SegWalk walk;
   walk.init(p);
+  if (p.sched == kSchedStreamK && ftid < kRowsetRows) {
+    // a stream-K range holds at most a few segments: their Q rows go to L2 now, so that a
+    // segment boundary reloads Q^T from L2
+    SegWalk ahead = walk;
+    Seg sa;
+    int te;
+    bool first = true;
+    while (ahead.next_range(p, sa, te)) {
+      const RowsetRows rr = rowset_rows(p, sa.r);
+      if (!first && ftid < rr.nvalid) prefetch_l2_bulk(qb + (rr.base + ftid) * (kRow * 2), kRow * 2);
+      first = false;
+    }
+  }
   Seg s;
   bool live = true;
   while (live && walk.next(p, s)) {
@@ -673,6 +687,11 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
       if (nh > 0) {
         tmem_ld32(lane_base + kTmemO + 64 * mb + 32 * ch, o);
         tmem_ld_wait();
+        if (mb == 3) {
+          // O^T is read: the next segment's first PV may overwrite it while these stores run
+          tc_fence_before();
+          mbar_arrive(bar(kBarOFree));
+        }
       } else {
 #pragma unroll
         for (int c = 0; c < 32; ++c) o[c] = 0u;
@@ -685,16 +704,14 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
           if (c < nv) dst[c * kVdim] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(o[c]) * inv[c], 0.f));
         }
       } else {
-        // a part of a split row-set: its normalised rows in fp32 for the merge
-        float* dst = p.part_o + (static_cast<long long>(s.slot) * kRowsetRows + 32 * ch) * kVdim + chan;
+        // a part of a split row-set: its normalised rows in fp16 for the merge
+        uint16_t* dst = p.part_o + (static_cast<long long>(s.slot) * kRowsetRows + 32 * ch) * kVdim + chan;
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-          if (c < nv) dst[c * kVdim] = __uint_as_float(o[c]) * inv[c];
+          if (c < nv) dst[c * kVdim] = f32_to_f16_bits(__uint_as_float(o[c]) * inv[c]);
         }
       }
     }
-    tc_fence_before();
-    if (nh > 0) mbar_arrive(bar(kBarOFree));
     named_bar_sync(kNamedBarSm, kSmThreads);
   }
 }

@@ -62,7 +62,7 @@ struct AttnParams {
   int tiles_per_rowset;  // stream-K: tiles of the longest list
   long long total_tiles;
   int num_ctas;
-  float* part_o;    // [2 * num_ctas, 64, 512] fp32 (stream-K partial segments)
+  uint16_t* part_o;  // [2 * num_ctas, 64, 512] fp16 (stream-K partial segments, normalised)
   float* part_lse;  // [2 * num_ctas, 64]
   int* status;
 };

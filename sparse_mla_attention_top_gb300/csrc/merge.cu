@@ -6,7 +6,8 @@
 // normalised output:  lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * o_s.
 //
 // One warp per output row: the slice LSEs are reduced with warp shuffles, then each lane
-// accumulates 16 of the 512 channels. Bound by reading the fp32 partials.
+// accumulates 16 of the 512 channels. Bound by reading the partials.
+#include <cuda_fp16.h>
 #include <math_constants.h>
 
 #include "device.cuh"
@@ -88,21 +89,34 @@ __global__ void __launch_bounds__(256) merge_splits_kernel(const float* __restri
 constexpr int kMergeWarpsPerCta = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Eight fp16 partial values (16 bytes) -> fp32.
+__device__ __forceinline__ void f16x8_to_f32(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2_raw hr;
+    hr.x = static_cast<unsigned short>(w[i] & 0xFFFFu);
+    hr.y = static_cast<unsigned short>(w[i] >> 16);
+    const float2 t = __half22float2(__half2(hr));
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
 // One half (channels 256 half .. +255) of output row `row` of a split row-set whose parts'
-// rows are part_o[part_row(s)], part_lse[part_row(s)]: lane l holds part l's LSE, and the
-// first four parts' half-rows are requested in the same trip.
+// rows (fp16) are part_o[part_row(s)], part_lse[part_row(s)]: lane l holds part l's LSE, and
+// the first four parts' half-rows are requested in the same trip.
 template <typename PartRow>
 __device__ __forceinline__ void merge_half_row(const AttnParams& p, int parts, PartRow part_row, int half,
                                                uint16_t* out_row, float* lse_out) {
   const int lane = threadIdx.x & 31;
   const float ls = lane < parts ? __ldcg(p.part_lse + part_row(lane)) : -CUDART_INF_F;
   const int ch0 = 256 * half + 8 * lane;  // this lane's 8 channels
-  float4 x[4][2];
+  uint4 x[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const float4* o = reinterpret_cast<const float4*>(p.part_o + part_row(min(j, parts - 1)) * kVdim + ch0);
-    x[j][0] = __ldcg(o);
-    x[j][1] = __ldcg(o + 1);
+    x[j] = j < parts ? __ldcg(reinterpret_cast<const uint4*>(p.part_o + part_row(j) * kVdim + ch0))
+                     : make_uint4(0, 0, 0, 0);
   }
   // L = ln sum_s exp(lse_s) (parts past 32 folded in by a loop)
   float mx = ls;
@@ -122,26 +136,19 @@ __device__ __forceinline__ void merge_half_row(const AttnParams& p, int parts, P
       const float lsj = s < 32 ? __shfl_sync(0xffffffffu, ls, s) : __ldcg(p.part_lse + part_row(s));
       return lsj == -CUDART_INF_F ? 0.f : ex2_approx((lsj - L) * kLog2e);
     };
-    auto accumulate = [&](float w, const float4(&v)[2]) {
-      acc[0] += w * v[0].x;
-      acc[1] += w * v[0].y;
-      acc[2] += w * v[0].z;
-      acc[3] += w * v[0].w;
-      acc[4] += w * v[1].x;
-      acc[5] += w * v[1].y;
-      acc[6] += w * v[1].z;
-      acc[7] += w * v[1].w;
+    auto accumulate = [&](float w, const uint4& v) {
+      float f[8];
+      f16x8_to_f32(v, f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += w * f[i];
     };
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float w = weight(j);  // every lane shuffles; parts past the last weigh nothing
       if (j < parts) accumulate(w, x[j]);
     }
-    for (int s = 4; s < parts; ++s) {
-      const float4* o = reinterpret_cast<const float4*>(p.part_o + part_row(s) * kVdim + ch0);
-      const float4 v[2] = {__ldcg(o), __ldcg(o + 1)};
-      accumulate(weight(s), v);
-    }
+    for (int s = 4; s < parts; ++s)
+      accumulate(weight(s), __ldcg(reinterpret_cast<const uint4*>(p.part_o + part_row(s) * kVdim + ch0)));
   }
   uint4 packed;
   packed.x = pack_bf16x2(acc[0], acc[1]);
