@@ -41,9 +41,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # streamk_merge_kernel), keyed by the hash of their sources it was measured on (stale -> null).
 TRAFFIC_BY_SOURCE = {
     # full-size capture (profiles/decode_bf16_attention_ncu.md, ncu --cache-control none after
-    # bench.py's own L2 flush): attention 170.21 MB read + 62.25 MB written, merge 1.07 MB read
-    # + 0.21 MB written
-    "c1bc9cb17befaea7": (170.21 + 62.25 + 1.07 + 0.21) * 1e6,
+    # bench.py's own L2 flush): attention 167.23 MB read + 60.37 MB written, merge 1.08 MB read
+    # + 0.18 MB written
+    "ac0822ce2d408d04": (167.23 + 60.37 + 1.08 + 0.18) * 1e6,
 }
 
 
@@ -243,7 +243,7 @@ def replica_throughput(units_per_rank: int, ms_max: float, world: int) -> float:
 def source_hash() -> str:
     """Hash of the sources of the two decode kernels the roofline line times together."""
     h = hashlib.sha256()
-    for name in ("attention_bf16.cu", "merge.cu"):
+    for name in ("attention.cu", "merge.cu"):
         with open(os.path.join(ROOT, "sparse_mla_attention_top_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -482,8 +482,8 @@ def main():
             "gather_gbs": nb["gathered"] / (ms / 1000.0) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": TRAFFIC_BY_SOURCE.get(th),
-                         "kernel": ("bf16_attention_kernel + streamk_merge_kernel (one decode call, timed together)"
-                                    if launches_per_step == 2 else "bf16_attention_kernel (one decode call)"),
+                         "kernel": ("tile_attention_kernel + streamk_merge_kernel (one decode call, timed together)"
+                                    if launches_per_step == 2 else "tile_attention_kernel (one decode call)"),
                          "algorithmic_bytes": nb["algorithmic"], "peak_source": peak_src, "source_hash": th},
             "clocks": clk, "gpu_launches": launches_per_step * args.steps, "e2e": e2e, "cpu_baseline": cpu,
             "prefill": prefill,

@@ -14,7 +14,7 @@ CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 LIB = PKG / "libsvt.so"
 BUILD_DIR = PKG / "_build"
-SOURCES = ["api.cu", "attention.cu", "attention_bf16.cu", "resolve.cu", "union.cu", "merge.cu", "noalloc.cu", "topk.cu"]
+SOURCES = ["api.cu", "attention.cu", "resolve.cu", "union.cu", "merge.cu", "noalloc.cu", "topk.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden", f"-I{INCLUDE}", f"-I{CSRC}"]
 

@@ -107,7 +107,7 @@ size_t decode_ws_bytes(const DecodePlan& d) {
   return b;
 }
 
-int decode_unit_rows(svt_kv_dtype dtype) { return dtype == SVT_KV_BF16 ? svt::kTileRows / 2 : svt::kTileRows; }
+int decode_unit_rows(svt_kv_dtype) { return svt::kTileRows / 2; }
 
 }  // namespace
 
@@ -238,7 +238,7 @@ svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const
     p.total_tiles = d.rowsets;
     p.num_ctas = d.rowsets;
   }
-  cudaError_t e = kv->dtype == SVT_KV_BF16 ? svt::launch_attention_bf16(p, s) : svt::launch_attention(p, s);
+  cudaError_t e = svt::launch_attention(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
   if (d.partials) {
     e = svt::launch_streamk_merge(p, s);
@@ -314,8 +314,7 @@ svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T, int32_t
   if (sms <= 0) sms = 1;
   p.num_ctas = p.num_rowsets < sms ? p.num_rowsets : sms;
   p.status = static_cast<int*>(ws);
-  cudaError_t e = kv->dtype == SVT_KV_BF16 ? svt::launch_attention_bf16(p, reinterpret_cast<cudaStream_t>(stream))
-                                           : svt::launch_attention(p, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = svt::launch_attention(p, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
   return SVT_OK;
 }

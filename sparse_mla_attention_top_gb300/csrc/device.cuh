@@ -5,6 +5,8 @@
 
 #include <cstdint>
 
+#include <cuda_fp16.h>
+
 #include "svt.h"
 
 namespace svt {
@@ -293,5 +295,29 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
+
+// A block scale split into two f16 (hi = the nearest f16, lo = the f16 nearest the rest),
+// each broadcast to both halves of an f16x2.
+__device__ __forceinline__ void split_scale_f16x2(float scale, uint32_t& hi2, uint32_t& lo2) {
+  const __half hi = __float2half_rn(scale);
+  const __half lo = __float2half_rn(scale - __half2float(hi));
+  const uint16_t h = __half_as_ushort(hi), l = __half_as_ushort(lo);
+  hi2 = static_cast<uint32_t>(h) | (static_cast<uint32_t>(h) << 16);
+  lo2 = static_cast<uint32_t>(l) | (static_cast<uint32_t>(l) << 16);
+}
+
+// Two e4m3 codes (low byte = lower channel) -> two f16 of code * scale: the codes widen to
+// f16 exactly, code * lo is rounded to f16 and code * hi + that is rounded once, which is the
+// f16 nearest code * scale but for rare one-ulp differences (max relative error 5.1e-4 over
+// every finite code against 4.9e-4 for the fp32 product rounded to f16). Three
+// instructions per pair of codes.
+__device__ __forceinline__ uint32_t e4m3x2_times_f16x2(uint32_t codes16, uint32_t hi2, uint32_t lo2) {
+  uint32_t c2, t, r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(c2) : "h"(static_cast<unsigned short>(codes16)));
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(t) : "r"(c2), "r"(lo2));
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(c2), "r"(hi2), "r"(t));
+  return r;
+}
+
 
 }  // namespace svt

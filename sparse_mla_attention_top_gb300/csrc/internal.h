@@ -16,8 +16,8 @@ constexpr int kRowBytesBf16 = 1152;
 constexpr int kRowBytesFp8 = 656;  // 512 e4m3 | 4 fp32 scales | 64 bf16 rope
 constexpr size_t kStatusBytes = 256;  // status header at the start of every workspace
 
-// Attention kernel geometry (the tcgen05 tile): a tile is 128 KV rows (the MMA M), a
-// row-set is up to 64 query rows sharing one KV list (the MMA N).
+// Attention geometry: a row-set is up to 64 query rows sharing one KV list (the MMA N); the
+// kernel stages KV rows in half-tiles of kTileRows / 2 = 64 (the MMA M of S^T).
 constexpr int kTileRows = 128;
 constexpr int kRowsetRows = 64;
 
@@ -121,17 +121,14 @@ cudaError_t launch_merge_splits(const float* o_part, const float* lse_part, int 
 cudaError_t launch_topk(const float* scores, int T, int N, long long stride, const int32_t* lens, int K, int32_t* out,
                         cudaStream_t stream);
 
-// Decode and grouped prefill over an e4m3 cache (128-row tiles staged through registers).
+// Decode and grouped prefill over either cache dtype (two shared-memory stages of 64-row
+// half-tiles; decode work units are half-tiles).
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
-// Decode and grouped prefill over a bf16 cache (two stages of 64-row half-tiles; decode
-// work units are half-tiles).
-cudaError_t launch_attention_bf16(const AttnParams& p, cudaStream_t stream);
 // Merges the partial results of the row-sets a stream-K decode split between CTAs; launched
 // right behind the attention kernel (programmatic dependent launch) and waiting for it.
 cudaError_t launch_streamk_merge(const AttnParams& p, cudaStream_t stream);
 
 // Records the message svt_last_error_string() returns on this thread and passes `st` back.
 svt_status set_last_error(svt_status st, const char* fmt, ...);
-int attention_smem_bytes();
 
 }  // namespace svt
