@@ -8,8 +8,9 @@
 // One CTA per query. Scores become order-preserving 32-bit keys (NaN -> 0, the lowest),
 // kept in shared memory when the row fits. A most-significant-digit-first radix select
 // (four 8-bit digits, per-warp shared histograms) finds the K-th largest key exactly and
-// how many keys equal to it are kept; one ordered pass then compacts the kept positions
-// with warp ballots and a block-wide scan, so the output is ascending by construction.
+// how many keys equal to it are kept; the kept positions are then compacted in position
+// order (warp-contiguous ranges, ballots, one scan over the warps), so the output is
+// ascending by construction.
 #include <cstdint>
 
 #include "internal.h"
@@ -31,42 +32,15 @@ __device__ __forceinline__ uint32_t score_key(float x) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-constexpr int kBatch = 8;  // positions per thread per compaction round
-
 struct TopkShared {
   uint32_t hist[256];
-  uint32_t cnt[kBatch * kTopkWarps];  // per-(batch slot, warp) counts of the current round
-  uint32_t off[kBatch * kTopkWarps];  // their exclusive prefix in position order
-  uint32_t total;
+  uint32_t cnt[2 * kTopkWarps];  // per-warp counts of keys > thr, then their exclusive prefix
+  uint32_t off[2 * kTopkWarps];  // the same for keys == thr
   uint32_t digit, above;
 };
 
 // keys + per-warp histograms (dynamic) + the block's scalars (static) within 227 KB
 static_assert(kKeysInSmemMax * 4 + kTopkWarps * 256 * 4 + sizeof(TopkShared) <= 232448, "top-k smem budget");
-
-// Exclusive prefix of sh.cnt (256 values in position order) into sh.off, total into
-// sh.total; run by warp 0, lane l taking values 8l .. 8l + 7.
-__device__ __forceinline__ void scan_counts(TopkShared& sh, int lane) {
-  uint32_t v[8], tot = 0;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    v[i] = sh.cnt[8 * lane + i];
-    tot += v[i];
-  }
-  uint32_t incl = tot;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t u = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += u;
-  }
-  uint32_t acc = incl - tot;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    sh.off[8 * lane + i] = acc;
-    acc += v[i];
-  }
-  if (lane == 31) sh.total = incl;
-}
 
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ scores, int N, long long stride,
                                                              const int32_t* __restrict__ lens, int K,
@@ -163,48 +137,57 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   const uint32_t thr = prefix;
   const uint32_t need = rank;  // keys equal to thr to keep, lowest positions first
 
-  // ordered compaction: kept = key > thr, or key == thr among the first `need` equal ones.
-  // A round covers kBatch x 1024 positions: slot u of thread (warp, lane) is position
-  // j0 + 1024 u + 32 warp + lane, so (u, warp, lane) is position order.
-  uint32_t base_out = 0, base_eq = 0;
+  // ordered compaction. Kept: key > thr, or key == thr among the first `need` equal keys in
+  // position order. A kept key's output position is (keys > thr before it) + min(keys == thr
+  // before it, need). Warp w scans positions [w seg, (w + 1) seg) 32 at a time: one pass
+  // counts its keys above and equal to thr, a scan over the 32 warps gives each warp its
+  // prefix, and a second pass writes.
+  const int seg = ((len + kTopkThreads - 1) / kTopkThreads) * 32;  // a multiple of 32
+  const int w0 = warp * seg;
+  const int w1 = min(len, w0 + seg);
   const uint32_t lt_mask = (1u << lane) - 1u;
-#pragma unroll 1
-  for (int j0 = 0; j0 < len; j0 += kBatch * kTopkThreads) {
-    uint32_t key[kBatch], eq_b[kBatch], kept_b[kBatch];
+  auto key_at = [&](int j) -> uint32_t { return in_smem ? keys_smem[j] : score_key(__ldg(row + j)); };
+  uint32_t n_gt = 0, n_eq = 0;
+  for (int j0 = w0; j0 < w1; j0 += 32) {
+    const int j = j0 + lane;
+    const uint32_t k = j < w1 ? key_at(j) : 0u;
+    n_gt += __popc(__ballot_sync(0xffffffffu, j < w1 && k > thr));
+    n_eq += __popc(__ballot_sync(0xffffffffu, j < w1 && k == thr));
+  }
+  if (lane == 0) {
+    sh.cnt[warp] = n_gt;
+    sh.off[warp] = n_eq;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t g = sh.cnt[lane], e = sh.off[lane];
+    uint32_t gi = g, ei = e;
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int j = j0 + u * kTopkThreads + tid;
-      key[u] = j < len ? (in_smem ? keys_smem[j] : score_key(__ldg(row + j))) : 0u;
-      eq_b[u] = __ballot_sync(0xffffffffu, j < len && key[u] == thr);
-      if (lane == 0) sh.cnt[u * kTopkWarps + warp] = __popc(eq_b[u]);
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t ug = __shfl_up_sync(0xffffffffu, gi, o), ue = __shfl_up_sync(0xffffffffu, ei, o);
+      if (lane >= o) {
+        gi += ug;
+        ei += ue;
+      }
     }
-    __syncthreads();
-    if (warp == 0) scan_counts(sh, lane);
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int j = j0 + u * kTopkThreads + tid;
-      const bool eq = (eq_b[u] >> lane) & 1u;
-      const uint32_t eq_before = base_eq + sh.off[u * kTopkWarps + warp] + __popc(eq_b[u] & lt_mask);
-      const bool kept = (j < len && key[u] > thr) || (eq && eq_before < need);
-      kept_b[u] = __ballot_sync(0xffffffffu, kept);
-    }
-    base_eq += sh.total;
-    __syncthreads();  // the equal-key offsets are read
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u)
-      if (lane == 0) sh.cnt[u * kTopkWarps + warp] = __popc(kept_b[u]);
-    __syncthreads();
-    if (warp == 0) scan_counts(sh, lane);
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const uint32_t pos = base_out + sh.off[u * kTopkWarps + warp] + __popc(kept_b[u] & lt_mask);
-      // exactly K are kept; the bound is a guard
-      if (((kept_b[u] >> lane) & 1u) && pos < static_cast<uint32_t>(K)) dst[pos] = j0 + u * kTopkThreads + tid;
-    }
-    base_out += sh.total;
-    __syncthreads();
+    sh.cnt[32 + lane] = gi - g;  // exclusive prefixes
+    sh.off[32 + lane] = ei - e;
+  }
+  __syncthreads();
+  uint32_t gt_before = sh.cnt[32 + warp], eq_before = sh.off[32 + warp];
+  for (int j0 = w0; j0 < w1; j0 += 32) {
+    const int j = j0 + lane;
+    const uint32_t k = j < w1 ? key_at(j) : 0u;
+    const uint32_t b_gt = __ballot_sync(0xffffffffu, j < w1 && k > thr);
+    const uint32_t b_eq = __ballot_sync(0xffffffffu, j < w1 && k == thr);
+    const uint32_t g = gt_before + __popc(b_gt & lt_mask);
+    const uint32_t e = eq_before + __popc(b_eq & lt_mask);
+    const bool kept = ((b_gt >> lane) & 1u) || (((b_eq >> lane) & 1u) && e < need);
+    const uint32_t pos = g + (e < need ? e : need);
+    // exactly K are kept; the bound is a guard
+    if (kept && pos < static_cast<uint32_t>(K)) dst[pos] = j;
+    gt_before += __popc(b_gt);
+    eq_before += __popc(b_eq);
   }
 }
 
