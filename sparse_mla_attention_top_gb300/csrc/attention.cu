@@ -97,7 +97,7 @@ constexpr int kOffAlpha = kOffMref + kRowsetRows * 4;  // float[64]
 constexpr int kOffRed = kOffAlpha + kRowsetRows * 4;   // float[8][32]
 constexpr int kOffLfin = kOffRed + 8 * 32 * 4;         // float[64]
 constexpr int kOffBars = kOffLfin + kRowsetRows * 4;   // uint64[kNumBars]
-constexpr int kOffMisc = kOffBars + 24 * 8;            // tmem base, abort flag
+constexpr int kOffMisc = kOffBars + 32 * 8;            // tmem base, abort flag
 constexpr int kSmemUsed = kOffMisc + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory map exceeds 227 KB");
@@ -106,15 +106,19 @@ static_assert(kSmemBytes <= 232448, "shared memory map exceeds 227 KB");
 constexpr int kBarQFull = 0;        // the fillers' Q^T copies landed (cp.async arrivals)
 constexpr int kBarQEmpty = 1;       // last S^T of the segment issued and done
 constexpr int kBarFull = 2;         // 2: a half-tile's rows landed in stage s
-constexpr int kBarEmpty = 4;        // 2: PV done with stage s
-constexpr int kBarSFull = 6;        // 2: S^T buffer b ready
-constexpr int kBarPready = 8;       // 2: P^T of the half-tile in stage s written
-constexpr int kBarPvDone = 10;      // 2: PV of the half-tile in stage s done
-constexpr int kBarOFree = 12;       // the segment's epilogue has read O^T
-constexpr int kBarSlotsReady = 13;  // 4: ring entry k % 4 holds half-tile k's slots
-constexpr int kBarSlotFree = 17;    // 4: softmax and fillers are done with ring entry k % 4
-constexpr int kBarQReady = 21;      // e4m3 caches: Q^T converted to f16 in place (softmax warps)
-constexpr int kNumBars = 22;
+constexpr int kBarEmpty = 4;        // 8: 4 s + j: PV done with part j of stage s (see kEmptyParts)
+constexpr int kBarSFull = 12;       // 2: S^T buffer b ready
+constexpr int kBarPready = 14;      // 2: P^T of the half-tile in stage s written
+constexpr int kBarPvDone = 16;      // 2: PV of the half-tile in stage s done
+constexpr int kBarOFree = 18;       // the segment's epilogue has read O^T
+constexpr int kBarSlotsReady = 19;  // 4: ring entry k % 4 holds half-tile k's slots
+constexpr int kBarSlotFree = 23;    // 4: softmax and fillers are done with ring entry k % 4
+constexpr int kBarQReady = 27;      // e4m3 caches: Q^T converted to f16 in place (softmax warps)
+constexpr int kNumBars = 28;
+// PV frees a stage in four parts, one per 128-channel M-block: part j (< 3) is blocks 2 j and
+// 2 j + 1 (V channels 128 j ..), part 3 blocks 6, 7 and 8 (the rope block, holding P^T, which
+// every M-block reads). The fillers refill each part as soon as it is free.
+constexpr int kEmptyParts = 4;
 static_assert(kNumBars * 8 <= kOffMisc - kOffBars, "barrier block");
 constexpr int kSlotFreeArrivals = kSmThreads / 32 + kFillWarps;  // one per softmax / filler warp
 
@@ -480,7 +484,10 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, v
         rows.load(p, slots, ftid);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarSlotFree + e));
-        if (!mbar_wait(bar(kBarEmpty + st), ((g >> 1) & 1u) ^ 1u, p.status, abort_flag)) {
+        // the converting stores go in one sweep once the whole stage is free (the last part
+        // frees last); storing part by part costs registers the conversion needs
+        if (!mbar_wait(bar(kBarEmpty + kEmptyParts * st + kEmptyParts - 1), ((g >> 1) & 1u) ^ 1u, p.status,
+                       abort_flag)) {
           live = false;
           break;
         }
@@ -488,9 +495,9 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, v
         fence_proxy_async_smem();
         mbar_arrive(bar(kBarFull + st));
       } else {
-        // half-tile g's slots, and its stage free (PV of half-tile g - 2 done)
-        if (!mbar_wait(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, p.status, abort_flag) ||
-            !mbar_wait(bar(kBarEmpty + st), ((g >> 1) & 1u) ^ 1u, p.status, abort_flag)) {
+        // half-tile g's slots; the stage's parts are waited for below, each as PV of
+        // half-tile g - 2 frees it
+        if (!mbar_wait(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, p.status, abort_flag)) {
           live = false;
           break;
         }
@@ -510,10 +517,19 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, v
           dst[j] = stage + sw128_offset(row, chunk);
         }
 #pragma unroll
-        for (int blk = 0; blk < kBlocks; ++blk) {
+        for (int part = 0; part < kEmptyParts; ++part) {
+          if (!mbar_wait(bar(kBarEmpty + kEmptyParts * st + part), ((g >> 1) & 1u) ^ 1u, p.status, abort_flag)) {
+            live = false;
+            break;
+          }
 #pragma unroll
-          for (int j = 0; j < 4; ++j) cp_async16(dst[j] + blk * kBlk, src[j] + (nbytes[j] ? blk * 128 : 0), nbytes[j]);
+          for (int blk = 2 * part; blk < (part == 3 ? kBlocks : 2 * part + 2); ++blk) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              cp_async16(dst[j] + blk * kBlk, src[j] + (nbytes[j] ? blk * 128 : 0), nbytes[j]);
+          }
         }
+        if (!live) break;
         cp_async_arrive_noinc(bar(kBarFull + st));
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarSlotFree + e));
@@ -596,8 +612,8 @@ __device__ void pv_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem
           const uint64_t bp = smem_desc_sw128(pt + ks * 2048, kQBlk, 1024);
           umma_f16(tmem + kTmemO + 64 * mb, a, bp, kIdescPV<kF16>, (i > 0 || ks > 0) ? 1u : 0u);
         }
+        umma_commit(bar(kBarEmpty + kEmptyParts * b + mb));  // M-block mb's V blocks are read
       }
-      umma_commit(bar(kBarEmpty + b));
       umma_commit(bar(kBarPvDone + b));
     }
   }
@@ -854,7 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1) tile_attention_kernel(const __gri
     mbar_init(bar(kBarQEmpty), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kBarFull + s), kFillThreads);
-      mbar_init(bar(kBarEmpty + s), 1);
+      for (int j = 0; j < kEmptyParts; ++j) mbar_init(bar(kBarEmpty + kEmptyParts * s + j), 1);
       mbar_init(bar(kBarSFull + s), 1);
       mbar_init(bar(kBarPready + s), kSmThreads);
       mbar_init(bar(kBarPvDone + s), 1);
