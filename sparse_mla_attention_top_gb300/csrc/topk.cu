@@ -11,6 +11,8 @@
 // how many keys equal to it are kept; the kept positions are then compacted in position
 // order (warp-contiguous ranges, ballots, one scan over the warps), so the output is
 // ascending by construction.
+#include <cooperative_groups.h>
+
 #include <cstdint>
 
 #include "internal.h"
@@ -33,64 +35,77 @@ __device__ __forceinline__ uint32_t score_key(float x) {
 }
 
 struct TopkShared {
-  uint32_t hist[256];
+  uint32_t hist[2][256];  // per pass, alternating (a cluster peer reads the previous one)
   uint32_t cnt[2 * kTopkWarps];  // per-warp counts of keys > thr, then their exclusive prefix
   uint32_t off[2 * kTopkWarps];  // the same for keys == thr
   uint32_t digit, above;
+  uint32_t tot_gt, tot_eq;  // this CTA's kept-key counts (read by the next CTA of a cluster)
 };
 
 // keys + per-warp histograms (dynamic) + the block's scalars (static) within 227 KB
 static_assert(kKeysInSmemMax * 4 + kTopkWarps * 256 * 4 + sizeof(TopkShared) <= 232448, "top-k smem budget");
 
+// kSplit CTAs (a thread-block cluster when 2) share one query: CTA rank r takes positions
+// [r h, (r + 1) h) of the row, h = ceil(len / kSplit) rounded up to 32. Each pass's histogram
+// is the sum of the CTAs' (read across the cluster), so every CTA takes the same digit
+// decisions; the compaction offsets CTA r by the kept counts of the CTAs before it.
+template <int kSplit>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ scores, int N, long long stride,
                                                              const int32_t* __restrict__ lens, int K,
                                                              int32_t* __restrict__ out) {
   extern __shared__ uint32_t dyn_smem[];
   uint32_t* warp_hist = dyn_smem;                   // [32 warps][256 bins]
-  uint32_t* keys_smem = dyn_smem + kTopkWarps * 256;  // the row's keys, when they fit
+  uint32_t* keys_smem = dyn_smem + kTopkWarps * 256;  // this CTA's keys, when they fit
   __shared__ TopkShared sh;
-  const int t = blockIdx.x;
+  const int t = blockIdx.x / kSplit;
+  const int cr = kSplit == 1 ? 0 : static_cast<int>(cooperative_groups::this_cluster().block_rank());
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int len = lens ? lens[t] : N;
   len = len < 0 ? 0 : (len > N ? N : len);
   const float* row = scores + static_cast<long long>(t) * stride;
   int32_t* dst = out + static_cast<long long>(t) * K;
 
-  if (len <= K) {  // every candidate is kept
-    for (int j = tid; j < K; j += kTopkThreads) dst[j] = j < len ? j : -1;
+  if (len <= K) {  // every candidate is kept (the same branch in every CTA of the cluster)
+    if (cr == 0)
+      for (int j = tid; j < K; j += kTopkThreads) dst[j] = j < len ? j : -1;
     return;
   }
-  const bool in_smem = len <= kKeysInSmemMax;
+  const int half = ((len + kSplit - 1) / kSplit + 31) & ~31;
+  const int lo = min(len, cr * half), hi = min(len, lo + half);
+  const int n = hi - lo;  // this CTA's positions lo .. hi - 1
+  const bool in_smem = n <= kKeysInSmemMax;
   if (in_smem) {
     // eight loads in flight per thread, then their keys
 #pragma unroll 1
-    for (int j0 = 0; j0 < len; j0 += 8 * kTopkThreads) {
+    for (int j0 = 0; j0 < n; j0 += 8 * kTopkThreads) {
       float v[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int j = j0 + u * kTopkThreads + tid;
-        v[u] = j < len ? __ldg(row + j) : 0.f;
+        v[u] = j < n ? __ldg(row + lo + j) : 0.f;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int j = j0 + u * kTopkThreads + tid;
-        if (j < len) keys_smem[j] = score_key(v[u]);
+        if (j < n) keys_smem[j] = score_key(v[u]);
       }
     }
   }
+  auto key_at = [&](int j) -> uint32_t { return in_smem ? keys_smem[j] : score_key(__ldg(row + lo + j)); };
 
   // radix select: find thr = the K-th largest key, and `need` = how many keys equal to thr
   // are kept (the ones at the lowest positions)
   uint32_t prefix = 0, prefix_mask = 0;
   uint32_t rank = static_cast<uint32_t>(K);  // 1-based rank still to find among the matching keys
   uint32_t* my_hist = warp_hist + warp * 256;
+  int buf = 0;
 #pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8) {
+  for (int shift = 24; shift >= 0; shift -= 8, buf ^= 1) {
     for (int b = lane; b < 256; b += 32) my_hist[b] = 0;
     __syncthreads();
     // one histogram per warp, so warps never contend with each other
-    for (int j = tid; j < len; j += kTopkThreads) {
-      const uint32_t k = in_smem ? keys_smem[j] : score_key(__ldg(row + j));
+    for (int j = tid; j < n; j += kTopkThreads) {
+      const uint32_t k = key_at(j);
       if ((k & prefix_mask) == prefix) atomicAdd(&my_hist[(k >> shift) & 255u], 1u);
     }
     __syncthreads();
@@ -98,15 +113,26 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
       uint32_t c = 0;
 #pragma unroll 8
       for (int w = 0; w < kTopkWarps; ++w) c += warp_hist[w * 256 + tid];
-      sh.hist[tid] = c;
+      sh.hist[buf][tid] = c;
     }
-    __syncthreads();
+    if constexpr (kSplit > 1) {
+      cooperative_groups::this_cluster().sync();  // every CTA's histogram of this pass is complete
+    } else {
+      __syncthreads();
+    }
     if (warp == 0) {
-      // bins from the top: lane l owns bins 255 - 8l .. 248 - 8l
+      // bins from the top: lane l owns bins 255 - 8l .. 248 - 8l (summed over the cluster)
       uint32_t c[8], tot = 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        c[i] = sh.hist[255 - 8 * lane - i];
+        uint32_t v = sh.hist[buf][255 - 8 * lane - i];
+        if constexpr (kSplit > 1) {
+          auto cl = cooperative_groups::this_cluster();
+#pragma unroll
+          for (int q = 1; q < kSplit; ++q)
+            v += *cl.map_shared_rank(&sh.hist[buf][255 - 8 * lane - i], static_cast<unsigned>((cr + q) % kSplit));
+        }
+        c[i] = v;
         tot += c[i];
       }
       uint32_t incl = tot;  // inclusive prefix over lanes (higher bins first)
@@ -139,14 +165,13 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
 
   // ordered compaction. Kept: key > thr, or key == thr among the first `need` equal keys in
   // position order. A kept key's output position is (keys > thr before it) + min(keys == thr
-  // before it, need). Warp w scans positions [w seg, (w + 1) seg) 32 at a time: one pass
-  // counts its keys above and equal to thr, a scan over the 32 warps gives each warp its
-  // prefix, and a second pass writes.
-  const int seg = ((len + kTopkThreads - 1) / kTopkThreads) * 32;  // a multiple of 32
+  // before it, need). Warp w scans local positions [w seg, (w + 1) seg) 32 at a time: one
+  // pass counts its keys above and equal to thr, a scan over the 32 warps (and the CTAs
+  // before this one) gives each warp its prefix, and a second pass writes.
+  const int seg = ((n + kTopkThreads - 1) / kTopkThreads) * 32;  // a multiple of 32
   const int w0 = warp * seg;
-  const int w1 = min(len, w0 + seg);
+  const int w1 = min(n, w0 + seg);
   const uint32_t lt_mask = (1u << lane) - 1u;
-  auto key_at = [&](int j) -> uint32_t { return in_smem ? keys_smem[j] : score_key(__ldg(row + j)); };
   uint32_t n_gt = 0, n_eq = 0;
   for (int j0 = w0; j0 < w1; j0 += 32) {
     const int j = j0 + lane;
@@ -172,9 +197,25 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     }
     sh.cnt[32 + lane] = gi - g;  // exclusive prefixes
     sh.off[32 + lane] = ei - e;
+    if (lane == 31) {
+      sh.tot_gt = gi;
+      sh.tot_eq = ei;
+    }
   }
-  __syncthreads();
-  uint32_t gt_before = sh.cnt[32 + warp], eq_before = sh.off[32 + warp];
+  uint32_t base_gt = 0, base_eq = 0;
+  if constexpr (kSplit > 1) {
+    auto cl = cooperative_groups::this_cluster();
+    cl.sync();  // every CTA's totals are written
+    for (int q = 0; q < cr; ++q) {
+      const TopkShared* peer = cl.map_shared_rank(&sh, static_cast<unsigned>(q));
+      base_gt += peer->tot_gt;
+      base_eq += peer->tot_eq;
+    }
+    cl.sync();  // the totals are read: no CTA touches another's shared memory after this
+  } else {
+    __syncthreads();
+  }
+  uint32_t gt_before = base_gt + sh.cnt[32 + warp], eq_before = base_eq + sh.off[32 + warp];
   for (int j0 = w0; j0 < w1; j0 += 32) {
     const int j = j0 + lane;
     const uint32_t k = j < w1 ? key_at(j) : 0u;
@@ -185,7 +226,7 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     const bool kept = ((b_gt >> lane) & 1u) || (((b_eq >> lane) & 1u) && e < need);
     const uint32_t pos = g + (e < need ? e : need);
     // exactly K are kept; the bound is a guard
-    if (kept && pos < static_cast<uint32_t>(K)) dst[pos] = j;
+    if (kept && pos < static_cast<uint32_t>(K)) dst[pos] = lo + j;
     gt_before += __popc(b_gt);
     eq_before += __popc(b_eq);
   }
@@ -196,12 +237,37 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
 cudaError_t launch_topk(const float* scores, int T, int N, long long stride, const int32_t* lens, int K, int32_t* out,
                         cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  const int smem_keys = (N < kKeysInSmemMax ? N : kKeysInSmemMax);
-  const size_t smem = (static_cast<size_t>(kTopkWarps) * 256 + smem_keys) * sizeof(uint32_t);
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
-  topk_kernel<<<T, kTopkThreads, smem, stream>>>(scores, N, stride, lens, K, out);
-  return cudaGetLastError();
+  // a batch too small to fill the SMs splits each row between a pair of CTAs
+  const bool pair = 2ll * T <= sms;
+  const int split = pair ? 2 : 1;
+  const int row_keys = (N + split - 1) / split + 31;
+  const int smem_keys = row_keys < kKeysInSmemMax ? row_keys : kKeysInSmemMax;
+  const size_t smem = (static_cast<size_t>(kTopkWarps) * 256 + smem_keys) * sizeof(uint32_t);
+  if (!pair) {
+    e = cudaFuncSetAttribute(topk_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    topk_kernel<1><<<T, kTopkThreads, smem, stream>>>(scores, N, stride, lens, K, out);
+    return cudaGetLastError();
+  }
+  e = cudaFuncSetAttribute(topk_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * T));
+  cfg.blockDim = dim3(kTopkThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, topk_kernel<2>, scores, N, stride, lens, K, out);
 }
 
 }  // namespace svt

@@ -67,16 +67,31 @@ def test_topk_continuous_scores_span_chunks(S, dev):
 
 def test_topk_long_rows_and_strided_rows(S, dev):
     rng = np.random.default_rng(23)
-    # rows longer than the shared-memory key buffer are read from global memory
-    N, K = 60000, 2048
+    # rows whose half is longer than the shared-memory key buffer are read from global memory
+    N, K = 100000, 2048
     scores = W.bf16_bits_to_f32(W.f32_to_bf16_bits(rng.standard_normal((3, N), dtype=np.float32)))
-    lens = np.array([N, 50000, 40000], np.int32)
+    lens = np.array([N, 90000, 40000], np.int32)
     assert np.array_equal(gpu_topk(S, scores, K, dev, lens), oracle.topk_select(scores, K, lens=lens))
     # a [T, N] view of a wider buffer
     wide = torch.from_numpy(rng.standard_normal((4, 900)).astype(np.float32)).to(dev)
     view = wide[:, :700]
     got = S.topk_select(view, 100).cpu().numpy()
     assert np.array_equal(got, oracle.topk_select(view.cpu().numpy(), 100))
+
+
+def test_topk_many_rows_one_cta_each(S, dev):
+    # more rows than half the SMs: each row gets one CTA (smaller batches split a row between
+    # a pair of CTAs); tie-heavy rows, then rows longer than the shared-memory key buffer
+    rng = np.random.default_rng(26)
+    pool = np.array([0.0, -0.0, 1.0, -1.0, 2.5, np.inf, -np.inf, np.nan, 1e-30, -1e30], np.float32)
+    T, N, K = 100, 3000, 1000
+    scores = rng.choice(pool, size=(T, N)).astype(np.float32)
+    lens = rng.integers(0, N + 1, size=T).astype(np.int32)
+    assert np.array_equal(gpu_topk(S, scores, K, dev, lens), oracle.topk_select(scores, K, lens=lens))
+    T, N, K = 100, 50000, 2048
+    scores = rng.standard_normal((T, N)).astype(np.float32)
+    lens = rng.integers(K, N + 1, size=T).astype(np.int32)
+    assert np.array_equal(gpu_topk(S, scores, K, dev, lens), oracle.topk_select(scores, K, lens=lens))
 
 
 def test_topk_full_size_batch(S, dev):
