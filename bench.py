@@ -41,9 +41,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # streamk_merge_kernel), keyed by the hash of their sources it was measured on (stale -> null).
 TRAFFIC_BY_SOURCE = {
     # full-size capture (profiles/decode_bf16_attention_ncu.md, ncu --cache-control none after
-    # bench.py's own L2 flush): attention 167.23 MB read + 60.37 MB written, merge 1.08 MB read
-    # + 0.18 MB written
-    "ac0822ce2d408d04": (167.23 + 60.37 + 1.08 + 0.18) * 1e6,
+    # bench.py's own L2 flush): attention 168.58 MB read + 60.21 MB written, merge 1.00 MB read
+    # + 0.20 MB written
+    "b0623548097441fb": (168.58 + 60.21 + 1.00 + 0.20) * 1e6,
 }
 
 
