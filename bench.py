@@ -241,9 +241,9 @@ def replica_throughput(units_per_rank: int, ms_max: float, world: int) -> float:
 
 
 def source_hash() -> str:
-    """Hash of the sources of the two decode kernels the roofline line times together."""
+    """Hash of the sources of the decode kernels the roofline line times and of their launch plan."""
     h = hashlib.sha256()
-    for name in ("attention.cu", "merge.cu"):
+    for name in ("attention.cu", "merge.cu", "api.cu"):
         with open(os.path.join(ROOT, "sparse_mla_attention_top_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -126,13 +126,18 @@ SVT_API svt_status svt_resolve_topk_slots(const int32_t* topk_pos, int32_t T, in
  *            topk/topk_len are as for svt_resolve_topk_slots (slot resolution is fused here).
  *   out_bf16 [T, H, 512] bf16; lse [T, H] fp32 natural-log normaliser, or NULL.
  *            A query with no live entry gets out = 0 and lse = -inf.
- *   num_splits  0 = automatic (persistent CTAs share the whole batch's tiles evenly; a
- *            query whose list is split between CTAs is merged by a second kernel that the
- *            call enqueues right behind the attention kernel), 1 = one CTA per (query,
- *            64-head chunk), S > 1 = each query's list cut into S slices ("parallel tiled
- *            softmax", the explainer of arXiv 2511.11581, section 4.5), merged the same way.
- * Workspace: svt_sparse_mla_decode_workspace_size(T, H, K, num_splits) (depends on the
- * current device's SM count when num_splits == 0).
+ *   num_splits  1 = one CTA per (query, 64-head chunk). S > 1 = each query's list cut into
+ *            S slices ("parallel tiled softmax", the explainer of arXiv 2511.11581, section
+ *            4.5): for S = 2, 4 or 8 the slices' CTAs form a thread-block cluster and merge
+ *            in distributed shared memory at the end of the attention kernel; for other S
+ *            a second kernel, enqueued right behind it, merges them. 0 = automatic: whole
+ *            slices (8, 4, 2 or 1 per chunk, clustered) when they fill at least three
+ *            quarters of the SMs in one wave, else every SM takes an equal share of the
+ *            batch's 64-entry tiles (stream-K) and the second kernel merges the queries cut
+ *            between CTAs.
+ * Workspace: svt_sparse_mla_decode_workspace_size(T, H, K, num_splits): the 256-byte status
+ * header, plus the partial results when the second kernel merges (depends on the current
+ * device's SM count and cluster occupancy when num_splits == 0).
  */
 SVT_API size_t svt_sparse_mla_decode_workspace_size(int32_t T, int32_t H, int32_t K, int32_t num_splits);
 SVT_API svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const svt_kv_cache* kv,
@@ -150,8 +155,9 @@ SVT_API svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t 
  *
  * Same arguments and results as svt_sparse_mla_decode, without ws / ws_bytes. The scratch it
  * needs lives in an 8 MiB array inside the library that every GPU loading the library holds
- * until the process exits. That bounds it: one CTA per query (num_splits = 1) works for any
- * batch (256 bytes of scratch); a split decode works while
+ * until the process exits. That bounds it: one CTA per query (num_splits = 1) and slices
+ * merged inside a cluster (num_splits = 2, 4, 8) work for any batch (256 bytes of scratch); a
+ * decode whose slices a second kernel merges works while
  * svt_sparse_mla_decode_workspace_size(T, H, K, num_splits) <= 8 MiB (up to 63 CTAs with
  * partial results). Anything larger returns SVT_ERR_WORKSPACE before any work is enqueued.
  *   status_out  optional device int32: receives this call's device status bits (the

@@ -61,20 +61,36 @@ svt_status check_ws(void* ws, size_t ws_bytes, size_t need) {
 }
 
 // Decode launch shape: (number of CTAs, partial slots needed). The work unit is unit_rows
-// list entries: 64 (a half-tile) for the bf16 kernel, 128 (a tile) for the e4m3 kernel.
+// list entries (a 64-entry half-tile).
+//   num_splits 0: when whole slices of every row-set fill at least three quarters of the SMs
+//   in one wave, each row-set gets C = 8, 4 or 2 CTAs forming a thread-block cluster that
+//   merges its slices in distributed shared memory (or one CTA per row-set, nothing to
+//   merge); otherwise stream-K spreads all half-tiles evenly over one CTA per SM and a second
+//   kernel merges the row-sets cut between CTAs. The attention kernel is bound per SM (the
+//   gather -> S^T -> softmax -> PV chain of each half-tile), so whole slices cost little
+//   against the even split and save both the segment switches and the merge kernel.
+//   num_splits 2, 4 or 8 (at most the row-set's half-tiles): that many CTAs per row-set in a
+//   cluster, merged in the cluster; any other S: S CTAs per row-set, merged by the kernel.
 struct DecodePlan {
   int rowsets, hchunks, tiles_per_rowset;
   long long total_tiles;
   int num_ctas;
+  int cluster;
   bool partials;
 };
 
-DecodePlan plan_decode(int T, int H, int K, int num_splits, int unit_rows) {
+bool cluster_fits(int rowsets, int c, int kv_dtype) {
+  const int active = svt::attention_max_active_clusters(c, kv_dtype);
+  return active > 0 && rowsets <= active;
+}
+
+DecodePlan plan_decode(int T, int H, int K, int num_splits, int unit_rows, int kv_dtype) {
   DecodePlan d{};
   d.hchunks = (H + svt::kRowsetRows - 1) / svt::kRowsetRows;
   d.rowsets = T * d.hchunks;
   d.tiles_per_rowset = (K + unit_rows - 1) / unit_rows;
   d.total_tiles = static_cast<long long>(d.rowsets) * d.tiles_per_rowset;
+  d.cluster = 1;
   if (d.total_tiles == 0) {
     d.num_ctas = 0;
     d.partials = false;
@@ -82,19 +98,30 @@ DecodePlan plan_decode(int T, int H, int K, int num_splits, int unit_rows) {
   }
   long long n;
   if (num_splits == 0) {
-    n = sm_count();
-    if (n <= 0) n = 1;
+    int sms = sm_count();
+    if (sms <= 0) sms = 1;
+    n = sms;
+    const long long rs = d.rowsets;
+    for (int c = 8; c >= 1; c /= 2) {
+      if (c > d.tiles_per_rowset || rs * c > sms || 4 * rs * c < 3ll * sms) continue;
+      if (c > 1 && !cluster_fits(d.rowsets, c, kv_dtype)) continue;
+      n = rs * c;
+      d.cluster = c;
+      break;
+    }
   } else {
     const int s = num_splits > d.tiles_per_rowset ? d.tiles_per_rowset : num_splits;
     n = static_cast<long long>(d.rowsets) * s;
+    if (s == 2 || s == 4 || s == 8) d.cluster = s;
   }
   if (n > d.total_tiles) n = d.total_tiles;
   d.num_ctas = static_cast<int>(n);
-  d.partials = (d.total_tiles % n) != 0 || (d.total_tiles / n) % d.tiles_per_rowset != 0;
+  d.partials = d.cluster == 1 &&
+               ((d.total_tiles % n) != 0 || (d.total_tiles / n) % d.tiles_per_rowset != 0);
   return d;
 }
 
-// Workspace: status header | partial outputs | partial LSEs.
+// Workspace: status header | partial outputs | partial LSEs (stream-K and unclustered splits).
 size_t decode_part_o_bytes(const DecodePlan& d) {
   return round_up(2ull * d.num_ctas * svt::kRowsetRows * svt::kVdim * sizeof(uint16_t), 256);
 }
@@ -169,8 +196,9 @@ svt_status svt_resolve_topk_slots(const int32_t* topk_pos, int32_t T, int32_t K,
 size_t svt_sparse_mla_decode_workspace_size(int32_t T, int32_t H, int32_t K, int32_t num_splits) {
   if (T < 0 || H <= 0 || K < 0 || num_splits < 0) return svt::kStatusBytes;
   // the cache dtype is not an argument: enough for either kernel's plan
-  const size_t a = decode_ws_bytes(plan_decode(T, H, K, num_splits, decode_unit_rows(SVT_KV_BF16)));
-  const size_t b = decode_ws_bytes(plan_decode(T, H, K, num_splits, decode_unit_rows(SVT_KV_FP8_E4M3)));
+  const size_t a = decode_ws_bytes(plan_decode(T, H, K, num_splits, decode_unit_rows(SVT_KV_BF16), SVT_KV_BF16));
+  const size_t b =
+      decode_ws_bytes(plan_decode(T, H, K, num_splits, decode_unit_rows(SVT_KV_FP8_E4M3), SVT_KV_FP8_E4M3));
   return a > b ? a : b;
 }
 
@@ -189,7 +217,7 @@ svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const
   if (st != SVT_OK) return st;
   if (block_table != nullptr && (num_reqs <= 0 || max_blocks <= 0))
     return fail(SVT_ERR_INVALID_ARG, "num_reqs and max_blocks must be > 0 with a block table");
-  const DecodePlan d = plan_decode(T, H, K, num_splits, decode_unit_rows(kv->dtype));
+  const DecodePlan d = plan_decode(T, H, K, num_splits, decode_unit_rows(kv->dtype), kv->dtype);
   st = check_ws(ws, ws_bytes, decode_ws_bytes(d));
   if (st != SVT_OK) return st;
   if (T == 0) return SVT_OK;
@@ -225,6 +253,7 @@ svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const
   p.tiles_per_rowset = d.tiles_per_rowset;
   p.total_tiles = d.total_tiles;
   p.num_ctas = d.num_ctas;
+  p.cluster = d.cluster;
   p.status = static_cast<int*>(ws);
   if (d.partials) {
     char* base = static_cast<char*>(ws) + svt::kStatusBytes;
@@ -237,6 +266,7 @@ svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const
     p.tiles_per_rowset = 1;
     p.total_tiles = d.rowsets;
     p.num_ctas = d.rowsets;
+    p.cluster = 1;
   }
   cudaError_t e = svt::launch_attention(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
@@ -313,6 +343,7 @@ svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T, int32_t
   int sms = sm_count();
   if (sms <= 0) sms = 1;
   p.num_ctas = p.num_rowsets < sms ? p.num_rowsets : sms;
+  p.cluster = 1;
   p.status = static_cast<int*>(ws);
   cudaError_t e = svt::launch_attention(p, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");

@@ -22,10 +22,12 @@
 // PV(g) frees, so the serial chain S -> softmax -> PV of a single stage is broken; the M = 64
 // S^T costs the same cycles per MMA as M = 128, which is the price.
 //
-// Work: persistent CTAs walk segments (a row-set and a range of its half-tiles). Decode uses
+// Work: persistent CTAs walk segments (a row-set and a range of its half-tiles). Decode either
+// cuts each row-set into C whole slices, one per CTA of a thread-block cluster of C, merged
+// through distributed shared memory at the end of the kernel (cluster_merge), or uses
 // stream-K over (row-set, half-tile) so every SM gets the same number of half-tiles; a
-// row-set cut by a CTA boundary leaves, per part, its normalised rows in fp16 and an fp32
-// partial LSE, which the merge kernel (merge.cu) combines. Grouped prefill takes whole
+// row-set cut by a stream-K boundary leaves, per part, its normalised rows in fp16 and an
+// fp32 partial LSE, which the merge kernel (merge.cu) combines. Grouped prefill takes whole
 // row-sets round-robin.
 //
 // Warp roles (512 threads):
@@ -53,6 +55,7 @@
 //               also load each segment's Q^T.
 // Every wait is bounded (mbar_wait); the status word records range errors and timeouts.
 #include <climits>
+#include <mutex>
 
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -98,7 +101,14 @@ constexpr int kOffRed = kOffAlpha + kRowsetRows * 4;   // float[8][32]
 constexpr int kOffLfin = kOffRed + 8 * 32 * 4;         // float[64]
 constexpr int kOffBars = kOffLfin + kRowsetRows * 4;   // uint64[kNumBars]
 constexpr int kOffMisc = kOffBars + 32 * 8;            // tmem base, abort flag
-constexpr int kSmemUsed = kOffMisc + 16;
+// cluster merge (decode row-sets sliced between the CTAs of a cluster)
+constexpr int kMaxCluster = 8;
+constexpr int kOffMrgLse = kOffMisc + 16;                        // float[8][64]: each CTA's column LSEs
+constexpr int kOffMrgM = kOffMrgLse + kMaxCluster * kRowsetRows * 4;  // float[64]: this CTA's maxima
+constexpr int kOffMrgL = kOffMrgM + kRowsetRows * 4;               // float[64]: this CTA's column sums
+constexpr int kOffMrgF = kOffMrgL + kRowsetRows * 4;               // float[64]: this CTA's O^T weights
+constexpr int kOffMrgFlag = kOffMrgF + kRowsetRows * 4;            // int: O^T holds this CTA's sums
+constexpr int kSmemUsed = kOffMrgFlag + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory map exceeds 227 KB");
 
@@ -792,6 +802,20 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
       red[warp * 32 + 2 * idx + cp] = l;
     }
     named_bar_sync(kNamedBarSm, kSmThreads);
+    if (p.cluster > 1) {
+      // a slice of a clustered row-set: its column maxima and sums go to the cluster merge,
+      // which reads O^T from TMEM once every role of every CTA of the cluster is done
+      if (threadIdx.x < kRowsetRows) {
+        const int col = threadIdx.x, h = col >> 5, c = col & 31;
+        reinterpret_cast<float*>(smem + kOffMrgL)[col] =
+            (red[(4 * h + 0) * 32 + c] + red[(4 * h + 1) * 32 + c]) +
+            (red[(4 * h + 2) * 32 + c] + red[(4 * h + 3) * 32 + c]);
+        reinterpret_cast<float*>(smem + kOffMrgM)[col] = m_ref[col];
+        if (col == 0) *reinterpret_cast<int*>(smem + kOffMrgFlag) = nh > 0 ? 1 : 0;
+      }
+      named_bar_sync(kNamedBarSm, kSmThreads);
+      continue;
+    }
     if (threadIdx.x < kRowsetRows) {
       const int col = threadIdx.x, h = col >> 5, c = col & 31;
       const float l = (red[(4 * h + 0) * 32 + c] + red[(4 * h + 1) * 32 + c]) +
@@ -854,6 +878,107 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
   }
 }
 
+// ---------------------------------------------------------------------------------- cluster merge
+// Decode row-set r = blockIdx.x / C is cut into C slices, one per CTA of a cluster of C; each
+// CTA holds its slice's unnormalised O^T in TMEM with its column maxima m_k and sums l_k.
+// The split merge ("parallel tiled softmax", explainer of arXiv 2511.11581, section 4.5)
+// happens here, through distributed shared memory, once every role of every CTA is done:
+//   lse = log2 sum_k 2^(m_k + log2 l_k),   out = sum_k 2^(m_k - lse) O_k   (log2 units)
+// CTA j owns channels [512 j / C, 512 (j + 1) / C): every CTA sends its weighted O^T values of
+// those channels into CTA j's receive buffer (the freed stages), CTA j adds the C
+// contributions and writes its channels of the 64 rows. All 512 threads take part.
+__device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem) {
+  const int C = p.cluster;
+  const uint32_t rank = cluster_ctarank();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float* mrg_lse = reinterpret_cast<float*>(smem + kOffMrgLse);
+  const float* mrg_m = reinterpret_cast<const float*>(smem + kOffMrgM);
+  const float* mrg_l = reinterpret_cast<const float*>(smem + kOffMrgL);
+  float* mrg_f = reinterpret_cast<float*>(smem + kOffMrgF);
+  const bool had = *reinterpret_cast<const int*>(smem + kOffMrgFlag) != 0;
+  const RowsetRows rr = rowset_rows(p, static_cast<int>(blockIdx.x) / C);
+  // 1. this CTA's column LSEs into every CTA's table
+  if (tid < kRowsetRows) {
+    const float l = mrg_l[tid];
+    const float lse2 = l > 0.f ? mrg_m[tid] + __log2f(l) : -CUDART_INF_F;
+    const uint32_t a = smem_u32(mrg_lse + rank * kRowsetRows + tid);
+    for (int j = 0; j < C; ++j) st_cluster_f32(mapa_shared(a, static_cast<uint32_t>(j)), lse2);
+  }
+  cluster_sync_all();
+  // 2. the merged LSE and this CTA's weights
+  if (tid < kRowsetRows) {
+    float mx = -CUDART_INF_F;
+    for (int j = 0; j < C; ++j) mx = fmaxf(mx, mrg_lse[j * kRowsetRows + tid]);
+    float tot = -CUDART_INF_F;
+    if (mx != -CUDART_INF_F) {
+      float sum = 0.f;
+      for (int j = 0; j < C; ++j) {
+        const float lj = mrg_lse[j * kRowsetRows + tid];
+        if (lj != -CUDART_INF_F) sum += ex2_approx(lj - mx);
+      }
+      tot = mx + __log2f(sum);
+    }
+    mrg_f[tid] = (mrg_l[tid] > 0.f) ? ex2_approx(mrg_m[tid] - tot) : 0.f;
+    if (rank == 0 && p.lse != nullptr && tid < rr.nvalid) p.lse[rr.base + tid] = tot * 0.69314718055994530942f;
+  }
+  __syncthreads();
+  // 3. weighted O^T values to their channels' owners: receive buffer [C][64 rows][512 / C] fp32
+  //    over the stages. Warp w reads TMEM quadrant w % 4 (channels 128 mb + 32 (w % 4) + lane)
+  //    and query columns 16 (w / 4) .. + 15.
+  const int chunk = kVdim / C;
+  {
+    const int qd = warp & 3, cg = warp >> 2;
+    const uint32_t recv = smem_u32(smem + kOffStage);
+#pragma unroll 1
+    for (int mb = 0; mb < 4; ++mb) {
+      uint32_t o[16];
+      if (had) {
+        tmem_ld16(tmem + (static_cast<uint32_t>(32 * qd) << 16) + kTmemO + 64 * mb + 16 * cg, o);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) o[c] = 0u;
+      }
+      const int ch = 128 * mb + 32 * qd + lane;
+      const uint32_t owner = static_cast<uint32_t>(ch / chunk);
+      const int chl = ch - static_cast<int>(owner) * chunk;
+      const uint32_t base =
+          mapa_shared(recv + static_cast<uint32_t>(((static_cast<int>(rank) * kRowsetRows + 16 * cg) * chunk + chl) * 4),
+                      owner);
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        st_cluster_f32(base + static_cast<uint32_t>(c * chunk * 4), __uint_as_float(o[c]) * mrg_f[16 * cg + c]);
+    }
+  }
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  // 4. this CTA's channels of the 64 rows: the C contributions summed, as bf16
+  {
+    const float* recv = reinterpret_cast<const float*>(smem + kOffStage);
+    const int per_row = chunk / 8;
+    for (int item = tid; item < kRowsetRows * per_row; item += kThreads) {
+      const int q = item / per_row, c8 = item - q * per_row;
+      if (q >= rr.nvalid) continue;
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      for (int k = 0; k < C; ++k) {
+        const float4* v = reinterpret_cast<const float4*>(recv + (k * kRowsetRows + q) * chunk + 8 * c8);
+        const float4 a = v[0], b = v[1];
+        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+      }
+      uint4 w;
+      w.x = pack_bf16x2(acc[0], acc[1]);
+      w.y = pack_bf16x2(acc[2], acc[3]);
+      w.z = pack_bf16x2(acc[4], acc[5]);
+      w.w = pack_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(p.out + (rr.base + q) * kVdim + static_cast<int>(rank) * chunk + 8 * c8) = w;
+    }
+  }
+}
+
 template <bool kF16>
 __global__ void __launch_bounds__(kThreads, 1) tile_attention_kernel(const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -882,7 +1007,12 @@ __global__ void __launch_bounds__(kThreads, 1) tile_attention_kernel(const __gri
       mbar_init(bar(kBarSlotFree + e), kSlotFreeArrivals);
     }
     *abort_flag = 0;
+    *reinterpret_cast<int*>(smem + kOffMrgFlag) = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (threadIdx.x < kRowsetRows) {
+    reinterpret_cast<float*>(smem + kOffMrgL)[threadIdx.x] = 0.f;
+    reinterpret_cast<float*>(smem + kOffMrgM)[threadIdx.x] = -CUDART_INF_F;
   }
   if (warp == 0) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -910,6 +1040,12 @@ __global__ void __launch_bounds__(kThreads, 1) tile_attention_kernel(const __gri
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (p.cluster > 1) {
+    cluster_merge(p, smem, tmem);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+  }
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -918,11 +1054,65 @@ cudaError_t launch_tile_attention(const AttnParams& p, cudaStream_t stream) {
   cudaError_t e =
       cudaFuncSetAttribute(tile_attention_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
+  if (p.cluster > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.num_ctas));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tile_attention_kernel<kF16>, p);
+  }
   tile_attention_kernel<kF16><<<p.num_ctas, kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
+template <bool kF16>
+int max_active_clusters(int cluster) {
+  if (cudaFuncSetAttribute(tile_attention_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cluster));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, tile_attention_kernel<kF16>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
 }  // namespace
+
+int attention_max_active_clusters(int cluster, int kv_dtype) {
+  static std::mutex mu;
+  static int cache[64][2][4] = {};  // [device][dtype][log2(cluster) - 1], 0 = not asked yet
+  int dev = 0;
+  if (cluster < 2 || cluster > kMaxCluster || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  const int d = kv_dtype == SVT_KV_BF16 ? 0 : 1;
+  const int c = cluster == 2 ? 0 : (cluster == 4 ? 1 : 2);
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev][d][c] == 0) {
+    const int n = d == 0 ? max_active_clusters<false>(cluster) : max_active_clusters<true>(cluster);
+    cache[dev][d][c] = n > 0 ? n : -1;
+  }
+  return cache[dev][d][c] > 0 ? cache[dev][d][c] : 0;
+}
 
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
   if (p.num_ctas == 0) return cudaSuccess;

@@ -62,6 +62,8 @@ struct AttnParams {
   int tiles_per_rowset;  // stream-K: tiles of the longest list
   long long total_tiles;
   int num_ctas;
+  int cluster;       // decode: CTAs per row-set that merge their slices inside a thread-block
+                     // cluster through distributed shared memory (1 = no cluster merge)
   uint16_t* part_o;  // [2 * num_ctas, 64, 512] fp16 (stream-K partial segments, normalised)
   float* part_lse;  // [2 * num_ctas, 64]
   int* status;
@@ -124,6 +126,9 @@ cudaError_t launch_topk(const float* scores, int T, int N, long long stride, con
 // Decode and grouped prefill over either cache dtype (two shared-memory stages of 64-row
 // half-tiles; decode work units are half-tiles).
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
+// How many clusters of `cluster` attention CTAs (one per SM) the current device runs at once
+// (0 if the query fails); cached per device.
+int attention_max_active_clusters(int cluster, int kv_dtype);
 // Merges the partial results of the row-sets a stream-K decode split between CTAs; launched
 // right behind the attention kernel (programmatic dependent launch) and waiting for it.
 cudaError_t launch_streamk_merge(const AttnParams& p, cudaStream_t stream);

@@ -14,8 +14,8 @@
 namespace {
 
 // 8 MiB: the status header and partial results for up to 63 CTAs (2 slots x 64 rows x 512
-// fp16 + fp32 LSEs each). One CTA per query (num_splits = 1) needs
-// only the 256-byte header, whatever the batch.
+// fp16 + fp32 LSEs each). One CTA per query (num_splits = 1) and cluster-merged slices
+// (num_splits = 2, 4, 8) need only the 256-byte header, whatever the batch.
 constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

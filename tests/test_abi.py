@@ -140,10 +140,14 @@ def test_workspace_sizes(L):
     assert L.svt_sparse_mla_prefill_grouped_workspace_size(8192, 64, 2) >= 256
     # one CTA per query needs no partial buffers
     assert L.svt_sparse_mla_decode_workspace_size(64, 64, 2048, 1) == 256
-    # split lists need room for the partials: 2 slots per CTA of 64 rows x 512 fp16 + 64 fp32 lse
-    n_cta = 64 * 4
-    need = L.svt_sparse_mla_decode_workspace_size(64, 64, 2048, 4)
+    # lists split 3 ways are merged by a second kernel and need room for the partials: 2
+    # slots per CTA of 64 rows x 512 fp16 + 64 fp32 lse
+    n_cta = 64 * 3
+    need = L.svt_sparse_mla_decode_workspace_size(64, 64, 2048, 3)
     assert need >= 256 + 2 * n_cta * 64 * (512 * 2 + 4)
+    # 2, 4 or 8 slices per list merge inside a thread-block cluster: nothing beyond the header
+    for s in (2, 4, 8):
+        assert L.svt_sparse_mla_decode_workspace_size(64, 64, 2048, s) == 256
 
 
 def test_product_path_has_no_oracle_or_fallback():

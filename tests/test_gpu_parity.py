@@ -250,6 +250,45 @@ def test_decode_large_scores_rescale(S, dev, ws):
     compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
 
 
+# ------------------------------------------------------------------ cluster-merged slices
+
+@pytest.mark.parametrize("splits", [2, 4, 8])
+@pytest.mark.parametrize("H", [1, 33, 64, 100, 128])
+def test_decode_cluster_slices_match_oracle(S, dev, ws, splits, H):
+    # Each query's list cut into 2, 4 or 8 slices whose CTAs form a thread-block cluster and
+    # merge in distributed shared memory. K = 700 leaves a ragged last half-tile; the live
+    # counts leave whole slices with nothing (an empty query, a single entry, 65 entries).
+    w = W.make_decode(90 + H, T=5, H=H, K=700, ctx_lo=400, ctx_hi=3000, page_size=64)
+    lens = np.array([700, 0, 1, 65, 430], np.int32)
+    out, lse = gpu_decode(S, w, dev, ws, topk_len=lens, num_splits=splits)
+    ref, ref_lse, err = oracle_decode(w, topk_len=lens)
+    assert err == 0
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    assert torch.all(out[1] == 0) and torch.all(torch.isneginf(lse[1]))
+    assert ws.read_status() == 0
+
+
+def test_decode_fp8_cache_cluster_slices(S, dev, ws):
+    w = W.make_decode(97, T=6, H=64, K=520, ctx_lo=300, ctx_hi=5000, page_size=64, kv_dtype=W.KV_FP8_E4M3)
+    ref, ref_lse, err = oracle_decode(w)
+    assert err == 0
+    for splits in (2, 4, 8):
+        out, lse = gpu_decode(S, w, dev, ws, num_splits=splits)
+        compare(out, lse, ref, ref_lse, FP8_OUT_TOL)
+    assert ws.read_status() == 0
+
+
+def test_decode_cluster_slices_equal_unsplit(S, dev, ws):
+    # The same lists computed whole (one CTA per query) and in clustered slices agree within
+    # rounding, and the slices' merged LSE is the whole list's.
+    w = W.make_decode(98, T=4, H=64, K=1024, ctx_lo=2000, ctx_hi=6000, page_size=64)
+    out1, lse1 = gpu_decode(S, w, dev, ws, num_splits=1)
+    for splits in (2, 4, 8):
+        out, lse = gpu_decode(S, w, dev, ws, num_splits=splits)
+        assert float((out.float() - out1.float()).abs().max()) <= 1e-2
+        assert float((lse - lse1).abs().max()) <= 1e-4
+
+
 # ---------------------------------------------------------------------------------- merge
 
 def test_merge_splits_matches_oracle(S, dev):
@@ -324,7 +363,7 @@ def test_workspace_reuse_across_shapes_and_repeats(S, dev):
     ref_s, ref_lse_s, _ = oracle_decode(small)
     for w, ref, ref_lse in [(big, ref_b, ref_lse_b), (small, ref_s, ref_lse_s), (big, ref_b, ref_lse_b),
                             (small, ref_s, ref_lse_s)]:
-        for splits in (0, 3):
+        for splits in (0, 2, 3):
             out, lse = gpu_decode(S, w, dev, ws, num_splits=splits)
             compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
     assert ws.read_status() == 0
