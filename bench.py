@@ -41,9 +41,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # streamk_merge_kernel), keyed by the hash of their sources it was measured on (stale -> null).
 TRAFFIC_BY_SOURCE = {
     # full-size capture (profiles/decode_bf16_attention_ncu.md, ncu --cache-control none after
-    # bench.py's own L2 flush): attention 168.58 MB read + 60.21 MB written, merge 1.00 MB read
-    # + 0.20 MB written
-    "b0623548097441fb": (168.58 + 60.21 + 1.00 + 0.20) * 1e6,
+    # bench.py's own L2 flush): the cluster-merged attention kernel, 158.65 MB read + 61.00 MB
+    # written (no merge kernel on this plan)
+    "ac42cc583c934f36": (158.648832 + 60.999424) * 1e6,
 }
 
 
