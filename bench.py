@@ -302,6 +302,20 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def rowset_kept_counts(enc: np.ndarray, lens: np.ndarray, H: int) -> np.ndarray:
+    """Per 64-row half of each group, the union entries live for one of its members (the
+    attention kernel walks only those)."""
+    w = enc.view(np.uint32)
+    valid = (np.arange(w.shape[1])[None, :] < lens[:, None]) & (w != 0xFFFFFFFF)
+    m = w >> 24
+    out = []
+    for h in range(2):
+        lo, hi = h * 64 // H, (h * 64 + 63) // H
+        bits = ((2 << hi) - 1) & ~((1 << lo) - 1)
+        out.append(np.count_nonzero(valid & ((m & bits) != 0), axis=1))
+    return np.stack(out, axis=1).astype(np.int64).ravel()
+
+
 def time_steps(step, steps, flush, stream):
     import torch
 
@@ -455,12 +469,19 @@ def main():
         at = time_steps(attn_step, psteps, flush, stream)
         lens_h = lens.cpu().numpy().astype(np.int64)
         live = np.count_nonzero(pw.topk >= 0, axis=1)
-        executed = float(2 * 128 * lens_h.sum() * (576 + 512))
+        # Executed MMA flops: each 64-row half of a group walks the union entries live for one
+        # of its members, in 64-entry half-tiles (64 KV rows x 64 query rows x (576 + 512) MACs
+        # each, the last one padded). A 128-row tile over the whole union would execute
+        # `union` flops instead; useful flops count each query's own live entries.
+        kept = rowset_kept_counts(enc.cpu().numpy(), lens_h, pw.H)
+        executed = float(2 * 64 * 64 * ((kept + 63) // 64).sum() * (576 + 512))
+        union = float(2 * 128 * lens_h.sum() * (576 + 512))
         useful = float(2 * pw.H * live.sum() * (576 + 512))
         a_ms, u_ms = statistics.mean(at), statistics.mean(ut)
         prefill = {"workload": pw.name, "union_ms": round(u_ms, 4), "attention_ms": round(a_ms, 4),
                    "step_ms": round(u_ms + a_ms, 4),
                    "tflops_executed": executed / (a_ms / 1e3) / 1e12,
+                   "tflops_union": union / (a_ms / 1e3) / 1e12,
                    "tflops_useful": useful / (a_ms / 1e3) / 1e12,
                    "tflops_step_useful": useful / ((a_ms + u_ms) / 1e3) / 1e12,
                    "union_lists": float(lens_h.mean() / live.mean()),

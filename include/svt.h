@@ -204,8 +204,12 @@ SVT_API svt_status svt_build_group_union(const int32_t* slots, const int32_t* to
  *   enc/lens from svt_build_group_union with the same T, K, G.
  *   out_bf16 [T, H, 512] bf16; lse [T, H] fp32 or NULL. A query whose member bit is set on
  *            no entry gets out = 0 and lse = -inf.
- * The cache must hold fewer than 2^24 - 1 rows. Workspace:
- * svt_sparse_mla_prefill_grouped_workspace_size(T, H, G).
+ * Each half of a group's 128 rows (the members whose rows they are) walks only the union
+ * entries live for one of those members: a small integer kernel, enqueued first, counts them
+ * per half into the workspace. An entry whose slot is past the cache sets the range status
+ * bit and is dead. The cache must hold fewer than 2^24 - 1 rows. Workspace:
+ * svt_sparse_mla_prefill_grouped_workspace_size(T, H, G): the 256-byte status header and
+ * 8 bytes per group.
  */
 SVT_API size_t svt_sparse_mla_prefill_grouped_workspace_size(int32_t T, int32_t H, int32_t G);
 SVT_API svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T, int32_t H, int32_t G,

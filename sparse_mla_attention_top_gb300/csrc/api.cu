@@ -297,7 +297,12 @@ svt_status svt_build_group_union(const int32_t* slots, const int32_t* topk_len, 
   return SVT_OK;
 }
 
-size_t svt_sparse_mla_prefill_grouped_workspace_size(int32_t, int32_t, int32_t) { return svt::kStatusBytes; }
+size_t svt_sparse_mla_prefill_grouped_workspace_size(int32_t T, int32_t, int32_t G) {
+  // status header | per row-set kept-entry counts [2 * groups] int32
+  if (T <= 0 || G <= 0) return svt::kStatusBytes;
+  const size_t groups = (static_cast<size_t>(T) + G - 1) / G;
+  return svt::kStatusBytes + round_up(2 * groups * sizeof(int32_t), 256);
+}
 
 svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T, int32_t H, int32_t G,
                                           const svt_kv_cache* kv, const int32_t* enc, const int32_t* lens, int32_t K,
@@ -345,7 +350,12 @@ svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T, int32_t
   p.num_ctas = p.num_rowsets < sms ? p.num_rowsets : sms;
   p.cluster = 1;
   p.status = static_cast<int*>(ws);
-  cudaError_t e = svt::launch_attention(p, reinterpret_cast<cudaStream_t>(stream));
+  int* counts = reinterpret_cast<int*>(static_cast<char*>(ws) + svt::kStatusBytes);
+  p.counts = counts;
+  cudaError_t e = svt::launch_rowset_counts(enc, lens, groups, p.list_stride, H, num_slots, counts, p.status,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prefill row-set count launch");
+  e = svt::launch_attention(p, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
   return SVT_OK;
 }

@@ -11,7 +11,8 @@
 // Blackwell GPUs", The Investigation: slot = table[req, pos / P] * P + pos % P; The
 // Breakthrough: with no table the list already holds slots). Grouped prefill: a row-set is
 // half of a group's 128 packed rows and the list the group's union, each row seeing only the
-// entries whose membership bit is its query's (vLLM PR #63104, Overview).
+// entries whose membership bit is its query's (vLLM PR #63104, Overview); the row-set walks
+// only the union entries live for one of its members (the others are dead for all its rows).
 //
 // GB300 design. A half-tile is 64 list entries; per half-tile
 //   S^T[64 x 64]   = K_half[64 x 576] . Q^T     (M = 64: 36 MMAs of K = 16)
@@ -43,7 +44,9 @@
 //               ring of slot / mask tables, and each resolved row bulk-prefetched into L2 so
 //               that its fill waits for L2 rather than DRAM. A decode entry takes two
 //               dependent reads (the entry, then its page-table word); the entry read of the
-//               next half-tile is issued with the page read of the current one.
+//               next half-tile is issued with the page read of the current one. A prefill
+//               row-set's entries are the union entries live for its members, compacted in
+//               order from a window of 64 union entries loaded one window ahead.
 //   warps 12-15 fillers. bf16 cache: the moment PV frees a stage, cp.async the next
 //               half-tile's 64 rows into it (36 x 16 bytes per thread, dead rows zero-filled;
 //               Full completes as the copies land): copying straight into shared memory keeps
@@ -108,7 +111,8 @@ constexpr int kOffMrgM = kOffMrgLse + kMaxCluster * kRowsetRows * 4;  // float[6
 constexpr int kOffMrgL = kOffMrgM + kRowsetRows * 4;               // float[64]: this CTA's column sums
 constexpr int kOffMrgF = kOffMrgL + kRowsetRows * 4;               // float[64]: this CTA's O^T weights
 constexpr int kOffMrgFlag = kOffMrgF + kRowsetRows * 4;            // int: O^T holds this CTA's sums
-constexpr int kSmemUsed = kOffMrgFlag + 16;
+constexpr int kOffResX = kOffMrgFlag + 16;                          // int[4]: prefill resolvers' exchange
+constexpr int kSmemUsed = kOffResX + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory map exceeds 227 KB");
 
@@ -137,6 +141,7 @@ constexpr int kTmemS = 0;    // S^T buffer b: columns 64 b .. + 63 (lanes 0-15 o
 constexpr int kTmemO = 128;  // O^T M-block mb: columns 128 + 64 mb .. + 63
 
 constexpr int kNamedBarSm = 1;
+constexpr int kNamedBarRes = 2;  // the two resolver warps
 
 // operand type of both contractions: bf16 for a bf16 cache; f16 for an e4m3 cache, whose rows
 // become code x block scale in f16 on the way into shared memory (Q^T and P^T follow)
@@ -148,6 +153,15 @@ constexpr uint32_t kIdescPV = idesc_f32acc(128, 64, 1, 1, kF16 ? kFmtF16 : kFmtB
 constexpr int kDeadEntry = -2147483647 - 1;  // an entry past the list's live count
 
 __device__ __forceinline__ int halves_of(int len) { return (len + kHalf - 1) / kHalf; }
+
+// Prefill: the union entries row-set r keeps (live for one of its members, counted by the
+// row-set count kernel), at most the group's union length.
+__device__ __forceinline__ int prefill_kept(const AttnParams& p, int r) {
+  int ulen = __ldg(p.lens + (r >> 1));
+  ulen = ulen < 0 ? 0 : (ulen > p.list_stride ? p.list_stride : ulen);
+  const int c = __ldg(p.counts + r);
+  return c < 0 ? 0 : (c > ulen ? ulen : c);
+}
 
 // One stretch of a CTA's work: half-tiles i0 .. i0 + n - 1 of row-set r (only those with
 // live entries; a segment may have none and then only writes its epilogue).
@@ -182,8 +196,7 @@ struct SegWalk {
       const int len = p.topk_len ? p.topk_len[t] : p.K;
       return len < 0 ? 0 : (len > p.K ? p.K : len);
     }
-    const int len = p.lens[r >> 1];
-    return len < 0 ? 0 : (len > p.list_stride ? p.list_stride : len);
+    return prefill_kept(p, r);
   }
 
   // The next segment's row-set and half-tile range (te = one past its last half-tile); the
@@ -266,15 +279,14 @@ __device__ __forceinline__ float rows16_column_reduce(float (&v)[16], int lane, 
 }
 
 // ---------------------------------------------------------------------------------- resolvers
-// Half-tile k's 64 entries -> slot / mask ring entry k % 4 (waiting until the softmax and
-// the fillers are done with half-tile k - 4), then SlotsReady(k % 4).
+// Decode: half-tile k's 64 entries -> slot / mask ring entry k % 4 (waiting until the softmax
+// and the fillers are done with half-tile k - 4), then SlotsReady(k % 4).
 template <bool kF16>
 __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars, volatile int* abort_flag) {
   const int ltid = static_cast<int>(threadIdx.x) - kResWarp0 * 32;
   int* slot_tab = reinterpret_cast<int*>(smem + kOffSlot);
   uint32_t* mask_tab = reinterpret_cast<uint32_t*>(smem + kOffMask);
   auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
-  const bool decode = p.mode == kModeDecode;
   const bool has_table = p.block_table != nullptr;
   int err = 0;
   uint32_t k = 0;
@@ -286,27 +298,19 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
   while (live && walk.next_range(p, s, te)) {
     // first round of reads, all independent: the list length, the request id and the
     // segment's first entry (read speculatively below K, dropped below if past the length)
-    const int32_t* list;
-    int len_raw, req = 0, raw;
+    int req = 0;
     const int e0 = s.i0 * kHalf + ltid;
-    if (decode) {
-      const int t = s.r / p.hchunks;
-      list = p.topk + static_cast<long long>(t) * p.K;
-      len_raw = p.topk_len ? __ldg(p.topk_len + t) : p.K;
-      if (has_table) req = p.req_of_token ? __ldg(p.req_of_token + t) : t;
-      raw = e0 < p.K ? __ldg(list + e0) : kDeadEntry;
-    } else {
-      list = p.enc + static_cast<long long>(s.r >> 1) * p.list_stride;
-      len_raw = __ldg(p.lens + (s.r >> 1));
-      raw = e0 < p.list_stride ? __ldg(list + e0) : kDeadEntry;
-    }
-    const int cap = decode ? p.K : p.list_stride;
-    SegWalk::with_len(s, len_raw < 0 ? 0 : (len_raw > cap ? cap : len_raw), te);
+    const int t = s.r / p.hchunks;
+    const int32_t* list = p.topk + static_cast<long long>(t) * p.K;
+    const int len_raw = p.topk_len ? __ldg(p.topk_len + t) : p.K;
+    if (has_table) req = p.req_of_token ? __ldg(p.req_of_token + t) : t;
+    int raw = e0 < p.K ? __ldg(list + e0) : kDeadEntry;
+    SegWalk::with_len(s, len_raw < 0 ? 0 : (len_raw > p.K ? p.K : len_raw), te);
     if (s.n == 0) continue;
     if (e0 >= s.len) raw = kDeadEntry;
     // the request's block-table row and length (second round, with the page reads below)
     ReqContext rc{nullptr, INT_MAX, true};
-    if (decode && has_table) {
+    if (has_table) {
       rc.ok = req >= 0 && req < p.num_reqs;
       if (rc.ok) {
         rc.bt_row = p.block_table + static_cast<long long>(req) * p.max_blocks;
@@ -321,31 +325,17 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
       // the next half-tile's entry read goes out together with this one's page read
       const int raw_next = i + 1 < s.n ? entry(i + 1) : kDeadEntry;
       int slot = -1;
-      uint32_t mask = 0xFFFFFFFFu;
-      if (decode) {
-        if (raw != kDeadEntry) {
-          // the page word is read before the length check (in bounds of the table row
-          // either way), so that it travels with the request's length; slot_of drops it
-          // when a check fails
-          int phys = -1;
-          if (rc.bt_row != nullptr && raw >= 0) {
-            const int page = raw / p.page_size;
-            if (page < p.max_blocks) phys = __ldg(rc.bt_row + page);
-          }
-          slot = slot_of(raw, phys, rc, has_table, p.max_blocks, p.page_size, p.num_pages, &err);
+      const uint32_t mask = 0xFFFFFFFFu;
+      if (raw != kDeadEntry) {
+        // the page word is read before the length check (in bounds of the table row either
+        // way), so that it travels with the request's length; slot_of drops it when a check
+        // fails
+        int phys = -1;
+        if (rc.bt_row != nullptr && raw >= 0) {
+          const int page = raw / p.page_size;
+          if (page < p.max_blocks) phys = __ldg(rc.bt_row + page);
         }
-      } else {
-        mask = 0;
-        const uint32_t w = static_cast<uint32_t>(raw);
-        if (raw != kDeadEntry && w != 0xFFFFFFFFu) {
-          const int sl = static_cast<int>(w & 0xFFFFFFu);
-          if (static_cast<long long>(sl) < p.num_slots) {
-            slot = sl;
-            mask = w >> 24;
-          } else {
-            err = 1;
-          }
-        }
+        slot = slot_of(raw, phys, rc, has_table, p.max_blocks, p.page_size, p.num_pages, &err);
       }
       // the row is wanted a few half-tiles from now: start its trip from HBM into L2 here, so
       // that the fill, when its stage frees, waits for L2 rather than for DRAM
@@ -363,6 +353,102 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
     }
   }
   if (__any_sync(0xffffffffu, err) && (threadIdx.x & 31) == 0) atomicOr(p.status, SVT_DEV_ERR_INDEX_RANGE);
+}
+
+// Prefill: row-set r walks its group's union (ascending slots) and keeps, in order, the entries
+// whose membership mask has a bit of one of its members; every other entry is dead for all of
+// its rows. Half-tile k's ring entry gets the next 64 kept entries (the last one padded with
+// dead rows). The two resolver warps hold a window of 64 union entries, one per thread, with
+// each kept entry's rank among the window's kept entries (a ballot per warp and the two warp
+// counts); half-tiles take kept entries from the window by rank, and the next window's entries
+// are loaded one window ahead, so no load waits on the walk.
+__device__ __forceinline__ uint32_t rowset_member_bits(int rpar, int H) {
+  const int lo = rpar * kRowsetRows / H, hi = (rpar * kRowsetRows + kRowsetRows - 1) / H;
+  return ((2u << hi) - 1u) & ~((1u << lo) - 1u);
+}
+
+template <bool kF16>
+__device__ void resolver_prefill_role(const AttnParams& p, uint8_t* smem, uint32_t bars, volatile int* abort_flag) {
+  const int ltid = static_cast<int>(threadIdx.x) - kResWarp0 * 32;
+  const int rw = ltid >> 5, lane = ltid & 31;
+  int* slot_tab = reinterpret_cast<int*>(smem + kOffSlot);
+  uint32_t* mask_tab = reinterpret_cast<uint32_t*>(smem + kOffMask);
+  volatile int* xch = reinterpret_cast<volatile int*>(smem + kOffResX);  // [0..1] the warps' kept counts
+  auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
+  uint32_t k = 0;
+  SegWalk walk;
+  walk.init(p);
+  Seg s;
+  bool live = true;
+  int te;
+  while (live && walk.next_range(p, s, te)) {
+    const int g = s.r >> 1;
+    const int32_t* list = p.enc + static_cast<long long>(g) * p.list_stride;
+    int ulen = __ldg(p.lens + g);
+    ulen = ulen < 0 ? 0 : (ulen > p.list_stride ? p.list_stride : ulen);
+    SegWalk::with_len(s, prefill_kept(p, s.r), te);
+    if (s.n == 0) continue;
+    const uint32_t mbits = rowset_member_bits(s.r & 1, p.H);
+    auto load = [&](int base) -> uint32_t {
+      const int idx = base + ltid;
+      return idx < ulen ? static_cast<uint32_t>(__ldg(list + idx)) : 0xFFFFFFFFu;
+    };
+    // window state: this thread's entry, whether it is kept and its rank among the kept
+    // entries of the window; wtotal kept in the window, wused of them placed already
+    int base = 0;
+    uint32_t w = load(0), w_next = load(kResThreads);
+    int slot = -1, rank = 0, wtotal = 0, wused = 0;
+    auto open_window = [&]() {
+      slot = (w != 0xFFFFFFFFu && static_cast<long long>(w & 0xFFFFFFu) < p.num_slots && ((w >> 24) & mbits) != 0)
+                 ? static_cast<int>(w & 0xFFFFFFu)
+                 : -1;
+      const uint32_t kept = __ballot_sync(0xffffffffu, slot >= 0);
+      if (lane == 0) xch[rw] = __popc(kept);
+      named_bar_sync(kNamedBarRes, kResThreads);
+      const int c0 = xch[0];
+      wtotal = c0 + xch[1];
+      rank = (rw ? c0 : 0) + __popc(kept & ((1u << lane) - 1u));
+      wused = 0;
+      named_bar_sync(kNamedBarRes, kResThreads);  // the counts are rewritten by the next window
+    };
+    open_window();
+    for (int i = 0; i < s.n; ++i, ++k) {
+      const uint32_t e = k % kSlotRing;
+      // both warps stop together if the wait gives up (they share named barriers)
+      const bool freed =
+          k < kSlotRing || mbar_wait(bar(kBarSlotFree + e), ((k / kSlotRing) - 1) & 1u, p.status, abort_flag);
+      if (!named_bar_red_and(kNamedBarRes, kResThreads, freed)) {
+        live = false;
+        break;
+      }
+      int filled = 0;
+      while (filled < kHalf) {
+        if (wused == wtotal) {
+          // window used up: the next one (its entries are already on their way)
+          base += kResThreads;
+          if (base >= ulen) break;
+          w = w_next;
+          w_next = load(base + kResThreads);
+          open_window();
+          continue;
+        }
+        const int take = min(wtotal - wused, kHalf - filled);
+        if (slot >= 0 && rank >= wused && rank < wused + take) {
+          const int at = e * kHalf + filled + (rank - wused);
+          slot_tab[at] = slot;
+          mask_tab[at] = w >> 24;
+          prefetch_l2_bulk(p.kv + static_cast<long long>(slot) * p.row_stride, kF16 ? kRowBytesFp8 : kRowBytesBf16);
+        }
+        filled += take;
+        wused += take;
+      }
+      for (int j = filled + ltid; j < kHalf; j += kResThreads) {
+        slot_tab[e * kHalf + j] = -1;
+        mask_tab[e * kHalf + j] = 0u;
+      }
+      mbar_arrive(bar(kBarSlotsReady + e));
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------------- fillers
@@ -1026,7 +1112,10 @@ __global__ void __launch_bounds__(kThreads, 1) tile_attention_kernel(const __gri
   if (warp >= kFillWarp0) {
     filler_role<kF16>(p, smem, bars, abort_flag);
   } else if (warp >= kResWarp0) {
-    resolver_role<kF16>(p, smem, bars, abort_flag);
+    if (p.mode == kModeDecode)
+      resolver_role<kF16>(p, smem, bars, abort_flag);
+    else
+      resolver_prefill_role<kF16>(p, smem, bars, abort_flag);
   } else if (warp == kSIssuerWarp) {
     if ((threadIdx.x & 31) == 0) s_issuer_role<kF16>(p, smem, tmem, bars, abort_flag);
     __syncwarp();

@@ -50,6 +50,7 @@ struct AttnParams {
   const int* lens;
   int G;
   int list_stride;  // G * K
+  const int* counts;  // [2 * groups]: union entries each row-set keeps (live for one of its members)
   // softmax
   float scale_log2;  // softmax_scale * log2(e)
   // outputs
@@ -114,6 +115,11 @@ cudaError_t launch_resolve(const int32_t* topk, int T, int K, const int32_t* top
                            int page_size, long long num_pages, int32_t* slots, int* status, cudaStream_t stream);
 
 size_t union_smem_bytes(int G, int K);
+// Per row-set (half of a group's 128 packed rows) the number of union entries live for one of
+// its members: counts[2 g + half]. Entries whose slot is out of range are dead and set the
+// range error bit.
+cudaError_t launch_rowset_counts(const int32_t* enc, const int32_t* lens, int groups, int list_stride, int H,
+                                 long long num_slots, int* counts, int* status, cudaStream_t stream);
 cudaError_t launch_union(const int32_t* slots, const int32_t* topk_len, int T, int K, int G, long long num_slots,
                          int32_t* enc, int32_t* lens, int* status, cudaStream_t stream);
 

@@ -127,7 +127,60 @@ __global__ void union_kernel(const int32_t* __restrict__ slots, const int32_t* _
   for (int i = total + tid; i < n; i += nthreads) out[i] = -1;
 }
 
+// How many union entries each half of group g (64 packed rows: the members whose rows they
+// are) keeps, i.e. entries with a membership bit of one of those members. The attention
+// kernel walks only those, so the count fixes its number of 64-entry half-tiles.
+__global__ void __launch_bounds__(256) rowset_count_kernel(const int32_t* __restrict__ enc,
+                                                           const int32_t* __restrict__ lens, int list_stride, int H,
+                                                           long long num_slots, int* __restrict__ counts,
+                                                           int* status) {
+  __shared__ int red[2][8];
+  const int g = blockIdx.x;
+  int len = lens[g];
+  len = len < 0 ? 0 : (len > list_stride ? list_stride : len);
+  uint32_t bits[2];
+  for (int h = 0; h < 2; ++h) {
+    const int lo = h * 64 / H, hi = (h * 64 + 63) / H;
+    bits[h] = ((2u << hi) - 1u) & ~((1u << lo) - 1u);
+  }
+  const int32_t* row = enc + static_cast<long long>(g) * list_stride;
+  int c0 = 0, c1 = 0, err = 0;
+  for (int i = threadIdx.x; i < len; i += blockDim.x) {
+    const uint32_t w = static_cast<uint32_t>(row[i]);
+    if (w == 0xFFFFFFFFu) continue;
+    if (static_cast<long long>(w & 0xFFFFFFu) >= num_slots) {
+      err = 1;
+      continue;
+    }
+    const uint32_t m = w >> 24;
+    c0 += (m & bits[0]) != 0;
+    c1 += (m & bits[1]) != 0;
+  }
+  if (__any_sync(0xffffffffu, err) && (threadIdx.x & 31) == 0) atomicOr(status, SVT_DEV_ERR_INDEX_RANGE);
+  for (int off = 16; off > 0; off >>= 1) {
+    c0 += __shfl_xor_sync(0xffffffffu, c0, off);
+    c1 += __shfl_xor_sync(0xffffffffu, c1, off);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[0][threadIdx.x >> 5] = c0;
+    red[1][threadIdx.x >> 5] = c1;
+  }
+  __syncthreads();
+  if (threadIdx.x < 2) {
+    int t = 0;
+    for (int w = 0; w < (blockDim.x >> 5); ++w) t += red[threadIdx.x][w];
+    counts[2 * g + threadIdx.x] = t;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_rowset_counts(const int32_t* enc, const int32_t* lens, int groups, int list_stride, int H,
+                                 long long num_slots, int* counts, int* status, cudaStream_t stream) {
+  if (groups == 0) return cudaSuccess;
+  rowset_count_kernel<<<groups, 256, 0, stream>>>(enc, lens, list_stride, H, num_slots, counts, status);
+  return cudaGetLastError();
+}
 
 size_t union_smem_bytes(int G, int K) { return (static_cast<size_t>(next_pow2(G * K)) + 32) * sizeof(uint32_t); }
 

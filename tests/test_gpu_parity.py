@@ -331,6 +331,33 @@ def test_prefill_matches_oracle(S, dev, ws, H, G, T):
     assert ws.read_status() == 0
 
 
+@pytest.mark.parametrize("H,G", [(64, 2), (32, 4), (16, 8)])
+def test_prefill_row_sets_keep_only_their_members_entries(S, dev, ws, H, G):
+    # Each 64-row half of a group walks only the union entries live for one of its members.
+    # Odd tokens select nothing (a half may keep no entry at all), and tokens 4 apart share
+    # their lists, so some entries are live for several members and others for one.
+    w = W.make_prefill(110 + G, n_new=3 * G + 1, n_cached=700, H=H, G=G, K=200, page_size=16)
+    topk = w.topk.copy()
+    for t in range(w.T):
+        if t % 2 == 1:
+            topk[t] = -1
+        elif t >= 4:
+            topk[t] = topk[t - 4]
+    slots = S.resolve_topk_slots(to_dev(topk, dev), block_table=to_dev(w.block_table, dev),
+                                 seq_lens=to_dev(w.seq_lens, dev), req_of_token=to_dev(w.req_of_token, dev),
+                                 page_size=w.page_size, num_pages=w.num_pages, ws=ws)
+    enc, lens = S.build_group_union(slots, G, w.num_slots, ws=ws)
+    out, lse = S.sparse_mla_prefill_grouped(to_dev(w.q_bits, dev), G, kv_of(w, dev), enc, lens, w.K, w.scale, ws=ws)
+    ref_enc, ref_lens, _ = oracle.group_union(slots.cpu().numpy(), G, w.num_slots)
+    assert np.array_equal(enc.cpu().numpy(), ref_enc)
+    ref, ref_lse, err = oracle.prefill_grouped(w.q_bits, G, w.kv, w.kv_dtype, w.num_slots, ref_enc, ref_lens, w.K,
+                                               w.scale)
+    assert err == 0
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    assert torch.all(out[1::2] == 0) and torch.all(torch.isneginf(lse[1::2]))
+    assert ws.read_status() == 0
+
+
 def test_prefill_equals_per_query_decode_on_gpu(S, dev, ws):
     w = W.make_prefill(70, n_new=9, n_cached=300, H=64, G=2, K=200, page_size=64)
     _, _, _, out, lse = gpu_prefill(S, w, dev, ws)
