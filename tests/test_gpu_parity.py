@@ -358,6 +358,29 @@ def test_prefill_row_sets_keep_only_their_members_entries(S, dev, ws, H, G):
     assert ws.read_status() == 0
 
 
+@pytest.mark.parametrize("H,G,T", [(64, 2, 37), (32, 4, 41), (16, 8, 45)])
+def test_prefill_row_set_counts_bit_exact(S, dev, H, G, T):
+    # The count kernel's per-half kept entries (left in the workspace after the header) equal
+    # a plain recount from the oracle's union: entries with a membership bit of one of the
+    # members whose rows the half holds.
+    w = W.make_prefill(120 + G, n_new=T, n_cached=900, H=H, G=G, K=96, page_size=16)
+    ws = S.Workspace(dev)
+    slots, enc, lens, out, lse = gpu_prefill(S, w, dev, ws)
+    torch.cuda.synchronize()
+    ref_enc, ref_lens, _ = oracle.group_union(slots.cpu().numpy(), G, w.num_slots)
+    groups = ref_lens.shape[0]
+    got = ws.buf[256:256 + 8 * groups].cpu().view(torch.int32).numpy()
+    want = []
+    for g in range(groups):
+        masks = (ref_enc[g, :ref_lens[g]].astype(np.int64) & 0xFFFFFFFF) >> 24
+        for half in range(2):
+            members = {(half * 64 + r) // H for r in range(64)}
+            bits = sum(1 << m for m in members)
+            want.append(int(np.count_nonzero(masks & bits)))
+    assert np.array_equal(got, np.array(want, np.int32))
+    assert ws.read_status() == 0
+
+
 def test_prefill_equals_per_query_decode_on_gpu(S, dev, ws):
     w = W.make_prefill(70, n_new=9, n_cached=300, H=64, G=2, K=200, page_size=64)
     _, _, _, out, lse = gpu_prefill(S, w, dev, ws)
