@@ -41,9 +41,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # streamk_merge_kernel), keyed by the hash of their sources it was measured on (stale -> null).
 TRAFFIC_BY_SOURCE = {
     # full-size capture (profiles/decode_bf16_attention_ncu.md, ncu --cache-control none after
-    # bench.py's own L2 flush): the cluster-merged attention kernel, 158.65 MB read + 61.00 MB
-    # written (no merge kernel on this plan)
+    # bench.py's own L2 flush): the cluster-merged attention kernel (no merge kernel on this plan)
     "ac42cc583c934f36": (158.648832 + 60.999424) * 1e6,
+    # the same kernel after the prefill row-set compaction (decode path unchanged in effect)
+    "6a36a901a86fcc23": (159.517184 + 58.950400) * 1e6,
 }
 
 
