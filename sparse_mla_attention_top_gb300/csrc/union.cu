@@ -63,22 +63,64 @@ __global__ void union_kernel(const int32_t* __restrict__ slots, const int32_t* _
   if (__any_sync(0xffffffffu, err) && (tid & 31) == 0) atomicOr(status, SVT_DEV_ERR_INDEX_RANGE);
   __syncthreads();
 
-  // 2. bitonic sort, ascending; each thread takes pairs (i, i + j)
-  for (int k = 2; k <= npow; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const int lj = __ffs(j) - 1;
-      for (int p = tid; p < (npow >> 1); p += nthreads) {
-        const int i = ((p >> lj) << (lj + 1)) | (p & (j - 1));
-        const int ixj = i + j;
-        const uint32_t a = keys[i], b = keys[ixj];
-        const bool up = (i & k) == 0;
-        if ((a > b) == up) {
-          keys[i] = b;
-          keys[ixj] = a;
+  // 2. bitonic sort, ascending. Passes of stride j >= 64 pair (i, i + j) through shared
+  //    memory, one thread per pair; the passes of stride <= 32 of a merge stage stay inside
+  //    64-key blocks, which one warp sorts in registers (lane l holds keys l and l + 32 of the
+  //    block; stride 32 pairs them in the thread, smaller strides pair lanes by shuffle).
+  auto smem_pass = [&](int k, int j) {
+    const int lj = __ffs(j) - 1;
+    for (int p = tid; p < (npow >> 1); p += nthreads) {
+      const int i = ((p >> lj) << (lj + 1)) | (p & (j - 1));
+      const int ixj = i + j;
+      const uint32_t a = keys[i], b = keys[ixj];
+      const bool up = (i & k) == 0;
+      if ((a > b) == up) {
+        keys[i] = b;
+        keys[ixj] = a;
+      }
+    }
+    __syncthreads();
+  };
+  // merge stages k_lo .. k_hi (powers of two, k_hi <= 64 or k_lo == k_hi), strides j <= 32 of
+  // each, on every 64-key block held by this warp
+  auto warp_passes = [&](int k_lo, int k_hi, int jtop) {
+    const int lane = tid & 31;
+    for (int blk = tid >> 5; blk < (npow >> 6); blk += (nthreads >> 5)) {
+      const int base = blk << 6;
+      uint32_t x0 = keys[base + lane], x1 = keys[base + 32 + lane];
+      for (int k = k_lo; k <= k_hi; k <<= 1) {
+        for (int j = (k_lo == k_hi ? jtop : (k >> 1)); j > 0; j >>= 1) {
+          if (j == 32) {
+            const bool up = ((base + lane) & k) == 0;
+            if ((x0 > x1) == up) {
+              const uint32_t t = x0;
+              x0 = x1;
+              x1 = t;
+            }
+          } else {
+            const bool lower = (lane & j) == 0;
+            const uint32_t y0 = __shfl_xor_sync(0xffffffffu, x0, j);
+            const uint32_t y1 = __shfl_xor_sync(0xffffffffu, x1, j);
+            const bool up0 = ((base + lane) & k) == 0, up1 = ((base + 32 + lane) & k) == 0;
+            x0 = (lower == up0) ? min(x0, y0) : max(x0, y0);
+            x1 = (lower == up1) ? min(x1, y1) : max(x1, y1);
+          }
         }
       }
-      __syncthreads();
+      keys[base + lane] = x0;
+      keys[base + 32 + lane] = x1;
     }
+    __syncthreads();
+  };
+  if (npow >= 128) {
+    warp_passes(2, 64, 32);
+    for (int k = 128; k <= npow; k <<= 1) {
+      for (int j = k >> 1; j >= 64; j >>= 1) smem_pass(k, j);
+      warp_passes(k, k, 32);
+    }
+  } else {
+    for (int k = 2; k <= npow; k <<= 1)
+      for (int j = k >> 1; j > 0; j >>= 1) smem_pass(k, j);
   }
 
   // 3. run starts: a distinct slot begins where the slot part changes
