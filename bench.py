@@ -140,6 +140,10 @@ class ClockSampler:
             time.sleep(0.0002)
 
     def start(self):
+        # the timed loop holds the GIL between its CUDA calls: a short switch interval lets the
+        # sampling thread run every ~0.1 ms instead of once per 5 ms (longer than the region)
+        self._switch = sys.getswitchinterval()
+        sys.setswitchinterval(1e-4)
         if self._nvml_open():
             self.thread = threading.Thread(target=self._nvml_loop, daemon=True)
             self.thread.start()
@@ -159,6 +163,7 @@ class ClockSampler:
             self.lines.append(line.strip())
 
     def stop(self):
+        sys.setswitchinterval(getattr(self, "_switch", 0.005))
         if self.nvml is not None:
             self._stop.set()
             self.thread.join(timeout=2)
@@ -378,7 +383,6 @@ def main():
     clocks.start()
     times = time_steps(step, args.steps, flush, stream)
     barrier(world)
-    clk = clocks.stop()
     ms = max_over_ranks(statistics.mean(times), world)
     ms_med = max_over_ranks(statistics.median(times), world)
     nb = decode_bytes(w)
@@ -488,6 +492,12 @@ def main():
                    "union_lists": float(lens_h.mean() / live.mean()),
                    "frac_of_bf16_peak": executed / (a_ms / 1e3) / 1e12 / bf16_peak,
                    "peak_tflops": bf16_peak, "peak_source": peak_src}
+
+    # one clock record over every timed region above (decode, end to end, top-k, prefill) and
+    # the short warm-ups between them: a single region is too short for more than one NVML sample
+    clk = clocks.stop()
+    if clk is not None:
+        clk["window"] = "decode, e2e, top-k and prefill timed regions and the warm-ups between them"
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
