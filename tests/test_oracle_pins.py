@@ -453,6 +453,29 @@ def test_flipping_a_membership_bit_breaks_the_invariant(small_prefill):
     assert not np.allclose(lse, ref_lse, atol=1e-3)
 
 
+def test_dropping_the_tail_groups_output_fails_the_parity_check(small_prefill):
+    # Negative control for the parity harness (vLLM PR #63104, Tests: dropping the tail's
+    # output must fail): the oracle's own result, rounded as the GPU returns it, passes the
+    # comparison the GPU tests use; the same result with the short last group's rows zeroed
+    # (a kernel that skipped the tail) does not.
+    torch = pytest.importorskip("torch")
+    from tests._dev import BF16_OUT_TOL, compare
+
+    w = small_prefill
+    _, enc, lens = _union_of(w)
+    ref, ref_lse, err = oracle.prefill_grouped(w.q_bits, w.G, w.kv, w.kv_dtype, w.num_slots, enc, lens, w.K, w.scale)
+    assert err == 0
+    out = torch.from_numpy(ref).to(torch.bfloat16)
+    lse = torch.from_numpy(ref_lse.astype(np.float32))
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    tail = (w.T // w.G) * w.G  # 21 queries in groups of 4: query 20 is the tail group
+    dropped_out, dropped_lse = out.clone(), lse.clone()
+    dropped_out[tail:] = 0
+    dropped_lse[tail:] = -math.inf
+    with pytest.raises(AssertionError):
+        compare(dropped_out, dropped_lse, ref, ref_lse, BF16_OUT_TOL)
+
+
 def test_generators_hold_their_stated_shapes():
     w = W.make_prefill(14, n_new=40, n_cached=2100, H=2, G=2, K=64, page_size=64)
     live = [set(int(x) for x in row if x >= 0) for row in w.topk]
