@@ -268,6 +268,19 @@ def test_decode_cluster_slices_match_oracle(S, dev, ws, splits, H):
     assert ws.read_status() == 0
 
 
+@pytest.mark.parametrize("T,K", [(32, 1024), (64, 512), (120, 256), (100, 512)])
+def test_decode_automatic_plan_matches_oracle(S, dev, ws, T, K):
+    # The automatic plan over batch sizes that take each of its branches on a 152-SM GPU:
+    # 32 queries -> clusters of 4, 64 -> clusters of 2, 120 -> one CTA per query, 100 ->
+    # stream-K with the merge kernel. Every query is checked.
+    w = W.make_decode(130 + T, T=T, H=64, K=K, ctx_lo=K // 2, ctx_hi=3 * K, page_size=64)
+    out, lse = gpu_decode(S, w, dev, ws)
+    ref, ref_lse, err = oracle_decode(w)
+    assert err == 0
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    assert ws.read_status() == 0
+
+
 def test_decode_fp8_cache_cluster_slices(S, dev, ws):
     w = W.make_decode(97, T=6, H=64, K=520, ctx_lo=300, ctx_hi=5000, page_size=64, kv_dtype=W.KV_FP8_E4M3)
     ref, ref_lse, err = oracle_decode(w)
