@@ -4,20 +4,29 @@
 A step is one sparse-MLA decode of the bf16 decode batch: 64 requests x 64 heads, top-k
 2048 over contexts of 8K-32K tokens in a page_size-64 cache with shuffled pages (slot
 resolution, gather, both contractions, online softmax, epilogue and the split merge, all in
-the library's kernels). The headline is decode queries/s; gather GB/s and the roofline are
-reported beside it, and the grouped prefill (8192 new tokens, 64 heads, groups of 2) is
-measured after it as a second line item (union build + attention, TFLOP/s).
+the library's kernels). The headline is decode queries/s with its HBM roofline; every other
+workload is a line item of the same JSON line, timed the same way:
+  decode_fp8    128 requests x 64 heads, e4m3 cache, contexts 4K-46K
+  decode_mixed  128 requests x 16 heads, bf16, contexts 16K-46K
+  prefill       8192 new tokens, 64 heads, groups of 2 (union build + attention)
+  prefill_mixed 8192 new tokens on 24576 cached, 16 heads, groups of 8
+  prefill_fp8   the 8192-token prefill over an e4m3 cache
+  gather_probe  the bf16 batch's 131072 rows read with no arithmetic (the gather ceiling)
+  topk          top-k selection of 64 indexer rows of 8K-32K scores
+Decode items report HBM GB/s on algorithmic and on gathered bytes against the measured copy
+peak; prefill items report executed, union and useful TFLOP/s against the bf16 peak.
 
 Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events on the
 launching stream, with a 256 MB buffer written before every step (outside the events) so
 that L2 starts cold; barrier + synchronize on both sides; max over ranks.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl svt|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl svt|reference] [--phase-trace]
 """
 
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import os
@@ -37,14 +46,14 @@ UNIT = "queries/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 
-# dram__bytes_read.sum + dram__bytes_write.sum of one decode call (attention_kernel and
-# streamk_merge_kernel), keyed by the hash of their sources it was measured on (stale -> null).
+# dram__bytes_read.sum and dram__bytes_write.sum of one decode call of the bf16 batch (every
+# kernel of the call), keyed by the hash of the sources it was measured on (stale -> null),
+# with the flush the capture ran after.
 TRAFFIC_BY_SOURCE = {
-    # full-size capture (profiles/decode_bf16_attention_ncu.md, ncu --cache-control none after
-    # bench.py's own L2 flush): the cluster-merged attention kernel (no merge kernel on this plan)
-    "ac42cc583c934f36": (158.648832 + 60.999424) * 1e6,
-    # the same kernel after the prefill row-set compaction (decode path unchanged in effect)
-    "6a36a901a86fcc23": (159.517184 + 58.950400) * 1e6,
+    # earlier sources, flushed by a 256 MB write alone: the writes were the flush buffer's
+    # dirty lines evicted by the gather (the decode itself writes 4.2 MB of output)
+    "ac42cc583c934f36": (158.648832e6, 60.999424e6, "256 MB write"),
+    "6a36a901a86fcc23": (159.517184e6, 58.950400e6, "256 MB write"),
 }
 
 
@@ -58,8 +67,11 @@ def parse():
     ap.add_argument("--no-topk", action="store_true", help="skip the top-k selection line item")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-items", action="store_true", help="only the headline decode (with e2e and CPU legs)")
     ap.add_argument("--decode-T", type=int, default=64, help="decode batch size (64 = the benchmark workload)")
     ap.add_argument("--prefill-T", type=int, default=8192)
+    ap.add_argument("--phase-trace", action="store_true",
+                    help="build the phase-trace library and print per-phase times of the attention kernel")
     return ap.parse_args()
 
 
@@ -264,6 +276,16 @@ def decode_bytes(w) -> dict:
     return {"gathered": gathered, "algorithmic": gathered + other, "flops": flops, "live": live}
 
 
+L2_NOTE = "256 MB buffer written before each step, outside the events"
+
+
+def headline_config(w, world: int) -> dict:
+    """The headline workload's config: the same dict in both arms."""
+    return {"workload": w.name, "T": w.T, "H": w.H, "top_k": w.K, "page_size": w.page_size,
+            "kv_dtype": "bf16" if w.kv_dtype == 0 else "e4m3", "contexts": "uniform 8192..32768",
+            "l2": L2_NOTE, "parallelism": f"replicas x{world}"}
+
+
 def cpu_baseline(w, budget_s: float = 15.0):
     """The oracle as it stands, on the host cores, over a bounded sample of the queries."""
     import oracle
@@ -302,7 +324,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * w.T / value,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "T": w.T, "H": w.H, "top_k": w.K, "page_size": w.page_size},
+            "config": headline_config(w, args.gpus),
             "cpu_baseline": cb, "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                                         "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -322,12 +344,26 @@ def rowset_kept_counts(enc: np.ndarray, lens: np.ndarray, H: int) -> np.ndarray:
     return np.stack(out, axis=1).astype(np.int64).ravel()
 
 
+class Flusher:
+    """Leaves L2 cold between timed steps by writing a 256 MB buffer (twice the L2), as the
+    pages' benchmark does (vLLM PR #63104, bench_shardq_rank.py). The buffer's dirty lines
+    are written back while the next step runs: that step's DRAM write counter includes them."""
+
+    def __init__(self, dev):
+        import torch
+
+        self.wr = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.wr.zero_()
+
+
 def time_steps(step, steps, flush, stream):
     import torch
 
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     for s, e in evs:
-        flush.zero_()
+        flush()
         s.record(stream)
         step()
         e.record(stream)
@@ -335,10 +371,287 @@ def time_steps(step, steps, flush, stream):
     return [s.elapsed_time(e) for s, e in evs]
 
 
+def dev_inputs(S, w, dev):
+    import torch
+
+    return dict(kv=S.KVCache(torch.from_numpy(w.kv).to(dev), w.num_pages, w.page_size, w.kv_dtype),
+                q=torch.from_numpy(w.q_bits.view(np.int16)).to(dev).view(torch.bfloat16),
+                topk=torch.from_numpy(w.topk).to(dev), bt=torch.from_numpy(w.block_table).to(dev),
+                seq=torch.from_numpy(w.seq_lens).to(dev), req=torch.from_numpy(w.req_of_token).to(dev))
+
+
+def bench_decode(S, w, dev, stream, flush, steps, warmup, hbm_peak, ws=None):
+    """One decode workload resident in HBM: per-call time and its HBM roofline."""
+    import torch
+
+    d = dev_inputs(S, w, dev)
+    out = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
+    ws = S.Workspace(dev) if ws is None else ws
+
+    def step():
+        S.sparse_mla_decode(d["q"], d["kv"], d["topk"], w.scale, block_table=d["bt"], seq_lens=d["seq"], out=out,
+                            lse=lse, ws=ws)
+
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert ws.read_status() == 0, f"device status flagged an error during warm-up ({w.name})"
+    times = time_steps(step, steps, flush, stream)
+    assert ws.read_status() == 0, f"device status flagged an error ({w.name})"
+    nb = decode_bytes(w)
+    ms = statistics.mean(times)
+    ws_need = S.svt.lib().svt_sparse_mla_decode_workspace_size(w.T, w.H, w.K, 0)
+    return {"workload": w.name, "ms": ms, "ms_median": statistics.median(times), "queries_per_s": w.T / (ms / 1e3),
+            "algorithmic_bytes": nb["algorithmic"], "gathered_bytes": nb["gathered"],
+            "gbs_algorithmic": nb["algorithmic"] / (ms / 1e3) / 1e9, "gbs_gathered": nb["gathered"] / (ms / 1e3) / 1e9,
+            "frac_of_hbm_peak": nb["algorithmic"] / (ms / 1e3) / 1e9 / hbm_peak,
+            "frac_of_hbm_peak_gathered": nb["gathered"] / (ms / 1e3) / 1e9 / hbm_peak,
+            "tflops": nb["flops"] / (ms / 1e3) / 1e12,
+            "launches_per_call": 2 if ws_need > 256 else 1, "_times": times, "_d": d, "_out": out, "_lse": lse}
+
+
+def bench_prefill(S, pw, dev, stream, flush, steps, warmup, bf16_peak):
+    """One grouped-prefill workload: slot resolution + union build, then attention, timed apart."""
+    import torch
+
+    d = dev_inputs(S, pw, dev)
+    ws = S.Workspace(dev)
+    slots = torch.empty_like(d["topk"])
+    groups = (pw.T + pw.G - 1) // pw.G
+    enc = torch.empty((groups, pw.G * pw.K), dtype=torch.int32, device=dev)
+    lens = torch.empty((groups,), dtype=torch.int32, device=dev)
+    pout = torch.empty((pw.T, pw.H, 512), dtype=torch.bfloat16, device=dev)
+    plse = torch.empty((pw.T, pw.H), dtype=torch.float32, device=dev)
+
+    def union_step():
+        S.resolve_topk_slots(d["topk"], block_table=d["bt"], seq_lens=d["seq"], req_of_token=d["req"],
+                             page_size=pw.page_size, num_pages=pw.num_pages, out=slots, ws=ws)
+        S.build_group_union(slots, pw.G, pw.num_slots, enc=enc, lens=lens, ws=ws)
+
+    def attn_step():
+        S.sparse_mla_prefill_grouped(d["q"], pw.G, d["kv"], enc, lens, pw.K, pw.scale, out=pout, lse=plse, ws=ws)
+
+    for _ in range(max(3, warmup)):
+        union_step()
+        attn_step()
+    torch.cuda.synchronize()
+    assert ws.read_status() == 0, f"device status flagged an error ({pw.name})"
+    ut = time_steps(union_step, steps, flush, stream)
+    at = time_steps(attn_step, steps, flush, stream)
+    assert ws.read_status() == 0, f"device status flagged an error ({pw.name})"
+    lens_h = lens.cpu().numpy().astype(np.int64)
+    live = np.count_nonzero(pw.topk >= 0, axis=1)
+    # Executed MMA flops: each 64-row half of a group walks the union entries live for one of
+    # its members, in 64-entry half-tiles (64 KV rows x 64 query rows x (576 + 512) MACs
+    # each, the last one padded). A 128-row tile over the whole union would execute `union`
+    # flops instead; useful flops count each query's own live entries.
+    kept = rowset_kept_counts(enc.cpu().numpy(), lens_h, pw.H)
+    executed = float(2 * 64 * 64 * ((kept + 63) // 64).sum() * (576 + 512))
+    union = float(2 * 128 * lens_h.sum() * (576 + 512))
+    useful = float(2 * pw.H * live.sum() * (576 + 512))
+    a_ms, u_ms = statistics.mean(at), statistics.mean(ut)
+    return {"workload": pw.name, "kv_dtype": "bf16" if pw.kv_dtype == 0 else "e4m3",
+            "union_ms": round(u_ms, 4), "attention_ms": round(a_ms, 4), "step_ms": round(u_ms + a_ms, 4),
+            "tflops_executed": executed / (a_ms / 1e3) / 1e12,
+            "tflops_union": union / (a_ms / 1e3) / 1e12,
+            "tflops_useful": useful / (a_ms / 1e3) / 1e12,
+            "tflops_step_useful": useful / ((a_ms + u_ms) / 1e3) / 1e12,
+            "union_lists": float(lens_h.mean() / live.mean()),
+            "frac_of_bf16_peak": executed / (a_ms / 1e3) / 1e12 / bf16_peak,
+            "frac_of_bf16_peak_useful": useful / (a_ms / 1e3) / 1e12 / bf16_peak,
+            "peak_tflops": bf16_peak}
+
+
+def bench_probe(S, w, d, dev, stream, flush, steps, hbm_peak):
+    """The decode batch's rows read with no arithmetic, three ways, in the list's order and
+    sorted by slot: the gather's own ceiling next to the decode."""
+    import torch
+
+    ws = S.Workspace(dev)
+    slots = S.resolve_topk_slots(d["topk"], block_table=d["bt"], seq_lens=d["seq"], page_size=w.page_size,
+                                 num_pages=w.num_pages, ws=ws).view(-1)
+    slots = slots[slots >= 0].contiguous()
+    sorted_slots = torch.sort(slots).values.contiguous()
+    n = slots.numel()
+    out = torch.empty((n,), dtype=torch.int32, device=dev)
+    gathered = n * w.row_bytes
+    res = {"rows": n, "row_bytes": w.row_bytes, "gathered_bytes": gathered}
+    names = {0: "cp_async_16B", 1: "bulk_row", 2: "ld_16B_regs"}
+    for order, sl in (("list_order", slots), ("sorted", sorted_slots)):
+        for mode in (0, 1, 2):
+            def step(sl=sl, mode=mode):
+                S.gather_probe(d["kv"], sl, mode, out=out, ws=ws)
+
+            for _ in range(3):
+                step()
+            torch.cuda.synchronize()
+            t = time_steps(step, steps, flush, stream)
+            ms = statistics.median(t)
+            res[f"{names[mode]}_{order}"] = {"ms": ms, "gbs": gathered / (ms / 1e3) / 1e9,
+                                             "frac_of_hbm_peak": gathered / (ms / 1e3) / 1e9 / hbm_peak}
+    assert ws.read_status() == 0
+    return res
+
+
+def bench_topk(S, W, dev, stream, flush, steps, warmup, hbm_peak, T):
+    import torch
+
+    tw = W.topk_batch(T)
+    t_scores = torch.from_numpy(tw.scores).to(dev)
+    t_lens = torch.from_numpy(tw.lens).to(dev)
+    t_out = torch.empty((tw.T, tw.K), dtype=torch.int32, device=dev)
+
+    def topk_step():
+        S.topk_select(t_scores, tw.K, lens=t_lens, out=t_out)
+
+    for _ in range(max(3, warmup)):
+        topk_step()
+    torch.cuda.synchronize()
+    tt = time_steps(topk_step, steps, flush, stream)
+    t_ms = statistics.mean(tt)
+    t_bytes = float(tw.lens.astype(np.int64).sum() * 4 + tw.T * tw.K * 4)  # scores read once, lists written
+    return {"workload": tw.name, "ms": round(t_ms, 4), "queries_per_s": tw.T / (t_ms / 1e3),
+            "algorithmic_bytes": t_bytes, "gbs": t_bytes / (t_ms / 1e3) / 1e9,
+            "frac_of_hbm_peak": t_bytes / (t_ms / 1e3) / 1e9 / hbm_peak}
+
+
+def public(item: dict) -> dict:
+    return {k: v for k, v in item.items() if not k.startswith("_")}
+
+
+# ------------------------------------------------------------------------------ phase trace
+
+TRACE_HEAD, TRACE_G, TRACE_EV = 48, 48, 12
+
+
+def analyse_trace(tr: np.ndarray) -> dict:
+    """Per-phase times (µs) from the stamps of one traced launch ([CTAs, slots] uint64): see
+    the slot map in attention.cu. Medians over CTAs (and over half-tiles where per half-tile)."""
+    tr = tr.astype(np.int64)
+    ctas = tr[tr[:, 0] != 0]
+    if len(ctas) == 0:
+        return {"ctas": 0}
+    gt0, c0, gt1, c9 = ctas[:, 0], ctas[:, 1], ctas[:, 15], ctas[:, 9]
+    ghz = float(np.median((c9 - c0) / np.maximum(gt1 - gt0, 1)))
+    us = lambda cyc: float(cyc) / ghz / 1e3  # noqa: E731
+    n_half = ctas[:, 14]
+    ev = ctas[:, TRACE_HEAD:].reshape(len(ctas), TRACE_G, TRACE_EV)
+    out = {"ctas": int(len(ctas)), "sm_ghz": ghz, "half_tiles_per_cta_median": float(np.median(n_half)),
+           "launch_span_us": float(gt1.max() - gt0.min()) / 1e3,
+           "cta_start_spread_us": float(gt0.max() - gt0.min()) / 1e3,
+           "cta_span_us_median": float(np.median(gt1 - gt0)) / 1e3}
+    rel = lambda col: [us(x) for x in (col - c0)]  # noqa: E731
+    out["setup_us"] = float(np.median(rel(ctas[:, 2])))
+    out["first_q_issued_us"] = float(np.median(rel(ctas[:, 3])))
+    first_slots = ctas[:, 4]
+    ok = first_slots != 0
+    if np.any(ok):
+        out["first_slots_resolved_us"] = float(np.median([us(x) for x in (first_slots - c0)[ok]]))
+    has0 = ev[:, 0, 1] != 0
+    if np.any(has0):
+        out["first_rows_landed_us"] = float(np.median([us(x) for x in (ev[has0, 0, 1] - c0[has0])]))
+        out["first_s_issued_us"] = float(np.median([us(x) for x in (ev[has0, 0, 2] - c0[has0])]))
+        out["first_p_written_us"] = float(np.median([us(x) for x in (ev[has0, 0, 4] - c0[has0])]))
+    periods, fill_lat, s_lat, sm_lat, pv_gap, wait_rows, wait_buf = [], [], [], [], [], [], []
+    sm_ld, sm_bar, sm_exp, sm_arrive = [], [], [], []
+    for i in range(len(ctas)):
+        n = int(min(n_half[i], TRACE_G))
+        if n < 4:
+            continue
+        e = ev[i, :n]
+        periods.extend(np.diff(e[2:n - 1, 2]).tolist())
+        for g in range(2, n - 1):
+            fill_lat.append(e[g, 1] - e[g, 7])         # fill issued -> rows landed
+            s_lat.append(e[g, 3] - e[g, 2])            # S^T issued -> softmax sees it done
+            sm_lat.append(e[g, 4] - e[g, 3])           # softmax: S^T done -> P^T written
+            pv_gap.append(e[g, 5] - e[g, 4])           # P^T written -> PV issued
+            prev = max(e[g, 0], e[g - 1, 2])           # S issuer ready for g (buffer free, previous issued)
+            wait_rows.append(max(0, e[g, 1] - prev))   # ... then waited for the rows
+            wait_buf.append(max(0, e[g, 0] - e[g - 1, 2]))  # waited for the softmax to free the buffer
+            sm_ld.append(e[g, 8] - e[g, 3])            # softmax: S^T read from TMEM
+            sm_bar.append(e[g, 9] - e[g, 8])           # ... scaled, masked, maxima agreed (named barrier)
+            sm_exp.append(e[g, 10] - e[g, 9])          # ... exponentials, P^T stored
+            sm_arrive.append(e[g, 4] - e[g, 10])       # ... proxy fence and arrival
+    med = lambda v: float(np.median([us(x) for x in v])) if v else None  # noqa: E731
+    out.update({"half_tile_period_us": med(periods), "fill_issue_to_landed_us": med(fill_lat),
+                "s_issue_to_done_us": med(s_lat), "softmax_us": med(sm_lat), "p_to_pv_issue_us": med(pv_gap),
+                "s_issuer_wait_rows_us": med(wait_rows), "s_issuer_wait_buffer_us": med(wait_buf),
+                "softmax_tmem_load_us": med(sm_ld), "softmax_scale_max_us": med(sm_bar),
+                "softmax_exp_store_us": med(sm_exp), "softmax_fence_arrive_us": med(sm_arrive)})
+    last_p = []
+    for i in range(len(ctas)):
+        n = int(min(n_half[i], TRACE_G))
+        if n > 0 and n_half[i] <= TRACE_G:
+            last_p.append(ctas[i, 7] - ev[i, n - 1, 4])
+    out["last_p_to_roles_done_us"] = med(last_p)
+    out["epilogue_us"] = med((ctas[:, 6] - ctas[:, 5])[ctas[:, 6] != 0].tolist())
+    merged = ctas[:, 8] != 0
+    out["cluster_merge_us"] = med((ctas[merged, 8] - ctas[merged, 7]).tolist()) if np.any(merged) else None
+    out["roles_done_us"] = float(np.median(rel(ctas[:, 7])))
+    out["end_us"] = float(np.median(rel(ctas[:, 9])))
+    return out
+
+
+def run_phase_trace(args):
+    """Builds the phase-trace library, runs the bf16 decode batch, the e4m3 batch and the
+    grouped prefill once each (after warm-up and an L2 flush) and prints per-phase times."""
+    import torch
+
+    from sparse_mla_attention_top_gb300 import build as B
+    from sparse_mla_attention_top_gb300 import svt
+    from sparse_mla_attention_top_gb300 import workloads as W
+
+    svt.use_library(B.build(trace=True))
+    import sparse_mla_attention_top_gb300 as S
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush = Flusher(dev)
+    L = S.svt.lib()
+    L.svt_trace_attach.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+    slots_per_cta = L.svt_trace_slots()
+    assert slots_per_cta == TRACE_HEAD + TRACE_G * TRACE_EV
+    buf = torch.zeros((1024, slots_per_cta), dtype=torch.int64, device=dev)
+    res = {"trace": "phase stamps of one launch (clock64 per SM; medians over CTAs)"}
+
+    def traced(step, label):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        buf.zero_()
+        L.svt_trace_attach(ctypes.c_void_p(buf.data_ptr()), buf.numel() * 8)
+        flush()
+        step()
+        torch.cuda.synchronize()
+        L.svt_trace_attach(None, 0)
+        res[label] = analyse_trace(buf.cpu().numpy())
+
+    for name, w in (("decode_bf16", W.decode_bf16_batch(args.decode_T)), ("decode_fp8", W.decode_fp8_batch())):
+        d = dev_inputs(S, w, dev)
+        ws = S.Workspace(dev)
+        traced(lambda: S.sparse_mla_decode(d["q"], d["kv"], d["topk"], w.scale, block_table=d["bt"],
+                                           seq_lens=d["seq"], ws=ws), name)
+        del d
+    pw = W.grouped_prefill(args.prefill_T)
+    d = dev_inputs(S, pw, dev)
+    ws = S.Workspace(dev)
+    slots = S.resolve_topk_slots(d["topk"], block_table=d["bt"], seq_lens=d["seq"], req_of_token=d["req"],
+                                 page_size=pw.page_size, num_pages=pw.num_pages, ws=ws)
+    enc, lens = S.build_group_union(slots, pw.G, pw.num_slots, ws=ws)
+    traced(lambda: S.sparse_mla_prefill_grouped(d["q"], pw.G, d["kv"], enc, lens, pw.K, pw.scale, ws=ws),
+           "prefill_bf16")
+    print(json.dumps(res), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+        return
+    if args.phase_trace:
+        run_phase_trace(args)
         return
     import torch
 
@@ -353,57 +666,41 @@ def main():
     dev = torch.device("cuda", torch.cuda.current_device())
     stream = torch.cuda.current_stream()
     hbm_peak, bf16_peak, bf16_sust, peak_src = peaks()
+    flush = Flusher(dev)
 
-    # ---- decode batch, resident in HBM
+    # ---- headline: the bf16 decode batch, resident in HBM
     w = W.decode_bf16_batch(args.decode_T)
-    kv = S.KVCache(torch.from_numpy(w.kv).to(dev), w.num_pages, w.page_size, w.kv_dtype)
-    q = torch.from_numpy(w.q_bits.view(np.int16)).to(dev).view(torch.bfloat16)
-    topk = torch.from_numpy(w.topk).to(dev)
-    bt = torch.from_numpy(w.block_table).to(dev)
-    seq = torch.from_numpy(w.seq_lens).to(dev)
-    out = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((w.T, w.H), dtype=torch.float32, device=dev)
-    ws = S.Workspace(dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    # one attention kernel per decode call, plus the split merge when any query's list is split
-    # between CTAs (the workspace then holds partial results beyond the status header)
-    ws_need = S.svt.lib().svt_sparse_mla_decode_workspace_size(w.T, w.H, w.K, 0)
-    launches_per_step = 2 if ws_need > 256 else 1
-
-    def step():
-        S.sparse_mla_decode(q, kv, topk, w.scale, block_table=bt, seq_lens=seq, out=out, lse=lse, ws=ws)
-
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    assert ws.read_status() == 0, "device status flagged an error during warm-up"
     barrier(world)
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
-    times = time_steps(step, args.steps, flush, stream)
+    head = bench_decode(S, w, dev, stream, flush, args.steps, args.warmup, hbm_peak)
     barrier(world)
+    times = head["_times"]
     ms = max_over_ranks(statistics.mean(times), world)
     ms_med = max_over_ranks(statistics.median(times), world)
     nb = decode_bytes(w)
     value = replica_throughput(w.T, ms, world)
     achieved = nb["algorithmic"] / (ms / 1000.0) / 1e9
     th = source_hash()
+    d = head["_d"]
 
     # ---- end to end: host buffers in, results out, through the public API
     e2e = None
     if not args.no_e2e:
+        ws = S.Workspace(dev)
+        out, lse = head["_out"], head["_lse"]
         q_h = torch.from_numpy(w.q_bits.view(np.int16)).view(torch.bfloat16).pin_memory()
         topk_h = torch.from_numpy(w.topk).pin_memory()
         out_h = torch.empty((w.T, w.H, 512), dtype=torch.bfloat16).pin_memory()
         lse_h = torch.empty((w.T, w.H), dtype=torch.float32).pin_memory()
-        q_d, topk_d = torch.empty_like(q), torch.empty_like(topk)
+        q_d, topk_d = torch.empty_like(d["q"]), torch.empty_like(d["topk"])
 
         def e2e_step():
             q_d.copy_(q_h, non_blocking=True)
             topk_d.copy_(topk_h, non_blocking=True)
-            o, l = S.sparse_mla_decode(q_d, kv, topk_d, w.scale, block_table=bt, seq_lens=seq, out=out, lse=lse,
-                                       ws=ws)
+            o, l = S.sparse_mla_decode(q_d, d["kv"], topk_d, w.scale, block_table=d["bt"], seq_lens=d["seq"],
+                                       out=out, lse=lse, ws=ws)
             out_h.copy_(o, non_blocking=True)
             lse_h.copy_(l, non_blocking=True)
 
@@ -418,109 +715,59 @@ def main():
                "h2d_bytes_per_step": q_h.numel() * 2 + topk_h.numel() * 4,
                "d2h_bytes_per_step": out_h.numel() * 2 + lse_h.numel() * 4}
 
-    # ---- top-k selection line item (the indexer's last step, on the decode batch's contexts)
-    topk_item = None
+    # ---- the other workloads, each a line item timed the same way
+    items = {}
+    psteps = max(3, args.steps // 2)
+    if not args.no_items:
+        items["gather_probe"] = bench_probe(S, w, d, dev, stream, flush, psteps, hbm_peak)
+    del d, head["_d"]
+    if not args.no_items:
+        for key, fn in (("decode_fp8", W.decode_fp8_batch), ("decode_mixed", W.mixed_decode)):
+            it = bench_decode(S, fn(), dev, stream, flush, args.steps, args.warmup, hbm_peak)
+            items[key] = public(it)
+            del it
     if not args.no_topk:
-        tw = W.topk_batch(args.decode_T)
-        t_scores = torch.from_numpy(tw.scores).to(dev)
-        t_lens = torch.from_numpy(tw.lens).to(dev)
-        t_out = torch.empty((tw.T, tw.K), dtype=torch.int32, device=dev)
-
-        def topk_step():
-            S.topk_select(t_scores, tw.K, lens=t_lens, out=t_out)
-
-        for _ in range(max(3, args.warmup)):
-            topk_step()
-        torch.cuda.synchronize()
-        tt = time_steps(topk_step, max(3, args.steps // 2), flush, stream)
-        t_ms = statistics.mean(tt)
-        t_bytes = float(tw.lens.astype(np.int64).sum() * 4 + tw.T * tw.K * 4)  # scores read once, lists written
-        topk_item = {"workload": tw.name, "ms": round(t_ms, 4), "queries_per_s": tw.T / (t_ms / 1e3),
-                     "algorithmic_bytes": t_bytes, "gbs": t_bytes / (t_ms / 1e3) / 1e9,
-                     "frac_of_hbm_peak": t_bytes / (t_ms / 1e3) / 1e9 / hbm_peak}
-
-    # ---- grouped prefill line item (union + attention)
-    prefill = None
+        items["topk"] = bench_topk(S, W, dev, stream, flush, psteps, args.warmup, hbm_peak, args.decode_T)
     if not args.no_prefill:
-        pw = W.grouped_prefill(args.prefill_T)
-        pkv = S.KVCache(torch.from_numpy(pw.kv).to(dev), pw.num_pages, pw.page_size, pw.kv_dtype)
-        pq = torch.from_numpy(pw.q_bits.view(np.int16)).to(dev).view(torch.bfloat16)
-        ptopk = torch.from_numpy(pw.topk).to(dev)
-        pbt = torch.from_numpy(pw.block_table).to(dev)
-        pseq = torch.from_numpy(pw.seq_lens).to(dev)
-        preq = torch.from_numpy(pw.req_of_token).to(dev)
-        slots = torch.empty_like(ptopk)
-        groups = (pw.T + pw.G - 1) // pw.G
-        enc = torch.empty((groups, pw.G * pw.K), dtype=torch.int32, device=dev)
-        lens = torch.empty((groups,), dtype=torch.int32, device=dev)
-        pout = torch.empty((pw.T, pw.H, 512), dtype=torch.bfloat16, device=dev)
-        plse = torch.empty((pw.T, pw.H), dtype=torch.float32, device=dev)
+        items["prefill"] = bench_prefill(S, W.grouped_prefill(args.prefill_T), dev, stream, flush, psteps,
+                                         args.warmup, bf16_peak)
+        if not args.no_items:
+            items["prefill_mixed"] = bench_prefill(S, W.mixed_prefill(args.prefill_T), dev, stream, flush, psteps,
+                                                   args.warmup, bf16_peak)
+            items["prefill_fp8"] = bench_prefill(S, W.grouped_prefill_fp8(args.prefill_T), dev, stream, flush,
+                                                 psteps, args.warmup, bf16_peak)
 
-        def union_step():
-            S.resolve_topk_slots(ptopk, block_table=pbt, seq_lens=pseq, req_of_token=preq, page_size=pw.page_size,
-                                 num_pages=pw.num_pages, out=slots, ws=ws)
-            S.build_group_union(slots, pw.G, pw.num_slots, enc=enc, lens=lens, ws=ws)
-
-        def attn_step():
-            S.sparse_mla_prefill_grouped(pq, pw.G, pkv, enc, lens, pw.K, pw.scale, out=pout, lse=plse, ws=ws)
-
-        for _ in range(max(3, args.warmup)):
-            union_step()
-            attn_step()
-        torch.cuda.synchronize()
-        assert ws.read_status() == 0
-        psteps = max(3, args.steps // 2)
-        ut = time_steps(union_step, psteps, flush, stream)
-        at = time_steps(attn_step, psteps, flush, stream)
-        lens_h = lens.cpu().numpy().astype(np.int64)
-        live = np.count_nonzero(pw.topk >= 0, axis=1)
-        # Executed MMA flops: each 64-row half of a group walks the union entries live for one
-        # of its members, in 64-entry half-tiles (64 KV rows x 64 query rows x (576 + 512) MACs
-        # each, the last one padded). A 128-row tile over the whole union would execute
-        # `union` flops instead; useful flops count each query's own live entries.
-        kept = rowset_kept_counts(enc.cpu().numpy(), lens_h, pw.H)
-        executed = float(2 * 64 * 64 * ((kept + 63) // 64).sum() * (576 + 512))
-        union = float(2 * 128 * lens_h.sum() * (576 + 512))
-        useful = float(2 * pw.H * live.sum() * (576 + 512))
-        a_ms, u_ms = statistics.mean(at), statistics.mean(ut)
-        prefill = {"workload": pw.name, "union_ms": round(u_ms, 4), "attention_ms": round(a_ms, 4),
-                   "step_ms": round(u_ms + a_ms, 4),
-                   "tflops_executed": executed / (a_ms / 1e3) / 1e12,
-                   "tflops_union": union / (a_ms / 1e3) / 1e12,
-                   "tflops_useful": useful / (a_ms / 1e3) / 1e12,
-                   "tflops_step_useful": useful / ((a_ms + u_ms) / 1e3) / 1e12,
-                   "union_lists": float(lens_h.mean() / live.mean()),
-                   "frac_of_bf16_peak": executed / (a_ms / 1e3) / 1e12 / bf16_peak,
-                   "peak_tflops": bf16_peak, "peak_source": peak_src}
-
-    # one clock record over every timed region above (decode, end to end, top-k, prefill) and
-    # the short warm-ups between them: a single region is too short for more than one NVML sample
+    # one clock record over every timed region above and the short warm-ups between them: a
+    # single region is too short for more than one NVML sample
     clk = clocks.stop()
     if clk is not None:
-        clk["window"] = "decode, e2e, top-k and prefill timed regions and the warm-ups between them"
+        clk["window"] = "every timed region of this run and the warm-ups between them"
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w)
 
     if rank == 0:
+        tr = TRAFFIC_BY_SOURCE.get(th)
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_median": ms_med, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "T": w.T, "H": w.H, "top_k": w.K, "page_size": w.page_size,
-                       "kv_dtype": "bf16", "contexts": "uniform 8192..32768", "l2": "256 MB flush before each step",
-                       "parallelism": f"replicas x{world}"},
+            "config": headline_config(w, world),
             "gather_gbs": nb["gathered"] / (ms / 1000.0) / 1e9,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": TRAFFIC_BY_SOURCE.get(th),
+                         "frac": achieved / hbm_peak,
+                         "frac_gathered": nb["gathered"] / (ms / 1000.0) / 1e9 / hbm_peak,
+                         "traffic": (tr[0] + tr[1]) if tr else None,
+                         "traffic_read": tr[0] if tr else None, "traffic_write": tr[1] if tr else None,
+                         "traffic_flush": tr[2] if tr else None,
                          "kernel": ("tile_attention_kernel + streamk_merge_kernel (one decode call, timed together)"
-                                    if launches_per_step == 2 else "tile_attention_kernel (one decode call)"),
-                         "algorithmic_bytes": nb["algorithmic"], "peak_source": peak_src, "source_hash": th},
-            "clocks": clk, "gpu_launches": launches_per_step * args.steps, "e2e": e2e, "cpu_baseline": cpu,
-            "prefill": prefill,
-            "topk": topk_item,
+                                    if head["launches_per_call"] == 2 else "tile_attention_kernel (one decode call)"),
+                         "algorithmic_bytes": nb["algorithmic"], "gathered_bytes": nb["gathered"],
+                         "peak_source": peak_src, "source_hash": th},
+            "clocks": clk, "gpu_launches": head["launches_per_call"] * args.steps, "e2e": e2e, "cpu_baseline": cpu,
         }
+        line.update(items)
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -58,6 +58,9 @@ typedef enum {
 /* Bits of the device status word (ORed by kernels, read by svt_read_status). */
 #define SVT_DEV_ERR_INDEX_RANGE 0x1 /* a live index pointed outside its request or the cache  */
 #define SVT_DEV_ERR_TIMEOUT 0x2     /* a pipeline wait gave up; that call's outputs are junk  */
+#define SVT_DEV_ERR_FP8_RANGE 0x4   /* an e4m3-cache call met a value beyond the f16 range its
+                                       contractions run in (see svt_kv_cache); its outputs are
+                                       not reliable                                          */
 
 typedef enum { SVT_KV_BF16 = 0, SVT_KV_FP8_E4M3 = 1 } svt_kv_dtype;
 
@@ -68,6 +71,13 @@ typedef enum { SVT_KV_BF16 = 0, SVT_KV_FP8_E4M3 = 1 } svt_kv_dtype;
  *   SVT_KV_FP8_E4M3 : 512 e4m3 latent codes | 4 fp32 scales (channels 0-127, 128-255,
  *                     256-383, 384-511) | 64 bf16 rope = 656 bytes. The latent value of
  *                     channel d is e4m3(d) * scale[d / 128].
+ * With an e4m3 cache both contractions run on the tensor cores in f16 (fp32 accumulation):
+ * each latent value code * scale is rounded once to f16, the rope and q are converted from
+ * bf16 to f16, and P is rounded to f16. f16 holds magnitudes up to 65504, so the e4m3 path
+ * requires every block scale to be finite with 448 * |scale| <= 65504 (|scale| <= 146.2)
+ * and every q and rope value below 65536 in magnitude; a value outside that range sets
+ * SVT_DEV_ERR_FP8_RANGE. Tiny products lose precision in f16's subnormal range (below
+ * 6.1e-5). The bf16 cache path computes in bf16 and has no such limit.
  * row_stride_bytes = 0 means packed (1152 or 656); otherwise it must be >= that and a
  * multiple of 16. The bf16 layout is the pages' (vLLM PR #63104, bench script: 512 + 64
  * columns viewed as (-1, 64, 576)); the pages name an e4m3 cache ("The Assertion That
@@ -84,6 +94,20 @@ typedef struct {
 
 /* Human-readable reason for the last non-OK status returned on this thread. */
 SVT_API const char* svt_last_error_string(void);
+
+/*
+ * Failure-detection hook for tests; every ordinary caller leaves it at (0, 0). The pages'
+ * lesson ("The Assertion That Changed Everything": a failed device assertion took the whole
+ * server down) is that a device fault must be reported, not trapped; this hook lets a test
+ * make a pipeline wait run out on purpose and check that the kernel reports it and returns.
+ *   fault          0 = none; 1 = the attention kernels' gathering warps withhold the arrival
+ *                  that announces the first KV tile, so the first wait on it cannot complete.
+ *   wait_limit_ns  the time one pipeline wait may take before the kernel gives up, sets
+ *                  SVT_DEV_ERR_TIMEOUT and runs to its end (0 = the default, 2 seconds).
+ * Applies to the decode and grouped-prefill launches enqueued afterwards by any thread of
+ * the process. Returns SVT_ERR_INVALID_ARG for an unknown fault or a negative limit.
+ */
+SVT_API svt_status svt_debug_pipeline_fault(int32_t fault, int64_t wait_limit_ns);
 
 /* Zeroes a whole workspace (asynchronous, on `stream`). */
 SVT_API svt_status svt_workspace_init(void* ws, size_t ws_bytes, svt_stream_t stream);
@@ -129,7 +153,9 @@ SVT_API svt_status svt_resolve_topk_slots(const int32_t* topk_pos, int32_t T, in
  *   num_splits  1 = one CTA per (query, 64-head chunk). S > 1 = each query's list cut into
  *            S slices ("parallel tiled softmax", the explainer of arXiv 2511.11581, section
  *            4.5): for S = 2, 4 or 8 the slices' CTAs form a thread-block cluster and merge
- *            in distributed shared memory at the end of the attention kernel; for other S
+ *            in distributed shared memory at the end of the attention kernel (a list of
+ *            fewer than 64 * S entries gets the largest power of two of slices it can fill,
+ *            still merged in the cluster); for other S (at most one slice per 64 entries)
  *            a second kernel, enqueued right behind it, merges them. 0 = automatic: whole
  *            slices (8, 4, 2 or 1 per chunk, clustered) when they fill at least three
  *            quarters of the SMs in one wave, else every SM takes an equal share of the
@@ -157,16 +183,20 @@ SVT_API svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t 
  * needs lives in an 8 MiB array inside the library that every GPU loading the library holds
  * until the process exits. That bounds it: one CTA per query (num_splits = 1) and slices
  * merged inside a cluster (num_splits = 2, 4, 8) work for any batch (256 bytes of scratch); a
- * decode whose slices a second kernel merges works while
- * svt_sparse_mla_decode_workspace_size(T, H, K, num_splits) <= 8 MiB (up to 63 CTAs with
- * partial results). Anything larger returns SVT_ERR_WORKSPACE before any work is enqueued.
+ * decode whose slices a second kernel merges (other num_splits, and num_splits = 0 when the
+ * automatic plan picks stream-K, as it does for a few queries with long lists, e.g. 4
+ * queries of 64 heads and top-k 2048) works while its workspace would be at most 8 MiB (up
+ * to 63 CTAs with partial results). A larger one returns SVT_ERR_WORKSPACE. Like every
+ * failed check, that happens before anything is enqueued.
  *   status_out  optional device int32: receives this call's device status bits (the
  *               SVT_DEV_ERR_* values) when the call's kernels have run; NULL to skip.
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress)
- * with that device current; make that first call before any stream capture. Every call shares
- * the one array: the call clears its status word first, so calls that follow one
- * another on a stream are independent, but calls that overlap on the GPU (other streams or
- * threads) race on it. It calls no cudaMalloc, cudaFree or other allocating routine.
+ * with that device current and keeps it for the life of the process; make that first call
+ * before any stream capture, and do not use this entry point after a cudaDeviceReset (the
+ * kept address would belong to the old context). Every call shares the one array: once its
+ * checks pass, a call clears the status word first, so calls that follow one another on a
+ * stream are independent, but calls that overlap on the GPU (other streams or threads) race
+ * on it. It calls no cudaMalloc, cudaFree or other allocating routine.
  */
 SVT_API svt_status svt_sparse_mla_decode_noalloc(const void* q_bf16, int32_t T, int32_t H, const svt_kv_cache* kv,
                                                  const int32_t* block_table, int32_t num_reqs, int32_t max_blocks,
@@ -244,6 +274,25 @@ SVT_API svt_status svt_merge_splits(const float* o_part, const float* lse_part, 
  */
 SVT_API svt_status svt_topk_select(const float* scores, int32_t T, int32_t N, int64_t stride, const int32_t* lens,
                                    int32_t K, int32_t* topk_out, svt_stream_t stream);
+
+/*
+ * Gather probe, a measurement tool rather than a step of the method: reads the cache rows of
+ * a slot list exactly as the decode's row gather does, with no attention arithmetic, so that
+ * the gather's own ceiling on this GPU can be measured next to the decode (the pages measure
+ * their kernels with CUDA events after an L2 flush, vLLM PR #63104, bench_shardq_rank.py;
+ * the row gather is "The Virtual Block Table", The Breakthrough: one cache row per selected
+ * token).
+ *   kv       the cache (either dtype); rows are read whole (1152 or 656 bytes).
+ *   slots    [n] int32 cache slots; a negative or out-of-range slot is skipped (its result 0).
+ *   mode     0 = 16-byte cp.async copies from all threads into shared memory (the decode's
+ *            bf16 fill); 1 = one bulk copy per row into shared memory; 2 = 16-byte loads
+ *            into registers.
+ *   row_xor  [n] uint32: the XOR of each row's 32-bit words (0 for a skipped slot).
+ * Workspace: the 256-byte status header (a copy that does not land within 2 s sets
+ * SVT_DEV_ERR_TIMEOUT).
+ */
+SVT_API svt_status svt_gather_probe(const svt_kv_cache* kv, const int32_t* slots, int64_t n, int32_t mode,
+                                    uint32_t* row_xor, void* ws, size_t ws_bytes, svt_stream_t stream);
 
 #ifdef __cplusplus
 }

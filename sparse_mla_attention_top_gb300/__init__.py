@@ -13,6 +13,8 @@ from .svt import (  # noqa: F401
     SvtError,
     Workspace,
     build_group_union,
+    debug_pipeline_fault,
+    gather_probe,
     merge_splits,
     resolve_topk_slots,
     sparse_mla_decode,

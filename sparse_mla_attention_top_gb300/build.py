@@ -14,7 +14,11 @@ CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 LIB = PKG / "libsvt.so"
 BUILD_DIR = PKG / "_build"
-SOURCES = ["api.cu", "attention.cu", "resolve.cu", "union.cu", "merge.cu", "noalloc.cu", "topk.cu"]
+# The phase-trace build: the same sources with SVT_PHASE_TRACE defined (clock stamps at each
+# pipeline step of the attention kernel); a separate library that only profiling loads.
+TRACE_LIB = PKG / "libsvt_trace.so"
+TRACE_BUILD_DIR = PKG / "_build_trace"
+SOURCES = ["api.cu", "attention.cu", "resolve.cu", "union.cu", "merge.cu", "noalloc.cu", "topk.cu", "probe.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden", f"-I{INCLUDE}", f"-I{CSRC}"]
 
@@ -30,24 +34,28 @@ def _inputs():
     return [CSRC / s for s in SOURCES] + list(CSRC.glob("*.cuh")) + list(CSRC.glob("*.h")) + [INCLUDE / "svt.h"]
 
 
-def up_to_date() -> bool:
-    if not LIB.exists():
+def up_to_date(lib: Path = LIB) -> bool:
+    if not lib.exists():
         return False
-    t = LIB.stat().st_mtime
+    t = lib.stat().st_mtime
     return all(p.stat().st_mtime <= t for p in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False) -> Path:
-    if not force and up_to_date():
-        return LIB
-    BUILD_DIR.mkdir(exist_ok=True)
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> Path:
+    """Builds libsvt.so (or, with trace=True, the phase-trace library) and returns its path."""
+    lib = TRACE_LIB if trace else LIB
+    build_dir = TRACE_BUILD_DIR if trace else BUILD_DIR
+    flags = NVCC_FLAGS + (["-DSVT_PHASE_TRACE"] if trace else [])
+    if not force and up_to_date(lib):
+        return lib
+    build_dir.mkdir(exist_ok=True)
     nvcc = _nvcc()
     procs = []
     objs = []
     for src in SOURCES:
-        obj = BUILD_DIR / (Path(src).stem + ".o")
+        obj = build_dir / (Path(src).stem + ".o")
         objs.append(obj)
-        cmd = [nvcc, *NVCC_FLAGS, "-c", str(CSRC / src), "-o", str(obj)]
+        cmd = [nvcc, *flags, "-c", str(CSRC / src), "-o", str(obj)]
         if verbose:
             print(" ".join(cmd), flush=True)
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)))
@@ -60,13 +68,13 @@ def build(force: bool = False, verbose: bool = False) -> Path:
             print(out)
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
-    tmp = LIB.with_suffix(f".so.tmp{os.getpid()}")
+    tmp = lib.with_suffix(f".so.tmp{os.getpid()}")
     cmd = [nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", str(tmp), *map(str, objs)]
     r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + r.stdout)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -1,10 +1,15 @@
 // The C ABI of libsvt.so: argument checks, workspace sizing, launch configuration and
 // status readback. Every check happens before anything is enqueued; nothing here allocates
 // device memory or synchronises a stream (except svt_read_status).
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
 
 #include "internal.h"
 
@@ -69,8 +74,10 @@ svt_status check_ws(void* ws, size_t ws_bytes, size_t need) {
 //   kernel merges the row-sets cut between CTAs. The attention kernel is bound per SM (the
 //   gather -> S^T -> softmax -> PV chain of each half-tile), so whole slices cost little
 //   against the even split and save both the segment switches and the merge kernel.
-//   num_splits 2, 4 or 8 (at most the row-set's half-tiles): that many CTAs per row-set in a
-//   cluster, merged in the cluster; any other S: S CTAs per row-set, merged by the kernel.
+//   num_splits 2, 4 or 8: that many CTAs per row-set in a cluster, merged in the cluster (cut
+//   to the largest power of two that does not exceed the row-set's half-tiles, so a short
+//   list stays on the cluster merge); any other S: S CTAs per row-set (at most its
+//   half-tiles), merged by the second kernel.
 struct DecodePlan {
   int rowsets, hchunks, tiles_per_rowset;
   long long total_tiles;
@@ -110,7 +117,11 @@ DecodePlan plan_decode(int T, int H, int K, int num_splits, int unit_rows, int k
       break;
     }
   } else {
-    const int s = num_splits > d.tiles_per_rowset ? d.tiles_per_rowset : num_splits;
+    int s = num_splits > d.tiles_per_rowset ? d.tiles_per_rowset : num_splits;
+    if (num_splits == 2 || num_splits == 4 || num_splits == 8) {
+      // a list too short for that many slices keeps the cluster merge with fewer of them
+      while (s & (s - 1)) s &= s - 1;
+    }
     n = static_cast<long long>(d.rowsets) * s;
     if (s == 2 || s == 4 || s == 8) d.cluster = s;
   }
@@ -139,6 +150,50 @@ int decode_unit_rows(svt_kv_dtype) { return svt::kTileRows / 2; }
 }  // namespace
 
 namespace svt {
+namespace {
+std::atomic<int> g_debug_fault{0};
+std::atomic<unsigned long long> g_debug_wait_limit_ns{0};
+}  // namespace
+
+#ifdef SVT_PHASE_TRACE
+std::atomic<unsigned long long*> g_trace_buf{nullptr};
+std::atomic<size_t> g_trace_bytes{0};
+// The trace buffer for a launch of num_ctas CTAs, or null when none is attached or it is too small.
+unsigned long long* trace_for(int num_ctas) {
+  const size_t need = static_cast<size_t>(num_ctas) * kTraceSlots * sizeof(unsigned long long);
+  return g_trace_bytes.load() >= need ? g_trace_buf.load() : nullptr;
+}
+#endif
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;
+std::once_flag g_encode_once;
+}  // namespace
+
+bool encode_q_map(AttnParams& p, long long rows) {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult res = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &res) ==
+            cudaSuccess &&
+        res == cudaDriverEntryPointSuccess)
+      g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (g_encode_tiled == nullptr || rows <= 0 || rows >= (1ll << 31)) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kRow), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kRow) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kRowsetRows)};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  return g_encode_tiled(&p.q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(p.q), dims, strides, box,
+                        elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+void debug_fault_state(int* fault, unsigned long long* wait_limit_ns) {
+  *fault = g_debug_fault.load(std::memory_order_relaxed);
+  *wait_limit_ns = g_debug_wait_limit_ns.load(std::memory_order_relaxed);
+}
+
 svt_status set_last_error(svt_status st, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -151,6 +206,27 @@ svt_status set_last_error(svt_status st, const char* fmt, ...) {
 extern "C" {
 
 const char* svt_last_error_string(void) { return g_err; }
+
+#ifdef SVT_PHASE_TRACE
+// Trace build only (not declared in svt.h): attention launches enqueued afterwards write their
+// phase stamps into `buf` (device memory of `bytes` bytes; null detaches) when it holds
+// kTraceSlots 64-bit words for each of their CTAs.
+SVT_API svt_status svt_trace_attach(void* buf, size_t bytes) {
+  svt::g_trace_buf.store(static_cast<unsigned long long*>(buf));
+  svt::g_trace_bytes.store(buf == nullptr ? 0 : bytes);
+  return SVT_OK;
+}
+SVT_API int32_t svt_trace_slots(void) { return svt::kTraceSlots; }
+#endif
+
+svt_status svt_debug_pipeline_fault(int32_t fault, int64_t wait_limit_ns) {
+  if (fault != 0 && fault != svt::kFaultWithholdFirstFill)
+    return fail(SVT_ERR_INVALID_ARG, "unknown fault %d", static_cast<int>(fault));
+  if (wait_limit_ns < 0) return fail(SVT_ERR_INVALID_ARG, "wait_limit_ns must be >= 0");
+  svt::g_debug_fault.store(fault, std::memory_order_relaxed);
+  svt::g_debug_wait_limit_ns.store(static_cast<unsigned long long>(wait_limit_ns), std::memory_order_relaxed);
+  return SVT_OK;
+}
 
 svt_status svt_workspace_init(void* ws, size_t ws_bytes, svt_stream_t stream) {
   svt_status st = check_ws(ws, ws_bytes, svt::kStatusBytes);
@@ -202,11 +278,15 @@ size_t svt_sparse_mla_decode_workspace_size(int32_t T, int32_t H, int32_t K, int
   return a > b ? a : b;
 }
 
-svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const svt_kv_cache* kv,
-                                 const int32_t* block_table, int32_t num_reqs, int32_t max_blocks,
-                                 const int32_t* req_of_token, const int32_t* seq_lens, const int32_t* topk, int32_t K,
-                                 const int32_t* topk_len, float softmax_scale, void* out_bf16, float* lse,
-                                 int32_t num_splits, void* ws, size_t ws_bytes, svt_stream_t stream) {
+}  // extern "C"
+
+namespace svt {
+svt_status sparse_mla_decode_enqueue(const void* q_bf16, int32_t T, int32_t H, const svt_kv_cache* kv,
+                                     const int32_t* block_table, int32_t num_reqs, int32_t max_blocks,
+                                     const int32_t* req_of_token, const int32_t* seq_lens, const int32_t* topk,
+                                     int32_t K, const int32_t* topk_len, float softmax_scale, void* out_bf16,
+                                     float* lse, int32_t num_splits, void* ws, size_t ws_bytes,
+                                     bool clear_status_first, svt_stream_t stream) {
   if (T < 0 || K < 0) return fail(SVT_ERR_INVALID_ARG, "T and K must be >= 0");
   if (H <= 0) return fail(SVT_ERR_INVALID_ARG, "H must be > 0");
   if (H > 128) return fail(SVT_ERR_UNSUPPORTED, "decode supports at most 128 heads, got %d", H);
@@ -255,12 +335,20 @@ svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const
   p.num_ctas = d.num_ctas;
   p.cluster = d.cluster;
   p.status = static_cast<int*>(ws);
+  debug_fault_state(&p.fault, &p.wait_limit_ns);
+  if (!encode_q_map(p, static_cast<long long>(T) * H))
+    return fail(SVT_ERR_CUDA, "the TMA descriptor of q could not be encoded (cuTensorMapEncodeTiled)");
   if (d.partials) {
     char* base = static_cast<char*>(ws) + svt::kStatusBytes;
     p.part_o = reinterpret_cast<uint16_t*>(base);
     p.part_lse = reinterpret_cast<float*>(base + decode_part_o_bytes(d));
   }
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (clear_status_first) {
+    // every check above has passed: from here on the call enqueues its work
+    cudaError_t ce = cudaMemsetAsync(ws, 0, kStatusBytes, s);
+    if (ce != cudaSuccess) return cuda_fail(ce, "clearing the status word");
+  }
   if (d.num_ctas == 0) {
     // K == 0: every query is empty; one CTA per row-set writes out = 0 and lse = -inf
     p.tiles_per_rowset = 1;
@@ -268,6 +356,9 @@ svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const
     p.num_ctas = d.rowsets;
     p.cluster = 1;
   }
+#ifdef SVT_PHASE_TRACE
+  p.trace = trace_for(p.num_ctas);
+#endif
   cudaError_t e = svt::launch_attention(p, s);
   if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
   if (d.partials) {
@@ -275,6 +366,19 @@ svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const
     if (e != cudaSuccess) return cuda_fail(e, "decode merge launch");
   }
   return SVT_OK;
+}
+}  // namespace svt
+
+extern "C" {
+
+svt_status svt_sparse_mla_decode(const void* q_bf16, int32_t T, int32_t H, const svt_kv_cache* kv,
+                                 const int32_t* block_table, int32_t num_reqs, int32_t max_blocks,
+                                 const int32_t* req_of_token, const int32_t* seq_lens, const int32_t* topk, int32_t K,
+                                 const int32_t* topk_len, float softmax_scale, void* out_bf16, float* lse,
+                                 int32_t num_splits, void* ws, size_t ws_bytes, svt_stream_t stream) {
+  return svt::sparse_mla_decode_enqueue(q_bf16, T, H, kv, block_table, num_reqs, max_blocks, req_of_token, seq_lens,
+                                        topk, K, topk_len, softmax_scale, out_bf16, lse, num_splits, ws, ws_bytes,
+                                        false, stream);
 }
 
 size_t svt_build_group_union_workspace_size(int32_t, int32_t, int32_t) { return svt::kStatusBytes; }
@@ -350,6 +454,12 @@ svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T, int32_t
   p.num_ctas = p.num_rowsets < sms ? p.num_rowsets : sms;
   p.cluster = 1;
   p.status = static_cast<int*>(ws);
+  svt::debug_fault_state(&p.fault, &p.wait_limit_ns);
+  if (!svt::encode_q_map(p, static_cast<long long>(T) * H))
+    return fail(SVT_ERR_CUDA, "the TMA descriptor of q could not be encoded (cuTensorMapEncodeTiled)");
+#ifdef SVT_PHASE_TRACE
+  p.trace = svt::trace_for(p.num_ctas);
+#endif
   int* counts = reinterpret_cast<int*>(static_cast<char*>(ws) + svt::kStatusBytes);
   p.counts = counts;
   cudaError_t e = svt::launch_rowset_counts(enc, lens, groups, p.list_stride, H, num_slots, counts, p.status,
@@ -372,6 +482,25 @@ svt_status svt_merge_splits(const float* o_part, const float* lse_part, int32_t 
                                            static_cast<uint16_t*>(out_bf16), lse,
                                            reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "merge launch");
+  return SVT_OK;
+}
+
+svt_status svt_gather_probe(const svt_kv_cache* kv, const int32_t* slots, int64_t n, int32_t mode,
+                            uint32_t* row_xor, void* ws, size_t ws_bytes, svt_stream_t stream) {
+  long long row_stride = 0;
+  svt_status st = check_kv(kv, &row_stride);
+  if (st != SVT_OK) return st;
+  if (n < 0) return fail(SVT_ERR_INVALID_ARG, "n must be >= 0");
+  if (mode < 0 || mode > 2) return fail(SVT_ERR_INVALID_ARG, "mode must be 0, 1 or 2, got %d", static_cast<int>(mode));
+  st = check_ws(ws, ws_bytes, svt::kStatusBytes);
+  if (st != SVT_OK) return st;
+  if (n == 0) return SVT_OK;
+  if (slots == nullptr || row_xor == nullptr) return fail(SVT_ERR_INVALID_ARG, "null array argument");
+  const int row_bytes = kv->dtype == SVT_KV_BF16 ? svt::kRowBytesBf16 : svt::kRowBytesFp8;
+  cudaError_t e = svt::launch_gather_probe(static_cast<const uint8_t*>(kv->data), row_stride, row_bytes,
+                                           kv->num_pages * static_cast<long long>(kv->page_size), slots, n, mode,
+                                           row_xor, static_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "gather probe launch");
   return SVT_OK;
 }
 

@@ -106,18 +106,16 @@ constexpr int kOffBars = kOffLfin + kRowsetRows * 4;   // uint64[kNumBars]
 constexpr int kOffMisc = kOffBars + 32 * 8;            // tmem base, abort flag
 // cluster merge (decode row-sets sliced between the CTAs of a cluster)
 constexpr int kMaxCluster = 8;
-constexpr int kOffMrgLse = kOffMisc + 16;                        // float[8][64]: each CTA's column LSEs
-constexpr int kOffMrgM = kOffMrgLse + kMaxCluster * kRowsetRows * 4;  // float[64]: this CTA's maxima
+constexpr int kOffMrgM = kOffMisc + 16;                            // float[64]: this CTA's maxima
 constexpr int kOffMrgL = kOffMrgM + kRowsetRows * 4;               // float[64]: this CTA's column sums
-constexpr int kOffMrgF = kOffMrgL + kRowsetRows * 4;               // float[64]: this CTA's O^T weights
-constexpr int kOffMrgFlag = kOffMrgF + kRowsetRows * 4;            // int: O^T holds this CTA's sums
+constexpr int kOffMrgFlag = kOffMrgL + kRowsetRows * 4;            // int: O^T holds this CTA's sums
 constexpr int kOffResX = kOffMrgFlag + 16;                          // int[4]: prefill resolvers' exchange
 constexpr int kSmemUsed = kOffResX + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory map exceeds 227 KB");
 
 // barriers (stage / buffer pairs at +0, +1; slot ring entries at +0 .. +3)
-constexpr int kBarQFull = 0;        // the fillers' Q^T copies landed (cp.async arrivals)
+constexpr int kBarQFull = 0;        // the segment's Q^T landed (TMA, one arrival + bytes)
 constexpr int kBarQEmpty = 1;       // last S^T of the segment issued and done
 constexpr int kBarFull = 2;         // 2: a half-tile's rows landed in stage s
 constexpr int kBarEmpty = 4;        // 8: 4 s + j: PV done with part j of stage s (see kEmptyParts)
@@ -128,7 +126,9 @@ constexpr int kBarOFree = 18;       // the segment's epilogue has read O^T
 constexpr int kBarSlotsReady = 19;  // 4: ring entry k % 4 holds half-tile k's slots
 constexpr int kBarSlotFree = 23;    // 4: softmax and fillers are done with ring entry k % 4
 constexpr int kBarQReady = 27;      // e4m3 caches: Q^T converted to f16 in place (softmax warps)
-constexpr int kNumBars = 28;
+constexpr int kBarDrain = 28;       // both MMA issuers' last commits: every MMA has completed
+constexpr int kBarMerge = 29;       // cluster merge: the other CTAs' messages have landed
+constexpr int kNumBars = 30;
 // PV frees a stage in four parts, one per 128-channel M-block: part j (< 3) is blocks 2 j and
 // 2 j + 1 (V channels 128 j ..), part 3 blocks 6, 7 and 8 (the rope block, holding P^T, which
 // every M-block reads). The fillers refill each part as soon as it is free.
@@ -151,6 +151,33 @@ template <bool kF16>
 constexpr uint32_t kIdescPV = idesc_f32acc(128, 64, 1, 1, kF16 ? kFmtF16 : kFmtBf16);
 
 constexpr int kDeadEntry = -2147483647 - 1;  // an entry past the list's live count
+
+// Phase trace (compiled only with SVT_PHASE_TRACE, into the trace build of the library).
+// Header slots: 0 start (%globaltimer), 1 start, 2 set-up done, 3 first Q^T issued, 4 first
+// slots resolved, 5 last epilogue begins, 6 last epilogue ends, 7 roles done, 8 cluster merge
+// done, 9 end, 10 fillers have their first segment, 11 first list entry read (resolvers),
+// 12 S^T issuer sees the first Q^T, 13 cluster merge: LSEs exchanged, 14 half-tiles walked (a
+// count), 15 end (%globaltimer), 16 cluster merge: messages sent, 17 messages received, 18 own
+// channels combined. Per half-tile g:
+// 0 S^T buffer free, 1 rows landed, 2 S^T issued, 3 S^T done (softmax), 4 P^T written,
+// 5 PV issued, 6 slots ready (filler), 7 fill issued, 8 softmax has S^T in registers, 9 the
+// softmax warps agreed on the maxima, 10 P^T stored (before the proxy fence).
+#ifdef SVT_PHASE_TRACE
+__device__ __forceinline__ void trace_at(const AttnParams& p, int slot, unsigned long long v) {
+  if (p.trace != nullptr) p.trace[static_cast<long long>(blockIdx.x) * kTraceSlots + slot] = v;
+}
+__device__ __forceinline__ void trace_g(const AttnParams& p, int ev, uint32_t g) {
+  if (p.trace != nullptr && g < static_cast<uint32_t>(kTraceG))
+    p.trace[static_cast<long long>(blockIdx.x) * kTraceSlots + kTraceHead + g * kTraceEv + ev] = clock64();
+}
+#define SVT_TRACE(slot) trace_at(p, (slot), clock64())
+#define SVT_TRACE_VALUE(slot, v) trace_at(p, (slot), (v))
+#define SVT_TRACE_G(ev, g) trace_g(p, (ev), (g))
+#else
+#define SVT_TRACE(slot) ((void)0)
+#define SVT_TRACE_VALUE(slot, v) ((void)0)
+#define SVT_TRACE_G(ev, g) ((void)0)
+#endif
 
 __device__ __forceinline__ int halves_of(int len) { return (len + kHalf - 1) / kHalf; }
 
@@ -282,7 +309,7 @@ __device__ __forceinline__ float rows16_column_reduce(float (&v)[16], int lane, 
 // Decode: half-tile k's 64 entries -> slot / mask ring entry k % 4 (waiting until the softmax
 // and the fillers are done with half-tile k - 4), then SlotsReady(k % 4).
 template <bool kF16>
-__device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars, volatile int* abort_flag) {
+__device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars, const WaitCtl& wc) {
   const int ltid = static_cast<int>(threadIdx.x) - kResWarp0 * 32;
   int* slot_tab = reinterpret_cast<int*>(smem + kOffSlot);
   uint32_t* mask_tab = reinterpret_cast<uint32_t*>(smem + kOffMask);
@@ -308,6 +335,12 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
     SegWalk::with_len(s, len_raw < 0 ? 0 : (len_raw > p.K ? p.K : len_raw), te);
     if (s.n == 0) continue;
     if (e0 >= s.len) raw = kDeadEntry;
+#ifdef SVT_PHASE_TRACE
+    if (k == 0 && ltid == 0) {
+      asm volatile("" ::"r"(raw));  // the stamp follows the first entry's arrival
+      SVT_TRACE(11);
+    }
+#endif
     // the request's block-table row and length (second round, with the page reads below)
     ReqContext rc{nullptr, INT_MAX, true};
     if (has_table) {
@@ -342,13 +375,14 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
       if (slot >= 0)
         prefetch_l2_bulk(p.kv + static_cast<long long>(slot) * p.row_stride, kF16 ? kRowBytesFp8 : kRowBytesBf16);
       const uint32_t e = k % kSlotRing;
-      if (k >= kSlotRing && !mbar_wait(bar(kBarSlotFree + e), ((k / kSlotRing) - 1) & 1u, p.status, abort_flag)) {
+      if (k >= kSlotRing && !mbar_wait(bar(kBarSlotFree + e), ((k / kSlotRing) - 1) & 1u, wc)) {
         live = false;
         break;
       }
       slot_tab[e * kHalf + ltid] = slot;
       mask_tab[e * kHalf + ltid] = mask;
       mbar_arrive(bar(kBarSlotsReady + e));
+      if (k == 0 && ltid == 0) SVT_TRACE(4);
       raw = raw_next;
     }
   }
@@ -368,7 +402,7 @@ __device__ __forceinline__ uint32_t rowset_member_bits(int rpar, int H) {
 }
 
 template <bool kF16>
-__device__ void resolver_prefill_role(const AttnParams& p, uint8_t* smem, uint32_t bars, volatile int* abort_flag) {
+__device__ void resolver_prefill_role(const AttnParams& p, uint8_t* smem, uint32_t bars, const WaitCtl& wc) {
   const int ltid = static_cast<int>(threadIdx.x) - kResWarp0 * 32;
   const int rw = ltid >> 5, lane = ltid & 31;
   int* slot_tab = reinterpret_cast<int*>(smem + kOffSlot);
@@ -416,7 +450,7 @@ __device__ void resolver_prefill_role(const AttnParams& p, uint8_t* smem, uint32
       const uint32_t e = k % kSlotRing;
       // both warps stop together if the wait gives up (they share named barriers)
       const bool freed =
-          k < kSlotRing || mbar_wait(bar(kBarSlotFree + e), ((k / kSlotRing) - 1) & 1u, p.status, abort_flag);
+          k < kSlotRing || mbar_wait(bar(kBarSlotFree + e), ((k / kSlotRing) - 1) & 1u, wc);
       if (!named_bar_red_and(kNamedBarRes, kResThreads, freed)) {
         live = false;
         break;
@@ -486,15 +520,20 @@ struct E4m3Rows {
     }
   }
 
-  // code x scale and the rope, as f16, into the stage's 128-byte-swizzled blocks
-  __device__ __forceinline__ void store(uint8_t* stage, int ftid) const {
+  // code x scale and the rope, as f16, into the stage's 128-byte-swizzled blocks. Returns
+  // true when a value leaves the f16 range the contractions run in: a block scale that is
+  // not finite or whose largest product (448 x |scale|) passes 65504, or a rope value of
+  // magnitude 65536 or more (or not finite).
+  __device__ __forceinline__ bool store(uint8_t* stage, int ftid) const {
     const int cc = ftid & 3, r0 = ftid >> 2;
+    bool out_of_range = false;
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
       const uint32_t sw[4] = {scales[m].x, scales[m].y, scales[m].z, scales[m].w};
 #pragma unroll
       for (int sb = 0; sb < 4; ++sb) {
         uint32_t hi2, lo2;
+        out_of_range |= !(fabsf(__uint_as_float(sw[sb])) * 448.0f <= 65504.0f);
         split_scale_f16x2(__uint_as_float(sw[sb]), hi2, lo2);
 #pragma unroll
       for (int kb = 2 * sb; kb < 2 * sb + 2; ++kb) {
@@ -516,14 +555,17 @@ struct E4m3Rows {
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const uint4 r = rope[m];
+      out_of_range |= bf16x2_beyond_f16(r.x) | bf16x2_beyond_f16(r.y) | bf16x2_beyond_f16(r.z) |
+                      bf16x2_beyond_f16(r.w);
       *reinterpret_cast<uint4*>(stage + 8 * kBlk + sw128_offset(rr0 + 16 * m, rc)) =
           make_uint4(bf16x2_to_f16x2(r.x), bf16x2_to_f16x2(r.y), bf16x2_to_f16x2(r.z), bf16x2_to_f16x2(r.w));
     }
+    return out_of_range;
   }
 };
 
 template <bool kF16>
-__device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, volatile int* abort_flag) {
+__device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, const WaitCtl& wc) {
   const int ftid = static_cast<int>(threadIdx.x) - kFillWarp0 * 32;
   const int lane = threadIdx.x & 31;
   const uint32_t sbase = smem_u32(smem);
@@ -531,17 +573,19 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, v
   auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
   const uint8_t* qb = reinterpret_cast<const uint8_t*>(p.q);
   uint32_t g = 0, qk = 0;
-  // Q^T of segment s's row-set, once the previous segment's last S^T is done with it
+  bool fp8_range = false;  // e4m3 caches: a value beyond the f16 range was met
+  // Q^T of segment s's row-set, once the previous segment's last S^T is done with it: nine
+  // TMA boxes of 64 rows x 64 channels, each landing as one 128-byte-swizzled 8 KB block (rows
+  // past the row-set's last are other queries' rows or zeros past the tensor; their columns
+  // of S^T and O^T are never written out)
   auto load_q = [&](const Seg& s) -> bool {
-    if (!mbar_wait(bar(kBarQEmpty), (qk & 1u) ^ 1u, p.status, abort_flag)) return false;
-    const RowsetRows rr = rowset_rows(p, s.r);
-    for (int idx = ftid; idx < kRowsetRows * 72; idx += kFillThreads) {
-      const int row = idx / 72, c = idx - row * 72;
-      const bool valid = row < rr.nvalid;
-      const uint8_t* src = qb + (valid ? (rr.base + row) * (kRow * 2) + c * 16 : 0);
-      cp_async16(sbase + kOffQ + (c >> 3) * kQBlk + sw128_offset(row, c & 7), src, valid ? 16u : 0u);
+    if (!mbar_wait(bar(kBarQEmpty), (qk & 1u) ^ 1u, wc)) return false;
+    if (ftid == 0) {
+      const RowsetRows rr = rowset_rows(p, s.r);
+      mbar_arrive_expect_tx(bar(kBarQFull), kBlocks * kQBlk);
+      for (int kb = 0; kb < kBlocks; ++kb)
+        tma_load_2d(sbase + kOffQ + kb * kQBlk, &p.q_map, 64 * kb, static_cast<int>(rr.base), bar(kBarQFull));
     }
-    cp_async_arrive_noinc(bar(kBarQFull));
     ++qk;
     return true;
   };
@@ -565,38 +609,42 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, v
   while (live && walk.next(p, s)) {
     if (s.n == 0) continue;
     // the first segment's Q^T needs no wait: it goes out before the first rows' slots exist
+    if (g == 0 && ftid == 0) SVT_TRACE(10);
     if (g == 0 && !load_q(s)) break;
+    if (g == 0 && ftid == 0) SVT_TRACE(3);
     for (int i = 0; i < s.n; ++i, ++g) {
       const uint32_t st = g & 1u, e = g % kSlotRing;
       const int* slots = slot_tab + e * kHalf;
       if constexpr (kF16) {
         // e4m3: the raw rows go into registers as soon as their slots are known, so that they
         // are in flight while the stage is still busy; converted and stored when it frees
-        if (!mbar_wait(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, p.status, abort_flag)) {
+        if (!mbar_wait(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, wc)) {
           live = false;
           break;
         }
+        if (ftid == 0) SVT_TRACE_G(6, g);
         E4m3Rows rows;
         rows.load(p, slots, ftid);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarSlotFree + e));
         // the converting stores go in one sweep once the whole stage is free (the last part
         // frees last); storing part by part costs registers the conversion needs
-        if (!mbar_wait(bar(kBarEmpty + kEmptyParts * st + kEmptyParts - 1), ((g >> 1) & 1u) ^ 1u, p.status,
-                       abort_flag)) {
+        if (!mbar_wait(bar(kBarEmpty + kEmptyParts * st + kEmptyParts - 1), ((g >> 1) & 1u) ^ 1u, wc)) {
           live = false;
           break;
         }
-        rows.store(smem + kOffStage + st * kStageBytes, ftid);
+        fp8_range |= rows.store(smem + kOffStage + st * kStageBytes, ftid);
+        if (ftid == 0) SVT_TRACE_G(7, g);
         fence_proxy_async_smem();
-        mbar_arrive(bar(kBarFull + st));
+        if (!(g == 0 && (p.fault & kFaultWithholdFirstFill))) mbar_arrive(bar(kBarFull + st));
       } else {
         // half-tile g's slots; the stage's parts are waited for below, each as PV of
         // half-tile g - 2 frees it
-        if (!mbar_wait(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, p.status, abort_flag)) {
+        if (!mbar_wait(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, wc)) {
           live = false;
           break;
         }
+        if (ftid == 0) SVT_TRACE_G(6, g);
         // chunk ftid + 128 u is block u / 4, row ftid / 8 + 16 (u % 4), 16-byte column ftid % 8:
         // a thread touches four rows, so their slots are read once and the 36 copies go out
         // back to back
@@ -614,7 +662,7 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, v
         }
 #pragma unroll
         for (int part = 0; part < kEmptyParts; ++part) {
-          if (!mbar_wait(bar(kBarEmpty + kEmptyParts * st + part), ((g >> 1) & 1u) ^ 1u, p.status, abort_flag)) {
+          if (!mbar_wait(bar(kBarEmpty + kEmptyParts * st + part), ((g >> 1) & 1u) ^ 1u, wc)) {
             live = false;
             break;
           }
@@ -626,7 +674,8 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, v
           }
         }
         if (!live) break;
-        cp_async_arrive_noinc(bar(kBarFull + st));
+        if (ftid == 0) SVT_TRACE_G(7, g);
+        if (!(g == 0 && (p.fault & kFaultWithholdFirstFill))) cp_async_arrive_noinc(bar(kBarFull + st));
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarSlotFree + e));
       }
@@ -638,6 +687,7 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, v
     }
   }
   cp_async_wait_all();
+  if (__any_sync(0xffffffffu, fp8_range) && lane == 0) atomicOr(p.status, SVT_DEV_ERR_FP8_RANGE);
 }
 
 // ---------------------------------------------------------------------------------- issuers
@@ -645,7 +695,7 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, v
 // softmax is done with the buffer's previous contents (half-tile g - 2).
 template <bool kF16>
 __device__ void s_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars,
-                              volatile int* abort_flag) {
+                              const WaitCtl& wc) {
   const uint32_t sbase = smem_u32(smem);
   auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
   uint32_t g = 0, qk = 0;
@@ -655,12 +705,15 @@ __device__ void s_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   while (walk.next(p, s)) {
     if (s.n == 0) continue;
     // Q^T landed (bf16), or landed and converted to f16 (e4m3 caches)
-    if (!mbar_wait(bar(kF16 ? kBarQReady : kBarQFull), qk & 1u, p.status, abort_flag)) return;
+    if (!mbar_wait(bar(kF16 ? kBarQReady : kBarQFull), qk & 1u, wc)) return;
+    if (qk == 0) SVT_TRACE(12);
     ++qk;
     for (int i = 0; i < s.n; ++i, ++g) {
       const uint32_t b = g & 1u;
-      if (g >= 2 && !mbar_wait(bar(kBarPready + b), ((g - 2) >> 1) & 1u, p.status, abort_flag)) return;
-      if (!mbar_wait(bar(kBarFull + b), (g >> 1) & 1u, p.status, abort_flag)) return;
+      if (g >= 2 && !mbar_wait(bar(kBarPready + b), ((g - 2) >> 1) & 1u, wc)) return;
+      SVT_TRACE_G(0, g);
+      if (!mbar_wait(bar(kBarFull + b), (g >> 1) & 1u, wc)) return;
+      SVT_TRACE_G(1, g);
       fence_proxy_async_smem();  // cp.async data (generic proxy) -> MMA operand reads
       tc_fence_after();
       const uint32_t stage = sbase + kOffStage + b * kStageBytes;
@@ -674,16 +727,18 @@ __device__ void s_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem,
         }
       }
       umma_commit(bar(kBarSFull + b));
+      SVT_TRACE_G(2, g);
       if (i == s.n - 1) umma_commit(bar(kBarQEmpty));
     }
   }
+  SVT_TRACE_VALUE(14, g);
 }
 
 // PV(g) from stage g % 2 and P^T, once the softmax has written P^T(g) (and, for a segment's
 // first half-tile, once the previous segment's epilogue has read O^T).
 template <bool kF16>
 __device__ void pv_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars,
-                               volatile int* abort_flag) {
+                               const WaitCtl& wc) {
   const uint32_t sbase = smem_u32(smem);
   auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
   uint32_t g = 0, qk = 0;
@@ -692,11 +747,11 @@ __device__ void pv_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem
   Seg s;
   while (walk.next(p, s)) {
     if (s.n == 0) continue;
-    if (qk > 0 && !mbar_wait(bar(kBarOFree), (qk - 1) & 1u, p.status, abort_flag)) return;
+    if (qk > 0 && !mbar_wait(bar(kBarOFree), (qk - 1) & 1u, wc)) return;
     ++qk;
     for (int i = 0; i < s.n; ++i, ++g) {
       const uint32_t b = g & 1u;
-      if (!mbar_wait(bar(kBarPready + b), (g >> 1) & 1u, p.status, abort_flag)) return;
+      if (!mbar_wait(bar(kBarPready + b), (g >> 1) & 1u, wc)) return;
       tc_fence_after();
       const uint32_t stage = sbase + kOffStage + b * kStageBytes;
       const uint32_t pt = stage + 8 * kBlk;
@@ -711,6 +766,7 @@ __device__ void pv_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem
         umma_commit(bar(kBarEmpty + kEmptyParts * b + mb));  // M-block mb's V blocks are read
       }
       umma_commit(bar(kBarPvDone + b));
+      SVT_TRACE_G(5, g);
     }
   }
 }
@@ -718,7 +774,7 @@ __device__ void pv_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem
 // ---------------------------------------------------------------------------------- softmax
 template <bool kF16>
 __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars,
-                             volatile int* abort_flag) {
+                             const WaitCtl& wc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int q = warp & 3, ch = warp >> 2;
   // .16x64b layout of the quadrant's 16 rows: this thread's KV row and column parity (its
@@ -745,12 +801,16 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
     if constexpr (kF16) {
       if (nh > 0) {
         // the segment's Q^T (bf16, as it landed) becomes f16 in place for the f16 contractions
-        mbar_wait(bar(kBarQFull), qs & 1u, p.status, abort_flag);
+        mbar_wait(bar(kBarQFull), qs & 1u, wc);
         uint4* qv = reinterpret_cast<uint4*>(smem + kOffQ);
+        bool q_range = false;
         for (int idx = threadIdx.x; idx < kBlocks * kQBlk / 16; idx += kSmThreads) {
           const uint4 v = qv[idx];
+          q_range |= bf16x2_beyond_f16(v.x) | bf16x2_beyond_f16(v.y) | bf16x2_beyond_f16(v.z) |
+                     bf16x2_beyond_f16(v.w);
           qv[idx] = make_uint4(bf16x2_to_f16x2(v.x), bf16x2_to_f16x2(v.y), bf16x2_to_f16x2(v.z), bf16x2_to_f16x2(v.w));
         }
+        if (__any_sync(0xffffffffu, q_range) && lane == 0) atomicOr(p.status, SVT_DEV_ERR_FP8_RANGE);
         fence_proxy_async_smem();
         mbar_arrive(bar(kBarQReady));
         ++qs;
@@ -763,8 +823,9 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
     for (int i = 0; i < nh; ++i, ++g) {
       const uint32_t b = g & 1u;
       const uint32_t e = g % kSlotRing;
-      mbar_wait(bar(kBarSFull + b), (g >> 1) & 1u, p.status, abort_flag);
-      mbar_wait(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, p.status, abort_flag);
+      mbar_wait(bar(kBarSFull + b), (g >> 1) & 1u, wc);
+      if (threadIdx.x == 0) SVT_TRACE_G(3, g);
+      mbar_wait(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, wc);
       tc_fence_after();
       float x[16];
       {
@@ -777,6 +838,7 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
         if (lane == 0) mbar_arrive(bar(kBarSlotFree + e));  // the ring entry is read
         const uint32_t live = slot < 0 ? 0u : (decode ? 0xFFFFFFFFu : live_columns(mk, rpar, ch, p.H) >> cp);
         tmem_ld_wait();
+        if (threadIdx.x == 0) SVT_TRACE_G(8, g);
 #pragma unroll
         for (int c = 0; c < 16; ++c)
           x[c] = ((live >> (2 * c)) & 1u) ? __uint_as_float(sv[c]) * p.scale_log2 : -CUDART_INF_F;
@@ -798,6 +860,7 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
           : "=r"(any)
           : "r"(static_cast<uint32_t>(exceed)), "r"(kNamedBarSm), "r"(kSmThreads)
           : "memory");
+      if (threadIdx.x == 0) SVT_TRACE_G(9, g);
       if (any) {
         // exact column maxima of this half-tile, then move the reference and rescale
         {
@@ -824,7 +887,7 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
         if (i > 0) {
           // O^T holds every PV so far once the previous half-tile's PV is done
           const uint32_t gp = g - 1;
-          mbar_wait(bar(kBarPvDone + (gp & 1u)), (gp >> 1) & 1u, p.status, abort_flag);
+          mbar_wait(bar(kBarPvDone + (gp & 1u)), (gp >> 1) & 1u, wc);
           tc_fence_after();
 #pragma unroll 1
           for (int part = 0; part < 8; ++part) {  // 4 M-blocks x my 32 columns in halves
@@ -870,15 +933,18 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
         *reinterpret_cast<uint4*>(prow + sw128_offset(kvrow, 4 * ch + 2 * cp)) = make_uint4(w[0], w[1], w[2], w[3]);
         *reinterpret_cast<uint4*>(prow + sw128_offset(kvrow, 4 * ch + 2 * cp + 1)) = make_uint4(w[4], w[5], w[6], w[7]);
       }
+      if (threadIdx.x == 0) SVT_TRACE_G(10, g);
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(bar(kBarPready + b));
+      if (threadIdx.x == 0) SVT_TRACE_G(4, g);
     }
 
     // ------------------------------------------------------------------ epilogue
+    if (threadIdx.x == 0) SVT_TRACE(5);
     if (nh > 0) {
       const uint32_t gp = g - 1;
-      mbar_wait(bar(kBarPvDone + (gp & 1u)), (gp >> 1) & 1u, p.status, abort_flag);
+      mbar_wait(bar(kBarPvDone + (gp & 1u)), (gp >> 1) & 1u, wc);
       tc_fence_after();
     }
     const RowsetRows rr = rowset_rows(p, s.r);
@@ -900,6 +966,7 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
         if (col == 0) *reinterpret_cast<int*>(smem + kOffMrgFlag) = nh > 0 ? 1 : 0;
       }
       named_bar_sync(kNamedBarSm, kSmThreads);
+      if (threadIdx.x == 0) SVT_TRACE(6);
       continue;
     }
     if (threadIdx.x < kRowsetRows) {
@@ -961,108 +1028,176 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
       }
     }
     named_bar_sync(kNamedBarSm, kSmThreads);
+    if (threadIdx.x == 0) SVT_TRACE(6);
   }
 }
 
 // ---------------------------------------------------------------------------------- cluster merge
 // Decode row-set r = blockIdx.x / C is cut into C slices, one per CTA of a cluster of C; each
-// CTA holds its slice's unnormalised O^T in TMEM with its column maxima m_k and sums l_k.
-// The split merge ("parallel tiled softmax", explainer of arXiv 2511.11581, section 4.5)
-// happens here, through distributed shared memory, once every role of every CTA is done:
-//   lse = log2 sum_k 2^(m_k + log2 l_k),   out = sum_k 2^(m_k - lse) O_k   (log2 units)
-// CTA j owns channels [512 j / C, 512 (j + 1) / C): every CTA sends its weighted O^T values of
-// those channels into CTA j's receive buffer (the freed stages), CTA j adds the C
-// contributions and writes its channels of the 64 rows. All 512 threads take part.
-__device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem) {
+// CTA holds its slice's unnormalised O^T in TMEM with its column maxima m_k and sums l_k
+// (log2 units). The split merge ("parallel tiled softmax", explainer of arXiv 2511.11581,
+// section 4.5) happens here, through distributed shared memory, once every role is done:
+//   lse = log2 sum_k 2^lse_k,  out = sum_k 2^(lse_k - lse) n_k,  lse_k = m_k + log2 l_k,
+// with n_k = O_k / l_k the slice's normalised output (bounded by the largest |V|, so fp16
+// keeps it to 2^-11 relative). CTA j owns channels [512 j / C, 512 (j + 1) / C). Each CTA
+// packs, for every other CTA j, one message in its own shared memory (its 64 column LSEs,
+// then n_k of j's channels as fp16 [channel][72]: 64 columns and a pad) and sends it with one
+// bulk copy into j's receive buffer, completing on j's merge barrier. Then it combines its
+// own channels with the C - 1 messages it received and writes them out, staged through
+// shared memory so that the global stores are whole 16-byte runs of a row. The only
+// cluster-wide wait is the cluster barrier whose arrival each CTA makes when its stages are
+// free (its receive buffer lives in them), waited for just before the sends.
+constexpr int kMrgPitch = 72;  // fp16 per channel row of a message: 64 columns + 8 pad
+__host__ __device__ constexpr int merge_msg_bytes(int C) { return 256 + (kVdim / C) * kMrgPitch * 2; }
+__host__ __device__ constexpr int merge_region_bytes(int C) { return ((C - 1) * merge_msg_bytes(C) + 255) & ~255; }
+// shared-memory use after the stages: messages out | messages in | the output tile [64][512 / C]
+// bf16 | weights [C][64] fp32 (own, then one row per message)
+__host__ __device__ constexpr int merge_bytes(int C) {
+  return 2 * merge_region_bytes(C) + kRowsetRows * (kVdim / C) * 2 + C * kRowsetRows * 4;
+}
+static_assert(merge_bytes(2) <= 2 * kStageBytes && merge_bytes(4) <= 2 * kStageBytes &&
+                  merge_bytes(8) <= 2 * kStageBytes,
+              "merge buffers");
+
+__device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars, const WaitCtl& wc) {
   const int C = p.cluster;
-  const uint32_t rank = cluster_ctarank();
+  const int rank = static_cast<int>(cluster_ctarank());
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  float* mrg_lse = reinterpret_cast<float*>(smem + kOffMrgLse);
+  const int qd = warp & 3, cg = warp >> 2;  // TMEM quadrant (channels) and 16-column group
+  const int chunk = kVdim / C;
+  const int msg = merge_msg_bytes(C);
+  uint8_t* send = smem + kOffStage;
+  uint8_t* recv = send + merge_region_bytes(C);
+  uint16_t* tile = reinterpret_cast<uint16_t*>(recv + merge_region_bytes(C));  // [64][chunk] bf16
+  float* wts = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tile) + kRowsetRows * chunk * 2);  // [C][64]
   const float* mrg_m = reinterpret_cast<const float*>(smem + kOffMrgM);
   const float* mrg_l = reinterpret_cast<const float*>(smem + kOffMrgL);
-  float* mrg_f = reinterpret_cast<float*>(smem + kOffMrgF);
   const bool had = *reinterpret_cast<const int*>(smem + kOffMrgFlag) != 0;
   const RowsetRows rr = rowset_rows(p, static_cast<int>(blockIdx.x) / C);
-  // 1. this CTA's column LSEs into every CTA's table
+  const uint32_t tq = tmem + (static_cast<uint32_t>(32 * qd) << 16) + kTmemO + 16 * cg;
+  // this CTA's stages are free: the other CTAs may send into them once all have arrived
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  // 1. per column: this CTA's LSE into every message header, 1 / l into wts[0]
   if (tid < kRowsetRows) {
     const float l = mrg_l[tid];
-    const float lse2 = l > 0.f ? mrg_m[tid] + __log2f(l) : -CUDART_INF_F;
-    const uint32_t a = smem_u32(mrg_lse + rank * kRowsetRows + tid);
-    for (int j = 0; j < C; ++j) st_cluster_f32(mapa_shared(a, static_cast<uint32_t>(j)), lse2);
+    const float v = l > 0.f ? mrg_m[tid] + __log2f(l) : -CUDART_INF_F;
+#pragma unroll 1
+    for (int s = 0; s < C - 1; ++s) reinterpret_cast<float*>(send + s * msg)[tid] = v;
+    wts[tid] = l > 0.f ? 1.0f / l : 0.f;
   }
-  cluster_sync_all();
-  // 2. the merged LSE and this CTA's weights
+  __syncthreads();
+  // 2. n_k of the other CTAs' channels into their messages. All four M-blocks' 16 columns
+  //    come out of TMEM with one wait (a TMEM load takes hundreds of cycles to return) and
+  //    stay in registers for step 4.
+  uint32_t o[4][16];
+  if (had) {
+#pragma unroll
+    for (int mb = 0; mb < 4; ++mb) tmem_ld16(tq + 64 * mb, o[mb]);
+    tmem_ld_wait();
+  } else {
+#pragma unroll
+    for (int mb = 0; mb < 4; ++mb)
+#pragma unroll
+      for (int c = 0; c < 16; ++c) o[mb][c] = 0u;
+  }
+#pragma unroll
+  for (int mb = 0; mb < 4; ++mb) {
+    const int ch0 = 128 * mb + 32 * qd;  // this warp's first channel; its owner is warp-uniform
+    const int owner = ch0 / chunk;
+    if (owner == rank) continue;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(send + (owner < rank ? owner : owner - 1) * msg + 256) +
+                    (ch0 + lane - owner * chunk) * kMrgPitch + 16 * cg;
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      h[i] = pack_f16x2(__uint_as_float(o[mb][2 * i]) * wts[16 * cg + 2 * i],
+                        __uint_as_float(o[mb][2 * i + 1]) * wts[16 * cg + 2 * i + 1]);
+    reinterpret_cast<uint4*>(dst)[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    reinterpret_cast<uint4*>(dst)[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+  fence_proxy_async_smem();  // the messages (generic writes) are read by the bulk copies
+  __syncthreads();
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (tid == 0) {
+#pragma unroll 1
+    for (int j = 0; j < C; ++j) {
+      if (j == rank) continue;
+      const uint32_t src = smem_u32(send + (j < rank ? j : j - 1) * msg);
+      const uint32_t dst = mapa_shared(smem_u32(recv + (rank < j ? rank : rank - 1) * msg), static_cast<uint32_t>(j));
+      const uint32_t bar = mapa_shared(bars + 8u * kBarMerge, static_cast<uint32_t>(j));
+      asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                       dst),
+                   "r"(src), "r"(msg), "r"(bar)
+                   : "memory");
+    }
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  }
+  if (tid == 0) SVT_TRACE(16);
+  mbar_wait_ignoring_abort(bars + 8u * kBarMerge, 0, wc);
+  if (tid == 0) SVT_TRACE(17);
+  // 3. per column: lse over the C slices; wts[0] = 2^(lse_own - lse) / l_own, wts[1 + s] =
+  //    2^(lse_s - lse) for message s; rank 0 writes the LSE
   if (tid < kRowsetRows) {
-    float mx = -CUDART_INF_F;
-    for (int j = 0; j < C; ++j) mx = fmaxf(mx, mrg_lse[j * kRowsetRows + tid]);
+    const float l = mrg_l[tid];
+    const float own = l > 0.f ? mrg_m[tid] + __log2f(l) : -CUDART_INF_F;
+    float mx = own;
+#pragma unroll 1
+    for (int s = 0; s < C - 1; ++s) mx = fmaxf(mx, reinterpret_cast<const float*>(recv + s * msg)[tid]);
     float tot = -CUDART_INF_F;
     if (mx != -CUDART_INF_F) {
-      float sum = 0.f;
-      for (int j = 0; j < C; ++j) {
-        const float lj = mrg_lse[j * kRowsetRows + tid];
-        if (lj != -CUDART_INF_F) sum += ex2_approx(lj - mx);
+      float sum = own == -CUDART_INF_F ? 0.f : ex2_approx(own - mx);
+#pragma unroll 1
+      for (int s = 0; s < C - 1; ++s) {
+        const float lk = reinterpret_cast<const float*>(recv + s * msg)[tid];
+        if (lk != -CUDART_INF_F) sum += ex2_approx(lk - mx);
       }
       tot = mx + __log2f(sum);
     }
-    mrg_f[tid] = (mrg_l[tid] > 0.f) ? ex2_approx(mrg_m[tid] - tot) : 0.f;
+    wts[tid] = own == -CUDART_INF_F ? 0.f : ex2_approx(own - tot) * wts[tid];
+#pragma unroll 1
+    for (int s = 0; s < C - 1; ++s) {
+      const float lk = reinterpret_cast<const float*>(recv + s * msg)[tid];
+      wts[(1 + s) * kRowsetRows + tid] = lk == -CUDART_INF_F ? 0.f : ex2_approx(lk - tot);
+    }
     if (rank == 0 && p.lse != nullptr && tid < rr.nvalid) p.lse[rr.base + tid] = tot * 0.69314718055994530942f;
   }
   __syncthreads();
-  // 3. weighted O^T values to their channels' owners: receive buffer [C][64 rows][512 / C] fp32
-  //    over the stages. Warp w reads TMEM quadrant w % 4 (channels 128 mb + 32 (w % 4) + lane)
-  //    and query columns 16 (w / 4) .. + 15.
-  const int chunk = kVdim / C;
-  {
-    const int qd = warp & 3, cg = warp >> 2;
-    const uint32_t recv = smem_u32(smem + kOffStage);
+  // 4. this CTA's channels: own n plus the messages', into the output tile
+#pragma unroll
+  for (int mb = 0; mb < 4; ++mb) {
+    const int ch0 = 128 * mb + 32 * qd;
+    if (ch0 / chunk != rank) continue;
+    const int cl = ch0 + lane - rank * chunk;
+    float acc[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) acc[c] = __uint_as_float(o[mb][c]) * wts[16 * cg + c];
 #pragma unroll 1
-    for (int mb = 0; mb < 4; ++mb) {
-      uint32_t o[16];
-      if (had) {
-        tmem_ld16(tmem + (static_cast<uint32_t>(32 * qd) << 16) + kTmemO + 64 * mb + 16 * cg, o);
-        tmem_ld_wait();
-      } else {
+    for (int s = 0; s < C - 1; ++s) {
+      const uint4* src = reinterpret_cast<const uint4*>(recv + s * msg + 256 + (cl * kMrgPitch + 16 * cg) * 2);
+      const uint4 a = src[0], b = src[1];
+      const uint32_t hw[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      const float* wk = wts + (1 + s) * kRowsetRows + 16 * cg;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) o[c] = 0u;
+      for (int i = 0; i < 8; ++i) {
+        acc[2 * i] += __half2float(__ushort_as_half(static_cast<unsigned short>(hw[i] & 0xFFFFu))) * wk[2 * i];
+        acc[2 * i + 1] += __half2float(__ushort_as_half(static_cast<unsigned short>(hw[i] >> 16))) * wk[2 * i + 1];
       }
-      const int ch = 128 * mb + 32 * qd + lane;
-      const uint32_t owner = static_cast<uint32_t>(ch / chunk);
-      const int chl = ch - static_cast<int>(owner) * chunk;
-      const uint32_t base =
-          mapa_shared(recv + static_cast<uint32_t>(((static_cast<int>(rank) * kRowsetRows + 16 * cg) * chunk + chl) * 4),
-                      owner);
-#pragma unroll
-      for (int c = 0; c < 16; ++c)
-        st_cluster_f32(base + static_cast<uint32_t>(c * chunk * 4), __uint_as_float(o[c]) * mrg_f[16 * cg + c]);
     }
-  }
-  tc_fence_before();
-  cluster_sync_all();
-  tc_fence_after();
-  // 4. this CTA's channels of the 64 rows: the C contributions summed, as bf16
-  {
-    const float* recv = reinterpret_cast<const float*>(smem + kOffStage);
-    const int per_row = chunk / 8;
-    for (int item = tid; item < kRowsetRows * per_row; item += kThreads) {
-      const int q = item / per_row, c8 = item - q * per_row;
-      if (q >= rr.nvalid) continue;
-      float acc[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      for (int k = 0; k < C; ++k) {
-        const float4* v = reinterpret_cast<const float4*>(recv + (k * kRowsetRows + q) * chunk + 8 * c8);
-        const float4 a = v[0], b = v[1];
-        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-      }
-      uint4 w;
-      w.x = pack_bf16x2(acc[0], acc[1]);
-      w.y = pack_bf16x2(acc[2], acc[3]);
-      w.z = pack_bf16x2(acc[4], acc[5]);
-      w.w = pack_bf16x2(acc[6], acc[7]);
-      *reinterpret_cast<uint4*>(p.out + (rr.base + q) * kVdim + static_cast<int>(rank) * chunk + 8 * c8) = w;
-    }
+    for (int c = 0; c < 16; ++c) tile[(16 * cg + c) * chunk + cl] = static_cast<uint16_t>(pack_bf16x2(acc[c], 0.f));
   }
+  __syncthreads();
+  if (tid == 0) SVT_TRACE(18);
+  // 5. the tile's rows that exist, as whole 16-byte runs of each output row
+  const int per_row = chunk / 8;
+#pragma unroll 1
+  for (int item = tid; item < rr.nvalid * per_row; item += kThreads) {
+    const int q = item / per_row, c8 = item - q * per_row;
+    *reinterpret_cast<uint4*>(p.out + (rr.base + q) * kVdim + rank * chunk + 8 * c8) =
+        *reinterpret_cast<const uint4*>(tile + q * chunk + 8 * c8);
+  }
+  // this CTA's messages must have been read before its shared memory goes away
+  if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 template <bool kF16>
@@ -1073,11 +1208,19 @@ __global__ void __launch_bounds__(kThreads, 1) tile_attention_kernel(const __gri
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   const int warp = threadIdx.x >> 5;
+#ifdef SVT_PHASE_TRACE
+  if (threadIdx.x == 0) {
+    unsigned long long gt;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(gt));
+    SVT_TRACE_VALUE(0, gt);
+    SVT_TRACE(1);
+  }
+#endif
   // a dependent launch (the split merge) may be scheduled on SMs as this grid's CTAs exit
   if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
-    mbar_init(bar(kBarQFull), kFillThreads);
+    mbar_init(bar(kBarQFull), 1);
     mbar_init(bar(kBarQEmpty), 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar(kBarFull + s), kFillThreads);
@@ -1088,6 +1231,8 @@ __global__ void __launch_bounds__(kThreads, 1) tile_attention_kernel(const __gri
     }
     mbar_init(bar(kBarOFree), kSmThreads);
     mbar_init(bar(kBarQReady), kSmThreads);
+    mbar_init(bar(kBarDrain), 2);
+    mbar_init(bar(kBarMerge), 1);
     for (int e = 0; e < kSlotRing; ++e) {
       mbar_init(bar(kBarSlotsReady + e), kResThreads);
       mbar_init(bar(kBarSlotFree + e), kSlotFreeArrivals);
@@ -1095,6 +1240,8 @@ __global__ void __launch_bounds__(kThreads, 1) tile_attention_kernel(const __gri
     *abort_flag = 0;
     *reinterpret_cast<int*>(smem + kOffMrgFlag) = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // the cluster merge's messages from the other CTAs of the cluster complete this phase
+    if (p.cluster > 1) mbar_arrive_expect_tx(bar(kBarMerge), (p.cluster - 1) * merge_msg_bytes(p.cluster));
   }
   if (threadIdx.x < kRowsetRows) {
     reinterpret_cast<float*>(smem + kOffMrgL)[threadIdx.x] = 0.f;
@@ -1108,34 +1255,53 @@ __global__ void __launch_bounds__(kThreads, 1) tile_attention_kernel(const __gri
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (threadIdx.x == 0) SVT_TRACE(2);
+  const WaitCtl wc{p.status, abort_flag, p.wait_limit_ns > 0 ? p.wait_limit_ns : kWaitLimitNs};
 
   if (warp >= kFillWarp0) {
-    filler_role<kF16>(p, smem, bars, abort_flag);
+    filler_role<kF16>(p, smem, bars, wc);
   } else if (warp >= kResWarp0) {
     if (p.mode == kModeDecode)
-      resolver_role<kF16>(p, smem, bars, abort_flag);
+      resolver_role<kF16>(p, smem, bars, wc);
     else
-      resolver_prefill_role<kF16>(p, smem, bars, abort_flag);
-  } else if (warp == kSIssuerWarp) {
-    if ((threadIdx.x & 31) == 0) s_issuer_role<kF16>(p, smem, tmem, bars, abort_flag);
-    __syncwarp();
-  } else if (warp == kPvIssuerWarp) {
-    if ((threadIdx.x & 31) == 0) pv_issuer_role<kF16>(p, smem, tmem, bars, abort_flag);
+      resolver_prefill_role<kF16>(p, smem, bars, wc);
+  } else if (warp == kSIssuerWarp || warp == kPvIssuerWarp) {
+    if ((threadIdx.x & 31) == 0) {
+      if (warp == kSIssuerWarp)
+        s_issuer_role<kF16>(p, smem, tmem, bars, wc);
+      else
+        pv_issuer_role<kF16>(p, smem, tmem, bars, wc);
+      // Drain arrives when every MMA this thread issued has completed (at once on a normal
+      // run; after a timed-out wait the MMAs already issued may still be running)
+      umma_commit(bars + 8u * kBarDrain);
+    }
     __syncwarp();
   } else {
-    softmax_role<kF16>(p, smem, tmem, bars, abort_flag);
+    softmax_role<kF16>(p, smem, tmem, bars, wc);
   }
 
+  // no MMA may still write TMEM (or read shared memory) when the roles below reuse it
+  if (threadIdx.x == 0) mbar_wait_ignoring_abort(bars + 8u * kBarDrain, 0, wc);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (threadIdx.x == 0) SVT_TRACE(7);
   if (p.cluster > 1) {
-    cluster_merge(p, smem, tmem);
+    cluster_merge(p, smem, tmem, bars, wc);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (threadIdx.x == 0) SVT_TRACE(8);
   }
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+#ifdef SVT_PHASE_TRACE
+  if (threadIdx.x == 0) {
+    SVT_TRACE(9);
+    unsigned long long gt;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(gt));
+    SVT_TRACE_VALUE(15, gt);
+  }
+#endif
 }
 
 template <bool kF16>

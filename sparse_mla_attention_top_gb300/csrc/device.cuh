@@ -11,8 +11,9 @@
 
 namespace svt {
 
-// A pipeline wait gives up after this long, sets SVT_DEV_ERR_TIMEOUT and lets the kernel
-// run to its end without waiting again (outputs of that call are then junk, never a hang).
+// A pipeline wait gives up after this long (unless the launch sets its own limit), sets
+// SVT_DEV_ERR_TIMEOUT and lets the kernel run to its end without waiting again (outputs of
+// that call are then junk, never a hang).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -64,23 +65,44 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// What every bounded wait of a CTA shares: the status word, the CTA's abort flag (shared
+// memory) and the time limit of one wait.
+struct WaitCtl {
+  int* status;
+  volatile int* abort_flag;
+  uint64_t limit_ns;
+};
+
 // Waits for the phase of `bar` with the given parity to complete. Bounded: after
-// kWaitLimitNs it records SVT_DEV_ERR_TIMEOUT, raises the CTA's abort flag and returns
+// wc.limit_ns it records SVT_DEV_ERR_TIMEOUT, raises the CTA's abort flag and returns
 // false; once the abort flag is up every later wait returns at once, so each role runs its
 // (finite) loops to the end and the kernel exits.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* status, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& wc) {
   if (mbar_try_wait(bar, parity)) return true;
-  if (*abort_flag) return false;
+  if (*wc.abort_flag) return false;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        atomicOr(status, SVT_DEV_ERR_TIMEOUT);
-        *abort_flag = 1;
+      if (*wc.abort_flag) return false;
+      if (globaltimer() - t0 > wc.limit_ns) {
+        atomicOr(wc.status, SVT_DEV_ERR_TIMEOUT);
+        *wc.abort_flag = 1;
         return false;
       }
+    }
+  }
+}
+
+// The same wait, ignoring the abort flag (used once at the end of a kernel, to let work
+// already handed to the tensor cores finish before their memory is released).
+__device__ __forceinline__ bool mbar_wait_ignoring_abort(uint32_t bar, uint32_t parity, const WaitCtl& wc) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 15u && globaltimer() - t0 > wc.limit_ns) {
+      atomicOr(wc.status, SVT_DEV_ERR_TIMEOUT);
+      return false;
     }
   }
 }
@@ -96,6 +118,17 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
+}
+
+// 2-D tiled TMA load of the box at (x, y) of the tensor `tmap` describes (a __grid_constant__
+// kernel parameter) into shared memory at dst; completes the box's bytes on `bar`. x is the
+// innermost coordinate, in elements; x * element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
 }
 
 // ------------------------------------------------------------------------------ clusters
@@ -218,6 +251,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -330,6 +370,12 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 // Two bf16 (low half = first element) -> the same two values as f16, rounded to nearest.
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
   return pack_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// Whether either bf16 of a pair has a magnitude of 65536 or more (or is inf / NaN): such a
+// value has no f16 counterpart (the largest f16 is 65504, and no bf16 lies between the two).
+__device__ __forceinline__ bool bf16x2_beyond_f16(uint32_t w) {
+  return (w & 0x7FFFu) >= 0x4780u || ((w >> 16) & 0x7FFFu) >= 0x4780u;
 }
 
 // A block scale split into two f16 (hi = the nearest f16, lo = the f16 nearest the rest),

@@ -2,6 +2,7 @@
 // the attention kernel, and the launchers each .cu file provides to the C-ABI layer.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the type only; the encoder is reached through the runtime)
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -25,7 +26,9 @@ enum AttnMode : int { kModeDecode = 0, kModePrefill = 1 };
 enum Sched : int { kSchedStreamK = 0, kSchedRowsets = 1 };
 
 struct AttnParams {
-  // queries [T, H, 576] bf16
+  // queries [T, H, 576] bf16, and the TMA descriptor of them as a 2-D tensor [T * H, 576]
+  // with 64 x 64 boxes, 128-byte swizzle (a row-set's Q^T is 9 such boxes)
+  alignas(64) CUtensorMap q_map;
   const uint16_t* q;
   int T, H;
   // cache
@@ -68,7 +71,28 @@ struct AttnParams {
   uint16_t* part_o;  // [2 * num_ctas, 64, 512] fp16 (stream-K partial segments, normalised)
   float* part_lse;  // [2 * num_ctas, 64]
   int* status;
+  // failure detection: the limit of one pipeline wait (0 = the default) and planted faults
+  // (kFault* bits; 0 on every ordinary call)
+  unsigned long long wait_limit_ns;
+  int fault;
+  // phase trace (libsvt_trace.so only; null otherwise): [num_ctas, kTraceSlots] clock stamps
+  unsigned long long* trace;
 };
+
+// Phase trace layout, per CTA: kTraceHead header slots, then kTraceEv stamps for each of the
+// first kTraceG half-tiles the CTA walks. Stamps are clock64 of the CTA's SM except slots 0
+// and 15, which hold %globaltimer (ns) at the start and the end of the CTA.
+constexpr int kTraceHead = 48;
+constexpr int kTraceG = 48;
+constexpr int kTraceEv = 12;
+constexpr int kTraceSlots = kTraceHead + kTraceG * kTraceEv;
+
+// Planted fault: the gathering warps withhold the arrival that announces the first KV
+// half-tile, so the first wait on it runs out (failure-detection tests).
+constexpr int kFaultWithholdFirstFill = 1;
+
+// The planted fault and wait limit the next launches take (svt_debug_pipeline_fault).
+void debug_fault_state(int* fault, unsigned long long* wait_limit_ns);
 
 // Query row n (< 64) of row-set r is row base + n of the [T*H, ...] q / out / lse arrays
 // and exists iff n < nvalid. Decode: base = t*H + 64*chunk. Prefill (H*G = 128): packed
@@ -109,6 +133,10 @@ __host__ __device__ inline long long streamk_part_slot(long long c, long long fi
   return streamk_lo(c, total, n) < first ? 2 * c + 1 : 2 * c;
 }
 
+// Fills p.q_map for q [rows, 576] bf16 (cuTensorMapEncodeTiled through the runtime's driver
+// entry point); false when the encoder is unavailable or refuses the tensor.
+bool encode_q_map(AttnParams& p, long long rows);
+
 // Launchers (each returns cudaSuccess or the launch error).
 cudaError_t launch_resolve(const int32_t* topk, int T, int K, const int32_t* topk_len, const int32_t* req_of_token,
                            const int32_t* block_table, int num_reqs, int max_blocks, const int32_t* seq_lens,
@@ -129,6 +157,12 @@ cudaError_t launch_merge_splits(const float* o_part, const float* lse_part, int 
 cudaError_t launch_topk(const float* scores, int T, int N, long long stride, const int32_t* lens, int K, int32_t* out,
                         cudaStream_t stream);
 
+// Reads the rows of `slots` (mode 0: cp.async 16-byte copies into shared memory, 1: one bulk
+// copy per row, 2: 16-byte loads into registers) and writes each row's XOR of 32-bit words.
+cudaError_t launch_gather_probe(const uint8_t* kv, long long row_stride, int row_bytes, long long num_slots,
+                                const int32_t* slots, long long n, int mode, uint32_t* out, int* timed_out,
+                                cudaStream_t stream);
+
 // Decode and grouped prefill over either cache dtype (two shared-memory stages of 64-row
 // half-tiles; decode work units are half-tiles).
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
@@ -138,6 +172,15 @@ int attention_max_active_clusters(int cluster, int kv_dtype);
 // Merges the partial results of the row-sets a stream-K decode split between CTAs; launched
 // right behind the attention kernel (programmatic dependent launch) and waiting for it.
 cudaError_t launch_streamk_merge(const AttnParams& p, cudaStream_t stream);
+
+// svt_sparse_mla_decode with one more option: after every argument check has passed and
+// before the kernels, clear the workspace's status word (clear_status_first).
+svt_status sparse_mla_decode_enqueue(const void* q_bf16, int32_t T, int32_t H, const svt_kv_cache* kv,
+                                     const int32_t* block_table, int32_t num_reqs, int32_t max_blocks,
+                                     const int32_t* req_of_token, const int32_t* seq_lens, const int32_t* topk,
+                                     int32_t K, const int32_t* topk_len, float softmax_scale, void* out_bf16,
+                                     float* lse, int32_t num_splits, void* ws, size_t ws_bytes,
+                                     bool clear_status_first, svt_stream_t stream);
 
 // Records the message svt_last_error_string() returns on this thread and passes `st` back.
 svt_status set_last_error(svt_status st, const char* fmt, ...);

@@ -48,24 +48,22 @@ extern "C" SVT_API svt_status svt_sparse_mla_decode_noalloc(
     }
     scratch = g_scratch_ptr[dev];
   }
-  if (T < 0 || H <= 0 || K < 0 || num_splits < 0)
-    return svt::set_last_error(SVT_ERR_INVALID_ARG, "T, K and num_splits must be >= 0 and H > 0");
-  const size_t need = svt_sparse_mla_decode_workspace_size(T, H, K, num_splits);
-  if (need > kNoAllocScratchBytes)
+  // The ordinary decode checks every argument (and that the array is large enough for this
+  // call's partial results) before it enqueues anything; only then does it clear the array's
+  // status word, which keeps the previous call's bits (partial results are always written
+  // before they are read).
+  const svt_status st = svt::sparse_mla_decode_enqueue(q_bf16, T, H, kv, block_table, num_reqs, max_blocks,
+                                                       req_of_token, seq_lens, topk, K, topk_len, softmax_scale,
+                                                       out_bf16, lse, num_splits, scratch, kNoAllocScratchBytes,
+                                                       /*clear_status_first=*/true, stream);
+  if (st == SVT_ERR_WORKSPACE)
     return svt::set_last_error(SVT_ERR_WORKSPACE,
-                               "this decode needs %zu bytes of scratch but the built-in buffer holds %zu; "
-                               "use num_splits = 1 (no partial results) or split the batch",
-                               need, kNoAllocScratchBytes);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // The array keeps the previous call's bytes: clear the status word (partial results are
-  // written before they are read).
-  e = cudaMemsetAsync(scratch, 0, svt::kStatusBytes, s);
-  if (e != cudaSuccess) return svt::set_last_error(SVT_ERR_CUDA, "clearing scratch: %s", cudaGetErrorString(e));
-  const svt_status st = svt_sparse_mla_decode(q_bf16, T, H, kv, block_table, num_reqs, max_blocks, req_of_token,
-                                              seq_lens, topk, K, topk_len, softmax_scale, out_bf16, lse, num_splits,
-                                              scratch, kNoAllocScratchBytes, stream);
+                               "this decode needs more scratch than the built-in %zu bytes; use num_splits = 1, "
+                               "2, 4 or 8 (no partial results) or split the batch",
+                               kNoAllocScratchBytes);
   if (st != SVT_OK || status_out == nullptr) return st;
-  e = cudaMemcpyAsync(status_out, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
+  e = cudaMemcpyAsync(status_out, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                      reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return svt::set_last_error(SVT_ERR_CUDA, "copying the status word: %s", cudaGetErrorString(e));
   return SVT_OK;
 }

@@ -23,6 +23,7 @@ STATUS_NAMES = {0: "SVT_OK", 1: "SVT_ERR_INVALID_ARG", 2: "SVT_ERR_UNSUPPORTED",
                 4: "SVT_ERR_CUDA"}
 DEV_ERR_INDEX_RANGE = 0x1
 DEV_ERR_TIMEOUT = 0x2
+DEV_ERR_FP8_RANGE = 0x4
 KV_BF16 = 0
 KV_FP8_E4M3 = 1
 ROW_BYTES = {KV_BF16: 1152, KV_FP8_E4M3: 656}
@@ -33,7 +34,7 @@ EXPORTED = [
     "svt_build_group_union_workspace_size", "svt_build_group_union",
     "svt_sparse_mla_prefill_grouped_workspace_size", "svt_sparse_mla_prefill_grouped", "svt_merge_splits",
     "svt_topk_select",
-    "svt_sparse_mla_decode_noalloc",
+    "svt_sparse_mla_decode_noalloc", "svt_debug_pipeline_fault", "svt_gather_probe",
 ]
 
 
@@ -50,6 +51,15 @@ class _KV(ctypes.Structure):
 
 def library_path() -> Path:
     return _LIB_PATH
+
+
+def use_library(path) -> None:
+    """Loads the library from `path` instead of libsvt.so (the phase-trace build, for
+    profiling); must come before the first call into the library."""
+    global _LIB_PATH
+    if _lib is not None:
+        raise RuntimeError("the library is already loaded")
+    _LIB_PATH = Path(path)
 
 
 def lib():
@@ -80,6 +90,8 @@ def lib():
         L.svt_topk_select.argtypes = [P, i32, i32, i64, P, i32, P, P]
         L.svt_sparse_mla_decode_noalloc.argtypes = [P, i32, i32, ctypes.POINTER(_KV), P, i32, i32, P, P, P, i32, P, f32,
                                                     P, P, i32, P, P]
+        L.svt_debug_pipeline_fault.argtypes = [i32, i64]
+        L.svt_gather_probe.argtypes = [ctypes.POINTER(_KV), P, i64, i32, P, P, sz, P]
         _lib = L
     return _lib
 
@@ -272,4 +284,25 @@ def topk_select(scores, K: int, *, lens=None, out=None):
     stride = scores.stride(0) if T > 1 else N  # a single row's stride is meaningless (can be 0)
     _check(lib().svt_topk_select(_ptr(scores), T, N, stride, _ptr(lens), int(K), _ptr(out), _stream()),
            "svt_topk_select")
+    return out
+
+
+def debug_pipeline_fault(fault: int = 0, wait_limit_ns: int = 0) -> None:
+    """Failure-detection hook for tests (svt_debug_pipeline_fault): plant a withheld arrival
+    in the attention kernels launched afterwards and/or shorten their wait limit; (0, 0)
+    restores ordinary behaviour."""
+    _check(lib().svt_debug_pipeline_fault(int(fault), int(wait_limit_ns)), "svt_debug_pipeline_fault")
+
+
+def gather_probe(kv: KVCache, slots, mode: int = 0, *, out=None, ws: Optional[Workspace] = None):
+    """Reads the cache rows of `slots` ([n] int32) the way the decode's gather does, with no
+    arithmetic (svt_gather_probe); returns each row's XOR of 32-bit words as int32 [n]."""
+    slots = _i32(slots, "slots")
+    n = slots.numel()
+    if out is None:
+        out = torch.empty((n,), dtype=torch.int32, device=slots.device)
+    ws = default_workspace() if ws is None else ws
+    kvc = kv._c()
+    _check(lib().svt_gather_probe(ctypes.byref(kvc), _ptr(slots), n, int(mode), _ptr(out), ws.ptr, ws.nbytes,
+                                  _stream()), "svt_gather_probe")
     return out

@@ -53,12 +53,38 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
-def _normal_bf16(rng: np.random.Generator, shape, chunk: int = 1 << 24) -> np.ndarray:
+_CHUNK = 1 << 22
+
+
+def _chunked(rng: np.random.Generator, n: int, fill) -> None:
+    """Calls fill(sub_rng, start, end) for consecutive chunks of n items, in parallel threads.
+    Chunk i draws from its own PCG64 stream seeded by (a number drawn from rng, i), so the
+    bytes depend only on rng's state, not on the thread count."""
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+
+    base = int(rng.integers(0, 2 ** 63 - 1))
+    chunks = (n + _CHUNK - 1) // _CHUNK
+
+    def job(i):
+        fill(np.random.default_rng([base, i]), i * _CHUNK, min(n, (i + 1) * _CHUNK))
+
+    if chunks <= 1:
+        for i in range(chunks):
+            job(i)
+        return
+    with ThreadPoolExecutor(min(chunks, os.cpu_count() or 1, 32)) as ex:
+        list(ex.map(job, range(chunks)))
+
+
+def _normal_bf16(rng: np.random.Generator, shape) -> np.ndarray:
     n = int(np.prod(shape))
     out = np.empty(n, np.uint16)
-    for s in range(0, n, chunk):
-        e = min(n, s + chunk)
-        out[s:e] = f32_to_bf16_bits(rng.standard_normal(e - s, dtype=np.float32))
+
+    def fill(r, s, e):
+        out[s:e] = f32_to_bf16_bits(r.standard_normal(e - s, dtype=np.float32))
+
+    _chunked(rng, n, fill)
     return out.reshape(shape)
 
 
@@ -70,18 +96,32 @@ def _e4m3_codes(x: np.ndarray) -> np.ndarray:
     return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy().copy()
 
 
-def make_cache(rng: np.random.Generator, num_rows: int, kv_dtype: int, chunk_rows: int = 1 << 16) -> np.ndarray:
+def make_cache(rng: np.random.Generator, num_rows: int, kv_dtype: int) -> np.ndarray:
     """Cache bytes [num_rows, row_bytes] (uint8)."""
     if kv_dtype == KV_BF16:
         return _normal_bf16(rng, (num_rows, ROW)).view(np.uint8).reshape(num_rows, ROW_BYTES_BF16)
     out = np.empty((num_rows, ROW_BYTES_FP8), np.uint8)
-    for s in range(0, num_rows, chunk_rows):
-        e = min(num_rows, s + chunk_rows)
-        n = e - s
-        out[s:e, :LATENT] = _e4m3_codes(rng.standard_normal((n, LATENT), dtype=np.float32))
-        scales = rng.uniform(0.5, 2.0, size=(n, 4)).astype(np.float32)
-        out[s:e, LATENT:LATENT + 16] = scales.view(np.uint8).reshape(n, 16)
-        out[s:e, LATENT + 16:] = _normal_bf16(rng, (n, ROPE)).view(np.uint8).reshape(n, ROPE * 2)
+    rows_per_chunk = max(1, _CHUNK // LATENT)
+
+    def fill(r, s, e):
+        # rows s .. e-1 of this chunk: latent codes, block scales, rope
+        out[s:e, :LATENT] = _e4m3_codes(r.standard_normal((e - s, LATENT), dtype=np.float32))
+        scales = r.uniform(0.5, 2.0, size=(e - s, 4)).astype(np.float32)
+        out[s:e, LATENT:LATENT + 16] = scales.view(np.uint8).reshape(e - s, 16)
+        rope = f32_to_bf16_bits(r.standard_normal((e - s) * ROPE, dtype=np.float32))
+        out[s:e, LATENT + 16:] = rope.view(np.uint8).reshape(e - s, ROPE * 2)
+
+    base = int(rng.integers(0, 2 ** 63 - 1))
+    from concurrent.futures import ThreadPoolExecutor
+    import os
+
+    chunks = (num_rows + rows_per_chunk - 1) // rows_per_chunk
+
+    def job(i):
+        fill(np.random.default_rng([base, i]), i * rows_per_chunk, min(num_rows, (i + 1) * rows_per_chunk))
+
+    with ThreadPoolExecutor(max(1, min(chunks, os.cpu_count() or 1, 32))) as ex:
+        list(ex.map(job, range(chunks)))
     return out
 
 
@@ -281,6 +321,12 @@ def grouped_prefill(n_new: int = 8192) -> PrefillWorkload:
     """One request of 8192 new causal tokens, 64 heads, groups of 2, page_size 64, top-k 2048."""
     return make_prefill(3, n_new=n_new, n_cached=0, H=64, G=2, K=2048, page_size=64,
                         name=f"prefill_bf16_t{n_new}_h64_g2_k2048_p64")
+
+
+def grouped_prefill_fp8(n_new: int = 8192) -> PrefillWorkload:
+    """The 8192-token grouped prefill (64 heads, groups of 2) over an e4m3 cache."""
+    return make_prefill(8, n_new=n_new, n_cached=0, H=64, G=2, K=2048, page_size=64, kv_dtype=KV_FP8_E4M3,
+                        name=f"prefill_fp8_t{n_new}_h64_g2_k2048_p64")
 
 
 def mixed_prefill(n_new: int = 8192) -> PrefillWorkload:

@@ -157,3 +157,10 @@ def test_product_path_has_no_oracle_or_fallback():
         if fn.endswith(".py"):
             src = open(os.path.join(pkg, fn)).read()
             assert "import oracle" not in src and "from oracle" not in src, fn
+
+
+def test_debug_pipeline_fault_checks_its_arguments(L):
+    assert L.svt_debug_pipeline_fault(7, 0) == svt.SVT_ERR_INVALID_ARG
+    assert L.svt_debug_pipeline_fault(0, -1) == svt.SVT_ERR_INVALID_ARG
+    assert L.svt_debug_pipeline_fault(1, 1000) == svt.SVT_OK
+    assert L.svt_debug_pipeline_fault(0, 0) == svt.SVT_OK  # back to ordinary behaviour

@@ -28,3 +28,35 @@ def test_rowset_kept_counts_brute_force(H, G):
                 n += any((m >> b) & 1 for b in members)
             want.append(n)
     assert got.tolist() == want
+
+
+def test_phase_trace_analysis_on_a_synthetic_launch():
+    # two CTAs at 2 GHz (2 cycles per ns): set-up 1000 cycles, half-tiles every 4000 cycles,
+    # rows landing 1500 cycles after their fill is issued, S^T done 800 cycles after issue
+    slots = bench.TRACE_HEAD + bench.TRACE_G * bench.TRACE_EV
+    tr = np.zeros((4, slots), np.uint64)
+    for c in range(2):
+        c0, gt0 = 10_000 + 37 * c, 5_000_000 + 100 * c
+        n = 10
+        ev = np.zeros((bench.TRACE_G, bench.TRACE_EV), np.int64)
+        for g in range(n):
+            issue = c0 + 6000 + 4000 * g
+            ev[g, :8] = [issue - 500, issue - 100, issue, issue + 800, issue + 1400, issue + 1500, issue - 3000,
+                         issue - 1600]
+            ev[g, 8:11] = [issue + 900, issue + 1000, issue + 1300]
+        end = c0 + 6000 + 4000 * n + 3000
+        tr[c, 0], tr[c, 1], tr[c, 2], tr[c, 3], tr[c, 4] = gt0, c0, c0 + 1000, c0 + 1200, c0 + 2000
+        tr[c, 5], tr[c, 6], tr[c, 7], tr[c, 9] = end - 2000, end - 1000, end - 500, end
+        tr[c, 14], tr[c, 15] = n, gt0 + (end - c0) // 2
+        tr[c, bench.TRACE_HEAD:] = ev.reshape(-1).astype(np.uint64)
+    out = bench.analyse_trace(tr)
+    assert out["ctas"] == 2 and abs(out["sm_ghz"] - 2.0) < 1e-6
+    assert out["half_tile_period_us"] == pytest.approx(2.0)      # 4000 cycles
+    assert out["fill_issue_to_landed_us"] == pytest.approx(0.75)  # 1500 cycles
+    assert out["s_issue_to_done_us"] == pytest.approx(0.4)
+    assert out["softmax_us"] == pytest.approx(0.3)
+    assert out["setup_us"] == pytest.approx(0.5)
+    assert out["first_s_issued_us"] == pytest.approx(3.0)
+    assert out["s_issuer_wait_rows_us"] == pytest.approx(0.2)     # buffer free at -500, rows at -100
+    assert out["softmax_tmem_load_us"] == pytest.approx(0.05)
+    assert out["softmax_fence_arrive_us"] == pytest.approx(0.05)

@@ -1,7 +1,9 @@
 """The five benchmark workloads at full size, in the launch configuration bench.py times
 (automatic split for decode), checked against the oracle: integer outputs (slots, unions)
-in full and bit-exact, attention outputs on sampled queries (every head of each) within
-the tolerances. Workloads: tiny decode (8 heads, 64 of 256); bf16 decode batch (64 x 64
+in full and bit-exact; attention outputs of every query of the decode workloads and of a
+stratified sample of more than 256 prefill queries (every member of groups spread over the
+run and of the groups where the lists change shape), every head of each, within the
+tolerances. Workloads: tiny decode (8 heads, 64 of 256); bf16 decode batch (64 x 64
 heads, top-k 2048, contexts 8K-32K); e4m3 decode batch (128 x 64 heads, contexts 4K-46K);
 grouped prefill (8192 new tokens, 64 heads, groups of 2); mixed step (16 heads, groups of 8,
 8192 new on 24K cached, 128 decodes at 16K-46K, top-k = all dense check at 4K)."""
@@ -57,14 +59,14 @@ def test_tiny_decode_full(S, dev):
     check_decode_sampled(S, w, dev, np.arange(w.T))
 
 
-def test_decode_bf16_batch_sampled(S, dev):
+def test_decode_bf16_batch_every_query(S, dev):
     w = W.decode_bf16_batch()
-    check_decode_sampled(S, w, dev, np.array([0, 17, 40, 63]))
+    check_decode_sampled(S, w, dev, np.arange(w.T))
 
 
-def test_decode_fp8_batch_sampled(S, dev):
+def test_decode_fp8_batch_every_query(S, dev):
     w = W.decode_fp8_batch()
-    check_decode_sampled(S, w, dev, np.array([0, 50, 99, 127]))
+    check_decode_sampled(S, w, dev, np.arange(w.T))
 
 
 def run_prefill_and_check(S, w, dev, ids):
@@ -92,23 +94,43 @@ def run_prefill_and_check(S, w, dev, ids):
     return float(ref_lens.mean() / live.mean())
 
 
-def test_grouped_prefill_sampled(S, dev):
+def stratified_groups(w, n_spread: int) -> np.ndarray:
+    """Every member of n_spread groups spread evenly over the run, plus every group whose
+    members' lists change from the whole causal prefix to the 70 % neighbour lists (the
+    queries whose prefix first exceeds K) and the first and last groups."""
+    groups = (w.T + w.G - 1) // w.G
+    gs = set(np.linspace(0, groups - 1, n_spread).round().astype(int).tolist())
+    n_cached = int(w.seq_lens[0]) - w.T
+    first_full = max(0, w.K - n_cached - 1)  # first query with at least K candidates
+    for q in (first_full - 1, first_full, first_full + 1):
+        if 0 <= q < w.T:
+            gs.add(q // w.G)
+    gs.update({0, groups - 1})
+    ids = [g * w.G + m for g in sorted(gs) for m in range(w.G) if g * w.G + m < w.T]
+    return np.array(ids, np.int64)
+
+
+def test_grouped_prefill_stratified(S, dev):
+    # both members of more than 128 groups (over 256 queries), every head of each
     w = W.grouped_prefill()
-    ids = np.array([0, 1, 2, 1000, 2046, 2047, 2048, 2049, 5001, 8190, 8191])
+    ids = stratified_groups(w, 130)
+    assert len(ids) >= 256
     union_lists = run_prefill_and_check(S, w, dev, ids)
     assert 1.0 < union_lists < 2.0
 
 
-def test_mixed_prefill_sampled(S, dev):
+def test_mixed_prefill_stratified(S, dev):
+    # all 8 members of 40 groups (320 queries)
     w = W.mixed_prefill()
-    ids = np.array([0, 7, 8, 15, 4003, 8184, 8191])
+    ids = stratified_groups(w, 40)
+    assert len(ids) >= 256
     union_lists = run_prefill_and_check(S, w, dev, ids)
     assert 1.0 < union_lists < 8.0
 
 
-def test_mixed_decode_sampled(S, dev):
+def test_mixed_decode_every_query(S, dev):
     w = W.mixed_decode()
-    check_decode_sampled(S, w, dev, np.array([0, 64, 127]))
+    check_decode_sampled(S, w, dev, np.arange(w.T))
 
 
 def test_dense_check_topk_all_equals_dense_paged(S, dev):
