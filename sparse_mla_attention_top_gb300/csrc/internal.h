@@ -143,6 +143,9 @@ cudaError_t launch_resolve(const int32_t* topk, int T, int K, const int32_t* top
                            int page_size, long long num_pages, int32_t* slots, int* status, cudaStream_t stream);
 
 size_t union_smem_bytes(int G, int K);
+// Caches of at most this many rows take the union's dense-table kernel (one shared-memory
+// byte per row); larger ones the sort.
+constexpr long long kDenseUnionSlots = 65536;
 // Per row-set (half of a group's 128 packed rows) the number of union entries live for one of
 // its members: counts[2 g + half]. Entries whose slot is out of range are dead and set the
 // range error bit.

@@ -3,7 +3,7 @@
 // "The Virtual Block Table: Reusing Triton MLA for Sparse Attention on Blackwell GPUs",
 // The Investigation: a position resolves through the request's page table as
 //   slot = table[req, pos / P] * P + pos % P.
-// One thread per (query, entry): blockIdx.y walks the queries, x the entries, so no index
+// Four entries per thread: blockIdx.y walks the queries, x the entries, so no index
 // division is needed. Memory-bound: 4 bytes in and 4 bytes out per entry, plus the
 // page-table read, which mostly hits L2.
 #include "device.cuh"
@@ -12,25 +12,50 @@
 
 namespace svt {
 
-__global__ void __launch_bounds__(256) resolve_kernel(const int32_t* __restrict__ topk, int T, int K,
-                                                      const int32_t* __restrict__ topk_len,
-                                                      const int32_t* __restrict__ req_of_token,
-                                                      const int32_t* __restrict__ block_table, int num_reqs,
-                                                      int max_blocks, const int32_t* __restrict__ seq_lens,
-                                                      int page_size, long long num_pages,
-                                                      int32_t* __restrict__ slots, int* status) {
+// Four consecutive entries of one query per thread (their page-table reads in flight
+// together), blockIdx.y walking the queries: no index division. With vec, K is a multiple of
+// 4 and both arrays are 16-byte aligned, so the entries move as one 16-byte load and store.
+constexpr int kResolveThreads = 256;
+
+__global__ void __launch_bounds__(kResolveThreads) resolve_kernel(const int32_t* __restrict__ topk, int T, int K,
+                                                                  const int32_t* __restrict__ topk_len,
+                                                                  const int32_t* __restrict__ req_of_token,
+                                                                  const int32_t* __restrict__ block_table,
+                                                                  int num_reqs, int max_blocks,
+                                                                  const int32_t* __restrict__ seq_lens,
+                                                                  int page_size, long long num_pages, int vec,
+                                                                  int32_t* __restrict__ slots, int* status) {
   int err = 0;
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  const int j0 = (blockIdx.x * kResolveThreads + threadIdx.x) * 4;
   for (int t = blockIdx.y; t < T; t += gridDim.y) {
-    if (j >= K) break;
+    if (j0 >= K) break;
     const int len = topk_len ? topk_len[t] : K;
-    const long long idx = static_cast<long long>(t) * K + j;
-    int slot = -1;
-    if (j < len) {
-      slot = resolve_position(__ldg(topk + idx), t, req_of_token, block_table, num_reqs, max_blocks, seq_lens,
-                              page_size, num_pages, &err);
+    const long long idx = static_cast<long long>(t) * K + j0;
+    int pos[4];
+    if (vec) {
+      const int4 v = __ldg(reinterpret_cast<const int4*>(topk + idx));
+      pos[0] = v.x, pos[1] = v.y, pos[2] = v.z, pos[3] = v.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) pos[i] = j0 + i < K ? __ldg(topk + idx + i) : -1;
     }
-    slots[idx] = slot;
+    const ReqContext c = request_context(t, req_of_token, block_table, num_reqs, max_blocks, seq_lens);
+    int phys[4], out[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (j0 + i >= len) pos[i] = -1;  // past the live count: dead, never checked
+      phys[i] = page_of(pos[i], c, max_blocks, page_size);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      out[i] = slot_of(pos[i], phys[i], c, block_table != nullptr, max_blocks, page_size, num_pages, &err);
+    if (vec) {
+      *reinterpret_cast<int4*>(slots + idx) = make_int4(out[0], out[1], out[2], out[3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (j0 + i < K) slots[idx + i] = out[i];
+    }
   }
   if (__any_sync(0xffffffffu, err) && (threadIdx.x & 31) == 0) atomicOr(status, SVT_DEV_ERR_INDEX_RANGE);
 }
@@ -39,9 +64,13 @@ cudaError_t launch_resolve(const int32_t* topk, int T, int K, const int32_t* top
                            const int32_t* block_table, int num_reqs, int max_blocks, const int32_t* seq_lens,
                            int page_size, long long num_pages, int32_t* slots, int* status, cudaStream_t stream) {
   if (static_cast<long long>(T) * K == 0) return cudaSuccess;
-  const dim3 grid((K + 255) / 256, T < 65535 ? T : 65535);
-  resolve_kernel<<<grid, 256, 0, stream>>>(topk, T, K, topk_len, req_of_token, block_table, num_reqs, max_blocks,
-                                           seq_lens, page_size, num_pages, slots, status);
+  const int vec = (K % 4 == 0 && (reinterpret_cast<uintptr_t>(topk) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(slots) & 15) == 0)
+                      ? 1
+                      : 0;
+  const dim3 grid((K + 4 * kResolveThreads - 1) / (4 * kResolveThreads), T < 65535 ? T : 65535);
+  resolve_kernel<<<grid, kResolveThreads, 0, stream>>>(topk, T, K, topk_len, req_of_token, block_table, num_reqs,
+                                                       max_blocks, seq_lens, page_size, num_pages, vec, slots, status);
   return cudaGetLastError();
 }
 

@@ -6,11 +6,13 @@
 // groups, entries past a query's count, negative rows and rows up to the 24-bit limit, and
 // every query keeps to its own rows through its membership bit.
 //
-// One CTA per group. The G*K candidate entries become 27-bit keys (slot << 3 | member) in
-// shared memory, a bitonic sort orders them by slot (then member), and a block scan over
-// run starts gives each distinct slot its output position; the run's members are ORed into
-// the mask. Output entry: (mask << 24) | slot, then -1 padding up to G*K. Integer only, so
-// the result is bit-exact by construction. Bound by shared-memory traffic of the sort.
+// One CTA per group, in one of two ways. A cache of at most kDenseUnionSlots rows gets a
+// dense table of one membership byte per row in shared memory, filled by the members and
+// scanned in row order (union_dense_kernel). A larger cache: the G*K candidate entries become
+// 27-bit keys (slot << 3 | member) in shared memory, a bitonic sort orders them by slot (then
+// member), and a block scan over run starts gives each distinct slot its output position;
+// the run's members are ORed into the mask. Output entry: (mask << 24) | slot, then -1
+// padding up to G*K. Integer only, so the result is bit-exact by construction either way.
 #include "device.cuh"
 #include "internal.h"
 
@@ -169,6 +171,94 @@ __global__ void union_kernel(const int32_t* __restrict__ slots, const int32_t* _
   for (int i = total + tid; i < n; i += nthreads) out[i] = -1;
 }
 
+// Dense slot table (caches of at most kDenseUnionSlots rows): the group's members OR their
+// bit into one byte per cache row in shared memory (atomicOr on the 32-bit word holding it),
+// then one ordered scan of the table emits every row whose byte is set, ascending, with the
+// byte as its membership mask. O(G*K + rows / 16) per group instead of a sort of G*K keys;
+// the output is the same union by construction (every live slot sets its member's bit; the
+// scan visits rows in ascending order and emits each set row once).
+constexpr int kDenseThreads = 256;
+
+__device__ __forceinline__ int nonzero_bytes(uint32_t w) {
+  return __popc((((w & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | w) & 0x80808080u);
+}
+
+__global__ void __launch_bounds__(kDenseThreads) union_dense_kernel(const int32_t* __restrict__ slots,
+                                                                   const int32_t* __restrict__ topk_len, int T,
+                                                                   int K, int G, int num_slots,
+                                                                   int32_t* __restrict__ enc,
+                                                                   int32_t* __restrict__ lens, int* status) {
+  extern __shared__ uint4 table4[];  // [chunks] 16 mask bytes each
+  __shared__ int warp_tot[kDenseThreads / 32];
+  uint32_t* table = reinterpret_cast<uint32_t*>(table4);
+  const int g = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int chunks = (num_slots + 15) >> 4;
+  for (int i = tid; i < chunks; i += kDenseThreads) table4[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  // 1. members' bits
+  int err = 0;
+  for (int m = 0; m < G; ++m) {
+    const int t = g * G + m;
+    if (t >= T) break;
+    int len = topk_len ? topk_len[t] : K;
+    len = len < 0 ? 0 : (len > K ? K : len);
+    const int32_t* row = slots + static_cast<long long>(t) * K;
+    const uint32_t bit = 1u << m;
+    for (int j = tid; j < len; j += kDenseThreads) {
+      const int sl = __ldg(row + j);
+      if (sl < 0) continue;
+      if (sl >= num_slots) {
+        err = 1;
+        continue;
+      }
+      atomicOr(table + (sl >> 2), bit << ((sl & 3) * 8));
+    }
+  }
+  if (__any_sync(0xffffffffu, err) && lane == 0) atomicOr(status, SVT_DEV_ERR_INDEX_RANGE);
+  __syncthreads();
+  // 2. ordered scan: thread tid takes chunks [c0, c1); count set rows, block exclusive scan
+  const int per = (chunks + kDenseThreads - 1) / kDenseThreads;
+  const int c0 = min(chunks, tid * per), c1 = min(chunks, c0 + per);
+  int cnt = 0;
+  for (int c = c0; c < c1; ++c) {
+    const uint4 v = table4[c];
+    cnt += nonzero_bytes(v.x) + nonzero_bytes(v.y) + nonzero_bytes(v.z) + nonzero_bytes(v.w);
+  }
+  int incl = cnt;
+  for (int off = 1; off < 32; off <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += u;
+  }
+  if (lane == 31) warp_tot[warp] = incl;
+  __syncthreads();
+  int base = 0, total = 0;
+  for (int w = 0; w < kDenseThreads / 32; ++w) {
+    const int v = warp_tot[w];
+    base += w < warp ? v : 0;
+    total += v;
+  }
+  int pos = base + incl - cnt;
+  const int n = G * K;
+  int32_t* out = enc + static_cast<long long>(g) * n;
+  for (int c = c0; c < c1; ++c) {
+    const uint4 v = table4[c];
+    const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    for (int q = 0; q < 4; ++q) {
+      uint32_t w = w4[q];
+      while (w != 0) {
+        const int b = __ffs(w) - 1;  // lowest set bit: byte b / 8 of the word
+        const int byte = b >> 3;
+        const uint32_t mask = (w >> (byte * 8)) & 0xFFu;
+        w &= ~(0xFFu << (byte * 8));
+        out[pos++] = static_cast<int32_t>((mask << 24) | static_cast<uint32_t>(c * 16 + q * 4 + byte));
+      }
+    }
+  }
+  if (tid == 0) lens[g] = total;
+  // 3. -1 after the union
+  for (int i = total + tid; i < n; i += kDenseThreads) out[i] = -1;
+}
+
 // How many union entries each half of group g (64 packed rows: the members whose rows they
 // are) keeps, i.e. entries with a membership bit of one of those members. The attention
 // kernel walks only those, so the count fixes its number of 64-entry half-tiles.
@@ -230,6 +320,14 @@ cudaError_t launch_union(const int32_t* slots, const int32_t* topk_len, int T, i
                          int32_t* enc, int32_t* lens, int* status, cudaStream_t stream) {
   const int groups = (T + G - 1) / G;
   if (groups == 0) return cudaSuccess;
+  if (num_slots <= kDenseUnionSlots) {
+    const int smem = static_cast<int>((num_slots + 15) / 16 * 16);
+    cudaError_t e = cudaFuncSetAttribute(union_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    union_dense_kernel<<<groups, kDenseThreads, smem, stream>>>(slots, topk_len, T, K, G, static_cast<int>(num_slots),
+                                                                enc, lens, status);
+    return cudaGetLastError();
+  }
   const int npow = next_pow2(G * K);
   int threads = npow / 4;
   threads = threads < 64 ? 64 : (threads > 512 ? 512 : threads);
