@@ -142,6 +142,10 @@ constexpr int kTmemO = 128;  // O^T M-block mb: columns 128 + 64 mb .. + 63
 
 constexpr int kNamedBarSm = 1;
 constexpr int kNamedBarRes = 2;  // the two resolver warps
+// The softmax warps of one 32-column half (warps 4 h .. 4 h + 3, the four TMEM quadrants of
+// those columns) agree on their columns' reference maxima among themselves: barrier 3 + h.
+constexpr int kNamedBarCols = 3;
+constexpr int kColThreads = 128;
 
 // operand type of both contractions: bf16 for a bf16 cache; f16 for an e4m3 cache, whose rows
 // become code x block scale in f16 on the way into shared memory (Q^T and P^T follow)
@@ -858,7 +862,7 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
           "bar.red.or.pred po, %2, %3, pi;\n\t"
           "selp.u32 %0, 1, 0, po;\n\t}"
           : "=r"(any)
-          : "r"(static_cast<uint32_t>(exceed)), "r"(kNamedBarSm), "r"(kSmThreads)
+          : "r"(static_cast<uint32_t>(exceed)), "r"(kNamedBarCols + ch), "r"(kColThreads)
           : "memory");
       if (threadIdx.x == 0) SVT_TRACE_G(9, g);
       if (any) {
@@ -871,17 +875,17 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
           const float m = rows16_column_reduce<true>(v, lane, idx);
           red[warp * 32 + 2 * idx + cp] = m;
         }
-        named_bar_sync(kNamedBarSm, kSmThreads);
-        if (threadIdx.x < kRowsetRows) {
-          const int col = threadIdx.x, h = col >> 5, c = col & 31;
-          const float mt = fmaxf(fmaxf(red[(4 * h + 0) * 32 + c], red[(4 * h + 1) * 32 + c]),
-                                 fmaxf(red[(4 * h + 2) * 32 + c], red[(4 * h + 3) * 32 + c]));
+        named_bar_sync(kNamedBarCols + ch, kColThreads);
+        if (q == 0) {  // one warp per 32 columns: its lane is the column
+          const int col = 32 * ch + lane;
+          const float mt = fmaxf(fmaxf(red[(4 * ch + 0) * 32 + lane], red[(4 * ch + 1) * 32 + lane]),
+                                 fmaxf(red[(4 * ch + 2) * 32 + lane], red[(4 * ch + 3) * 32 + lane]));
           const float mo = m_ref[col];
           const float mn = fmaxf(mo, mt);
           alpha_s[col] = (mo == -CUDART_INF_F) ? 0.f : ex2_approx(mo - mn);
           m_ref[col] = mn;
         }
-        named_bar_sync(kNamedBarSm, kSmThreads);
+        named_bar_sync(kNamedBarCols + ch, kColThreads);
 #pragma unroll
         for (int c = 0; c < 16; ++c) lpart[c] *= alpha_s[32 * ch + 2 * c + cp];
         if (i > 0) {
