@@ -54,6 +54,8 @@ TRAFFIC_BY_SOURCE = {
     # dirty lines evicted by the gather (the decode itself writes 4.2 MB of output)
     "ac42cc583c934f36": (158.648832e6, 60.999424e6, "256 MB write"),
     "6a36a901a86fcc23": (159.517184e6, 58.950400e6, "256 MB write"),
+    # TMA Q^T, bulk-copy cluster merge, column-group softmax barriers
+    "d700b230a6228da8": (159.347712e6, 60.956416e6, "256 MB write"),
 }
 
 
