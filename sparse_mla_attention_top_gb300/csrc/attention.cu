@@ -78,6 +78,7 @@ constexpr int kPvIssuerWarp = 9;  // issues PV
 constexpr int kResWarp0 = 10;
 constexpr int kResThreads = 64;   // warps 10-11: one list entry each
 constexpr int kFillWarp0 = 12;
+
 constexpr int kFillThreads = 128;  // warps 12-15
 constexpr int kFillWarps = kFillThreads / 32;
 constexpr int kHalf = 64;          // KV rows per half-tile
@@ -165,7 +166,8 @@ constexpr int kDeadEntry = -2147483647 - 1;  // an entry past the list's live co
 // channels combined. Per half-tile g:
 // 0 S^T buffer free, 1 rows landed, 2 S^T issued, 3 S^T done (softmax), 4 P^T written,
 // 5 PV issued, 6 slots ready (filler), 7 fill issued, 8 softmax has S^T in registers, 9 the
-// softmax warps agreed on the maxima, 10 P^T stored (before the proxy fence).
+// softmax warps agreed on the maxima, 10 P^T stored (before the proxy fence), 11 the S^T
+// issuer past its fences.
 #ifdef SVT_PHASE_TRACE
 __device__ __forceinline__ void trace_at(const AttnParams& p, int slot, unsigned long long v) {
   if (p.trace != nullptr) p.trace[static_cast<long long>(blockIdx.x) * kTraceSlots + slot] = v;
@@ -278,11 +280,20 @@ struct SegWalk {
 // Prefill: which query columns of 32-column half h of row-set half `rpar` a KV row is live
 // for, given its membership bits mk. Column c is packed row 64 rpar + 32 h + c, member
 // (64 rpar + 32 h + c) / H (H >= 16, so a half spans at most two members).
-__device__ __forceinline__ uint32_t live_columns(uint32_t mk, int rpar, int h, int H) {
+struct LiveCols {
+  int lo, hi;         // the members of the first and the last of the 32 columns
+  uint32_t split_hi;  // the columns that belong to member hi when it differs from lo
+};
+__device__ __forceinline__ LiveCols live_cols_of(int rpar, int h, int H) {
   const int packed0 = rpar * kRowsetRows + 32 * h;
-  const int lo = packed0 / H, hi = (packed0 + 31) / H;
-  const uint32_t split_hi = (hi != lo) ? (0xFFFFFFFFu << (H - (packed0 - lo * H))) : 0u;
-  return (((mk >> lo) & 1u) ? ~split_hi : 0u) | (((mk >> hi) & 1u) ? split_hi : 0u);
+  LiveCols c;
+  c.lo = packed0 / H;
+  c.hi = (packed0 + 31) / H;
+  c.split_hi = (c.hi != c.lo) ? (0xFFFFFFFFu << (H - (packed0 - c.lo * H))) : 0u;
+  return c;
+}
+__device__ __forceinline__ uint32_t live_columns(uint32_t mk, const LiveCols& c) {
+  return (((mk >> c.lo) & 1u) ? ~c.split_hi : 0u) | (((mk >> c.hi) & 1u) ? c.split_hi : 0u);
 }
 
 // Column reduction over the 16 rows a warp holds in the .16x64b layout: v[i] is column
@@ -335,6 +346,13 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
     const int32_t* list = p.topk + static_cast<long long>(t) * p.K;
     const int len_raw = p.topk_len ? __ldg(p.topk_len + t) : p.K;
     if (has_table) req = p.req_of_token ? __ldg(p.req_of_token + t) : t;
+    if (has_table && p.req_of_token == nullptr && ltid == 0 && t < p.num_reqs) {
+      // the request's block-table row heads for L2 beside the entries' first read, so that the
+      // dependent page-word reads below find it there
+      const int32_t* row = p.block_table + static_cast<long long>(t) * p.max_blocks;
+      const uint32_t bytes = static_cast<uint32_t>(min(p.max_blocks, 16384)) * 4u & ~15u;
+      if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0 && bytes >= 16u) prefetch_l2_bulk(row, bytes);
+    }
     int raw = e0 < p.K ? __ldg(list + e0) : kDeadEntry;
     SegWalk::with_len(s, len_raw < 0 ? 0 : (len_raw > p.K ? p.K : len_raw), te);
     if (s.n == 0) continue;
@@ -720,6 +738,7 @@ __device__ void s_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem,
       SVT_TRACE_G(1, g);
       fence_proxy_async_smem();  // cp.async data (generic proxy) -> MMA operand reads
       tc_fence_after();
+      SVT_TRACE_G(11, g);
       const uint32_t stage = sbase + kOffStage + b * kStageBytes;
 #pragma unroll 1
       for (int kb = 0; kb < kBlocks; ++kb) {
@@ -802,6 +821,7 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
   while (walk.next(p, s)) {
     const int nh = s.n;
     const int rpar = s.r & 1;
+    const LiveCols lcols = decode ? LiveCols{0, 0, 0u} : live_cols_of(rpar, ch, p.H);  // per segment
     if constexpr (kF16) {
       if (nh > 0) {
         // the segment's Q^T (bf16, as it landed) becomes f16 in place for the f16 contractions
@@ -840,7 +860,7 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
         const uint32_t mk = mask_tab[k];
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kBarSlotFree + e));  // the ring entry is read
-        const uint32_t live = slot < 0 ? 0u : (decode ? 0xFFFFFFFFu : live_columns(mk, rpar, ch, p.H) >> cp);
+        const uint32_t live = slot < 0 ? 0u : (decode ? 0xFFFFFFFFu : live_columns(mk, lcols) >> cp);
         tmem_ld_wait();
         if (threadIdx.x == 0) SVT_TRACE_G(8, g);
 #pragma unroll
