@@ -163,7 +163,7 @@ constexpr int kDeadEntry = -2147483647 - 1;  // an entry past the list's live co
 // done, 9 end, 10 fillers have their first segment, 11 first list entry read (resolvers),
 // 12 S^T issuer sees the first Q^T, 13 cluster merge: LSEs exchanged, 14 half-tiles walked (a
 // count), 15 end (%globaltimer), 16 cluster merge: messages sent, 17 messages received, 18 own
-// channels combined. Per half-tile g:
+// channels combined, 19 the first slot computed (resolvers), 20 the second half-tile's slots. Per half-tile g:
 // 0 S^T buffer free, 1 rows landed, 2 S^T issued, 3 S^T done (softmax), 4 P^T written,
 // 5 PV issued, 6 slots ready (filler), 7 fill issued, 8 softmax has S^T in registers, 9 the
 // softmax warps agreed on the maxima, 10 P^T stored (before the proxy fence), 11 the S^T
@@ -392,8 +392,15 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
         }
         slot = slot_of(raw, phys, rc, has_table, p.max_blocks, p.page_size, p.num_pages, &err);
       }
+#ifdef SVT_PHASE_TRACE
+      if (k == 0 && ltid == 0) {
+        asm volatile("" ::"r"(slot));  // after the page word (and the request's length) arrived
+        SVT_TRACE(19);
+      }
+#endif
       // the row is wanted a few half-tiles from now: start its trip from HBM into L2 here, so
-      // that the fill, when its stage frees, waits for L2 rather than for DRAM
+      // that the fill, when its stage frees, waits for L2 rather than for DRAM (even the first
+      // half-tile's: its 16-byte copies fetch faster from lines already on their way to L2)
       if (slot >= 0)
         prefetch_l2_bulk(p.kv + static_cast<long long>(slot) * p.row_stride, kF16 ? kRowBytesFp8 : kRowBytesBf16);
       const uint32_t e = k % kSlotRing;
@@ -405,6 +412,7 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
       mask_tab[e * kHalf + ltid] = mask;
       mbar_arrive(bar(kBarSlotsReady + e));
       if (k == 0 && ltid == 0) SVT_TRACE(4);
+      if (k == 1 && ltid == 0) SVT_TRACE(20);
       raw = raw_next;
     }
   }
