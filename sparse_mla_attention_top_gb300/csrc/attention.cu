@@ -354,6 +354,17 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
       if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0 && bytes >= 16u) prefetch_l2_bulk(row, bytes);
     }
     int raw = e0 < p.K ? __ldg(list + e0) : kDeadEntry;
+    // the request's block-table row and length: its length read goes out before anything waits
+    // for the entry, so that the page-word read below is the only one left on the way to the
+    // slot (with the identity request map it travels with the first round)
+    ReqContext rc{nullptr, INT_MAX, true};
+    if (has_table) {
+      rc.ok = req >= 0 && req < p.num_reqs;
+      if (rc.ok) {
+        rc.bt_row = p.block_table + static_cast<long long>(req) * p.max_blocks;
+        if (p.seq_lens != nullptr) rc.seq_len = __ldg(p.seq_lens + req);
+      }
+    }
     SegWalk::with_len(s, len_raw < 0 ? 0 : (len_raw > p.K ? p.K : len_raw), te);
     if (s.n == 0) continue;
     if (e0 >= s.len) raw = kDeadEntry;
@@ -363,15 +374,6 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
       SVT_TRACE(11);
     }
 #endif
-    // the request's block-table row and length (second round, with the page reads below)
-    ReqContext rc{nullptr, INT_MAX, true};
-    if (has_table) {
-      rc.ok = req >= 0 && req < p.num_reqs;
-      if (rc.ok) {
-        rc.bt_row = p.block_table + static_cast<long long>(req) * p.max_blocks;
-        if (p.seq_lens != nullptr) rc.seq_len = __ldg(p.seq_lens + req);
-      }
-    }
     auto entry = [&](int i) -> int {
       const int e = (s.i0 + i) * kHalf + ltid;
       return e < s.len ? __ldg(list + e) : kDeadEntry;
