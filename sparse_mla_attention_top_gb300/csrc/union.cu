@@ -185,7 +185,7 @@ __device__ __forceinline__ int nonzero_bytes(uint32_t w) {
 
 __global__ void __launch_bounds__(kDenseThreads) union_dense_kernel(const int32_t* __restrict__ slots,
                                                                    const int32_t* __restrict__ topk_len, int T,
-                                                                   int K, int G, int num_slots,
+                                                                   int K, int G, int num_slots, int vec,
                                                                    int32_t* __restrict__ enc,
                                                                    int32_t* __restrict__ lens, int* status) {
   extern __shared__ uint4 table4[];  // [chunks] 16 mask bytes each
@@ -195,8 +195,17 @@ __global__ void __launch_bounds__(kDenseThreads) union_dense_kernel(const int32_
   const int chunks = (num_slots + 15) >> 4;
   for (int i = tid; i < chunks; i += kDenseThreads) table4[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
-  // 1. members' bits
+  // 1. members' bits. With vec (K a multiple of 4, slots 16-byte aligned) a thread takes four
+  //    entries per 16-byte load, two loads in flight, before its atomics.
   int err = 0;
+  auto mark = [&](int sl, uint32_t bit) {
+    if (sl < 0) return;
+    if (sl >= num_slots) {
+      err = 1;
+      return;
+    }
+    atomicOr(table + (sl >> 2), bit << ((sl & 3) * 8));
+  };
   for (int m = 0; m < G; ++m) {
     const int t = g * G + m;
     if (t >= T) break;
@@ -204,15 +213,19 @@ __global__ void __launch_bounds__(kDenseThreads) union_dense_kernel(const int32_
     len = len < 0 ? 0 : (len > K ? K : len);
     const int32_t* row = slots + static_cast<long long>(t) * K;
     const uint32_t bit = 1u << m;
-    for (int j = tid; j < len; j += kDenseThreads) {
-      const int sl = __ldg(row + j);
-      if (sl < 0) continue;
-      if (sl >= num_slots) {
-        err = 1;
-        continue;
+    int j0 = 0;
+    if (vec) {
+      const int4* row4 = reinterpret_cast<const int4*>(row);
+      const int n4 = len >> 2;
+      for (int i = tid; i < n4; i += 2 * kDenseThreads) {
+        const int4 a = __ldg(row4 + i);
+        const int4 b = i + kDenseThreads < n4 ? __ldg(row4 + i + kDenseThreads) : make_int4(-1, -1, -1, -1);
+        mark(a.x, bit), mark(a.y, bit), mark(a.z, bit), mark(a.w, bit);
+        mark(b.x, bit), mark(b.y, bit), mark(b.z, bit), mark(b.w, bit);
       }
-      atomicOr(table + (sl >> 2), bit << ((sl & 3) * 8));
+      j0 = n4 << 2;
     }
+    for (int j = j0 + tid; j < len; j += kDenseThreads) mark(__ldg(row + j), bit);
   }
   if (__any_sync(0xffffffffu, err) && lane == 0) atomicOr(status, SVT_DEV_ERR_INDEX_RANGE);
   __syncthreads();
@@ -324,8 +337,9 @@ cudaError_t launch_union(const int32_t* slots, const int32_t* topk_len, int T, i
     const int smem = static_cast<int>((num_slots + 15) / 16 * 16);
     cudaError_t e = cudaFuncSetAttribute(union_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    const int vec = (K % 4 == 0 && (reinterpret_cast<uintptr_t>(slots) & 15) == 0) ? 1 : 0;
     union_dense_kernel<<<groups, kDenseThreads, smem, stream>>>(slots, topk_len, T, K, G, static_cast<int>(num_slots),
-                                                                enc, lens, status);
+                                                                vec, enc, lens, status);
     return cudaGetLastError();
   }
   const int npow = next_pow2(G * K);
