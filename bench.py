@@ -56,6 +56,8 @@ TRAFFIC_BY_SOURCE = {
     "6a36a901a86fcc23": (159.517184e6, 58.950400e6, "256 MB write"),
     # TMA Q^T, bulk-copy cluster merge, column-group softmax barriers
     "d700b230a6228da8": (159.347712e6, 60.956416e6, "256 MB write"),
+    # the same with the resolvers' first-round length read and the softmax's per-segment bounds
+    "4ff596103d408444": (159.387392e6, 60.962304e6, "256 MB write"),
 }
 
 
@@ -74,6 +76,8 @@ def parse():
     ap.add_argument("--prefill-T", type=int, default=8192)
     ap.add_argument("--phase-trace", action="store_true",
                     help="build the phase-trace library and print per-phase times of the attention kernel")
+    ap.add_argument("--item", choices=["decode_fp8", "decode_mixed", "prefill", "prefill_mixed", "prefill_fp8"],
+                    help="run that one line item alone and print it (for profiling one workload)")
     return ap.parse_args()
 
 
@@ -647,6 +651,30 @@ def run_phase_trace(args):
     print(json.dumps(res), flush=True)
 
 
+def run_item(args):
+    """One line item alone (same timing as in the full run), printed as {item: {...}}."""
+    import torch
+
+    import sparse_mla_attention_top_gb300 as S
+    from sparse_mla_attention_top_gb300 import build as B
+    from sparse_mla_attention_top_gb300 import workloads as W
+
+    B.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    hbm_peak, bf16_peak, _, _ = peaks()
+    flush = Flusher(dev)
+    if args.item.startswith("decode"):
+        w = W.decode_fp8_batch() if args.item == "decode_fp8" else W.mixed_decode()
+        item = public(bench_decode(S, w, dev, stream, flush, args.steps, args.warmup, hbm_peak))
+    else:
+        pw = {"prefill": W.grouped_prefill, "prefill_mixed": W.mixed_prefill,
+              "prefill_fp8": W.grouped_prefill_fp8}[args.item](args.prefill_T)
+        item = bench_prefill(S, pw, dev, stream, flush, args.steps, args.warmup, bf16_peak)
+    print(json.dumps({args.item: item}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -654,6 +682,9 @@ def main():
         return
     if args.phase_trace:
         run_phase_trace(args)
+        return
+    if args.item:
+        run_item(args)
         return
     import torch
 
