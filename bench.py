@@ -76,7 +76,8 @@ def parse():
     ap.add_argument("--prefill-T", type=int, default=8192)
     ap.add_argument("--phase-trace", action="store_true",
                     help="build the phase-trace library and print per-phase times of the attention kernel")
-    ap.add_argument("--item", choices=["decode_fp8", "decode_mixed", "prefill", "prefill_mixed", "prefill_fp8"],
+    ap.add_argument("--item", choices=["decode_fp8", "decode_mixed", "prefill", "prefill_mixed", "prefill_fp8",
+                                       "tensor_probe"],
                     help="run that one line item alone and print it (for profiling one workload)")
     return ap.parse_args()
 
@@ -500,6 +501,41 @@ def bench_probe(S, w, d, dev, stream, flush, steps, hbm_peak):
     return res
 
 
+# one 64-row half-tile's contractions: S^T (64 x 64 x 576) and PV (512 x 64 x 64), 2 flops per MAC
+HALF_TILE_FLOP = 2 * 64 * 64 * (576 + 512)
+
+
+def bench_tensor_probe(S, dev, stream, flush, steps, bf16_peak, reps=400):
+    """One half-tile's MMA group of the attention kernels, `reps` times on one CTA per SM,
+    with nothing else running: the contractions' own cost, the ceiling the grouped prefill's
+    half-tiles run against."""
+    import torch
+
+    rng = np.random.default_rng(12)
+    mk = lambda shape: torch.from_numpy(rng.standard_normal(shape).astype(np.float32)).to(torch.bfloat16).to(dev)  # noqa: E731
+    k_rows, q = mk((64, 576)), mk((64, 576))
+    pt = torch.from_numpy(rng.random((64, 64)).astype(np.float32)).to(torch.bfloat16).to(dev)
+    grid = torch.cuda.get_device_properties(dev).multi_processor_count
+    ws = S.Workspace(dev)
+    box = {}
+
+    def step():
+        box["r"] = S.tensor_probe(k_rows, q, pt, reps=reps, grid=grid, ws=ws)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    t = time_steps(step, steps, flush, stream)
+    assert ws.read_status() == 0
+    ms = statistics.median(t)
+    cycles = box["r"][2].cpu().numpy()
+    us_half = ms * 1e3 / reps
+    tflops = grid * HALF_TILE_FLOP * reps / (ms / 1e3) / 1e12
+    return {"grid": grid, "reps": reps, "ms": ms, "us_per_half_tile": us_half,
+            "cycles_per_half_tile_median": float(np.median(cycles)) / reps,
+            "mflop_per_half_tile": HALF_TILE_FLOP / 1e6, "tflops": tflops, "frac_of_bf16_peak": tflops / bf16_peak}
+
+
 def bench_topk(S, W, dev, stream, flush, steps, warmup, hbm_peak, T):
     import torch
 
@@ -668,6 +704,8 @@ def run_item(args):
     if args.item.startswith("decode"):
         w = W.decode_fp8_batch() if args.item == "decode_fp8" else W.mixed_decode()
         item = public(bench_decode(S, w, dev, stream, flush, args.steps, args.warmup, hbm_peak))
+    elif args.item == "tensor_probe":
+        item = bench_tensor_probe(S, dev, stream, flush, args.steps, bf16_peak)
     else:
         pw = {"prefill": W.grouped_prefill, "prefill_mixed": W.mixed_prefill,
               "prefill_fp8": W.grouped_prefill_fp8}[args.item](args.prefill_T)
@@ -770,6 +808,8 @@ def main():
     if not args.no_topk:
         items["topk"] = bench_topk(S, W, dev, stream, flush, psteps, args.warmup, hbm_peak, args.decode_T)
     if not args.no_prefill:
+        tp = bench_tensor_probe(S, dev, stream, flush, psteps, bf16_peak)
+        items["tensor_probe"] = tp
         items["prefill"] = bench_prefill(S, W.grouped_prefill(args.prefill_T), dev, stream, flush, psteps,
                                          args.warmup, bf16_peak)
         if not args.no_items:
@@ -777,6 +817,10 @@ def main():
                                                    args.warmup, bf16_peak)
             items["prefill_fp8"] = bench_prefill(S, W.grouped_prefill_fp8(args.prefill_T), dev, stream, flush,
                                                  psteps, args.warmup, bf16_peak)
+        # the prefill's executed rate against the same half-tiles' MMAs with nothing else running
+        for key in ("prefill", "prefill_mixed", "prefill_fp8"):
+            if key in items:
+                items[key]["frac_of_tensor_probe"] = items[key]["tflops_executed"] / tp["tflops"]
 
     # one clock record over every timed region above and the short warm-ups between them: a
     # single region is too short for more than one NVML sample

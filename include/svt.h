@@ -294,6 +294,32 @@ SVT_API svt_status svt_topk_select(const float* scores, int32_t T, int32_t N, in
 SVT_API svt_status svt_gather_probe(const svt_kv_cache* kv, const int32_t* slots, int64_t n, int32_t mode,
                                     uint32_t* row_xor, void* ws, size_t ws_bytes, svt_stream_t stream);
 
+/*
+ * Tensor probe, a measurement tool rather than a step of the method: the contractions of one
+ * 64-row half-tile of the attention kernels (S^T = K Q^T over the 576 channels, then
+ * O^T += V^T P^T over the 512 latent channels; "The Virtual Block Table", The Breakthrough:
+ * a query's scores against its gathered rows, then the weighted sum of the rows' latent
+ * part), as the kernels issue them: 36 tcgen05 MMAs of M = 64, N = 64, K = 16 and 16 of
+ * M = 128, N = 64, K = 16, operands in 128-byte swizzled shared memory, accumulators in
+ * tensor memory. One thread per CTA issues the group `reps` times back to back, so that the
+ * contractions' own cost per half-tile can be measured next to the kernels'.
+ *   k_rows  [64, 576] bf16 row-major (64 cache rows; V is their first 512 channels).
+ *   q       [64, 576] bf16 row-major (64 query rows).
+ *   pt      [64, 64] bf16: P^T, row = cache row, column = query row.
+ *   reps    1 .. 1000000; grid 1 .. 4096 CTAs (one per SM at most: 153 KB of shared memory each).
+ *   s_out   [64, 64] fp32: S^T of CTA 0 (row = cache row, column = query row), rewritten each
+ *           repetition.
+ *   o_out   [512, 64] fp32: O^T of CTA 0 (row = channel), accumulated over the repetitions:
+ *           reps * V^T P^T.
+ *   cycles  [grid] int64: clock64 cycles from the first MMA's issue to the last one's
+ *           completion, per CTA (-1 when the wait gave up).
+ * All arrays are device memory owned by the caller; inputs 16-byte aligned. Workspace: the
+ * 256-byte status header (MMAs not done within 2 s set SVT_DEV_ERR_TIMEOUT).
+ */
+SVT_API svt_status svt_tensor_probe(const void* k_rows_bf16, const void* q_bf16, const void* pt_bf16, int32_t reps,
+                                    int32_t grid, float* s_out, float* o_out, int64_t* cycles, void* ws,
+                                    size_t ws_bytes, svt_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -19,5 +19,6 @@ from .svt import (  # noqa: F401
     resolve_topk_slots,
     sparse_mla_decode,
     sparse_mla_prefill_grouped,
+    tensor_probe,
     topk_select,
 )

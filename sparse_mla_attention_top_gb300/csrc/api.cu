@@ -504,6 +504,26 @@ svt_status svt_gather_probe(const svt_kv_cache* kv, const int32_t* slots, int64_
   return SVT_OK;
 }
 
+svt_status svt_tensor_probe(const void* k_rows_bf16, const void* q_bf16, const void* pt_bf16, int32_t reps,
+                            int32_t grid, float* s_out, float* o_out, int64_t* cycles, void* ws, size_t ws_bytes,
+                            svt_stream_t stream) {
+  if (reps < 1 || reps > 1000000) return fail(SVT_ERR_INVALID_ARG, "reps must be in [1, 1000000], got %d", reps);
+  if (grid < 1 || grid > 4096) return fail(SVT_ERR_INVALID_ARG, "grid must be in [1, 4096], got %d", grid);
+  svt_status st = check_ws(ws, ws_bytes, svt::kStatusBytes);
+  if (st != SVT_OK) return st;
+  if (k_rows_bf16 == nullptr || q_bf16 == nullptr || pt_bf16 == nullptr || s_out == nullptr || o_out == nullptr ||
+      cycles == nullptr)
+    return fail(SVT_ERR_INVALID_ARG, "null array argument");
+  if (!aligned(k_rows_bf16, 16) || !aligned(q_bf16, 16) || !aligned(pt_bf16, 16))
+    return fail(SVT_ERR_INVALID_ARG, "k_rows, q and pt must be 16-byte aligned");
+  cudaError_t e = svt::launch_tensor_probe(
+      static_cast<const uint16_t*>(k_rows_bf16), static_cast<const uint16_t*>(q_bf16),
+      static_cast<const uint16_t*>(pt_bf16), reps, grid, s_out, o_out, reinterpret_cast<long long*>(cycles),
+      static_cast<int*>(ws), reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "tensor probe launch");
+  return SVT_OK;
+}
+
 svt_status svt_topk_select(const float* scores, int32_t T, int32_t N, int64_t stride, const int32_t* lens, int32_t K,
                            int32_t* topk_out, svt_stream_t stream) {
   if (T < 0 || N < 0) return fail(SVT_ERR_INVALID_ARG, "T and N must be >= 0");

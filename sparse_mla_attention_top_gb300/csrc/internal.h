@@ -166,6 +166,11 @@ cudaError_t launch_gather_probe(const uint8_t* kv, long long row_stride, int row
                                 const int32_t* slots, long long n, int mode, uint32_t* out, int* timed_out,
                                 cudaStream_t stream);
 
+// One half-tile's S^T and PV MMA group of the attention kernel, reps times per CTA on grid
+// CTAs; CTA 0 writes S^T [64, 64] and O^T [512, 64] (fp32), every CTA its clock64 cycles.
+cudaError_t launch_tensor_probe(const uint16_t* k_rows, const uint16_t* q, const uint16_t* pt, int reps, int grid,
+                                float* s_out, float* o_out, long long* cycles, int* status, cudaStream_t stream);
+
 // Decode and grouped prefill over either cache dtype (two shared-memory stages of 64-row
 // half-tiles; decode work units are half-tiles).
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);

@@ -194,7 +194,139 @@ __global__ void __launch_bounds__(kPThreads) gather_probe_regs(const uint8_t* __
   }
 }
 
+// ---------------------------------------------------------------------------------- tensor probe
+// One half-tile's contractions of the attention kernel, with nothing else running: S^T = K Q^T
+// as 9 blocks x 4 MMAs of M = 64, N = 64, K = 16 (K rows and Q^T K-major), then PV as 4
+// M-blocks x 4 MMAs of M = 128, N = 64, K = 16 (V^T and P^T MN-major), in the kernel's 128-byte
+// swizzled 8 KB blocks, issued `reps` times back to back by one thread per CTA. S^T is
+// rewritten each repetition, O^T accumulates over all of them.
+constexpr int kTThreads = 128;
+constexpr int kTBlk = 8192;                // 64 rows x 128 B
+constexpr int kTOffK = 0;                  // K rows: 9 blocks
+constexpr int kTOffQ = 9 * kTBlk;          // Q^T: 9 blocks
+constexpr int kTOffP = 18 * kTBlk;         // P^T: 1 block
+constexpr int kTSmem = 19 * kTBlk + 1024;  // + alignment
+constexpr uint32_t kTIdescS = idesc_f32acc(64, 64, 0, 0, kFmtBf16);
+constexpr uint32_t kTIdescPV = idesc_f32acc(128, 64, 1, 1, kFmtBf16);
+constexpr uint32_t kTTmemS = 0, kTTmemO = 128;
+
+// rows x (cols / 8) 16-byte chunks of a row-major bf16 matrix into swizzled 8 KB blocks of 64
+// columns each (block b holds columns 64 b ..)
+__device__ __forceinline__ void stage_bf16(uint8_t* dst, const uint16_t* src, int cols) {
+  const int chunks = cols / 8;
+  for (int j = threadIdx.x; j < 64 * chunks; j += kTThreads) {
+    const int r = j / chunks, c = j - r * chunks;
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + static_cast<size_t>(r) * cols) + c);
+    *reinterpret_cast<uint4*>(dst + (c >> 3) * kTBlk + sw128_offset(r, c & 7)) = v;
+  }
+}
+
+__global__ void __launch_bounds__(kTThreads, 1) tensor_probe_kernel(const uint16_t* __restrict__ k_rows,
+                                                                      const uint16_t* __restrict__ q,
+                                                                      const uint16_t* __restrict__ pt, int reps,
+                                                                      float* __restrict__ s_out,
+                                                                      float* __restrict__ o_out,
+                                                                      long long* __restrict__ cycles, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) uint64_t done;
+  __shared__ uint32_t tmem_slot;
+  stage_bf16(smem + kTOffK, k_rows, 576);
+  stage_bf16(smem + kTOffQ, q, 576);
+  stage_bf16(smem + kTOffP, pt, 64);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&done), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (threadIdx.x < 32) {
+    tmem_alloc(smem_u32(&tmem_slot), 512);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();  // the staged operands (generic proxy) -> MMA reads
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t base = smem_u32(smem);
+  if (threadIdx.x == 0) {
+    const long long t0 = clock64();
+    for (int rep = 0; rep < reps; ++rep) {
+#pragma unroll 1
+      for (int kb = 0; kb < 9; ++kb) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma_f16(tmem + kTTmemS, smem_desc_sw128(base + kTOffK + kb * kTBlk + ks * 32, 16, 1024),
+                   smem_desc_sw128(base + kTOffQ + kb * kTBlk + ks * 32, 16, 1024), kTIdescS, (kb | ks) != 0);
+      }
+#pragma unroll
+      for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma_f16(tmem + kTTmemO + 64 * mb, smem_desc_sw128(base + kTOffK + 2 * mb * kTBlk + ks * 2048, kTBlk, 1024),
+                   smem_desc_sw128(base + kTOffP + ks * 2048, kTBlk, 1024), kTIdescPV, (rep > 0 || ks > 0) ? 1u : 0u);
+      }
+    }
+    umma_commit(smem_u32(&done));
+    const uint64_t g0 = globaltimer();
+    bool ok = true;
+    while (!mbar_try_wait(smem_u32(&done), 0)) {
+      if (globaltimer() - g0 > kPWaitNs) {
+        ok = false;
+        atomicOr(status, SVT_DEV_ERR_TIMEOUT);
+        break;
+      }
+    }
+    cycles[blockIdx.x] = ok ? clock64() - t0 : -1;
+    if (!ok) {  // one more bounded wait: no MMA may still run when TMEM is released
+      const uint64_t g1 = globaltimer();
+      while (!mbar_test_wait(smem_u32(&done), 0) && globaltimer() - g1 < kPWaitNs) {
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (blockIdx.x == 0) {
+    const int q4 = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+    // O^T: thread (quadrant q4, lane) holds channel 128 mb + 32 q4 + lane
+#pragma unroll 1
+    for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + kTTmemO + 64 * mb + 32 * h, o);
+        tmem_ld_wait();
+        float* dst = o_out + static_cast<size_t>(128 * mb + 32 * q4 + lane) * 64 + 32 * h;
+        for (int c = 0; c < 32; ++c) dst[c] = __uint_as_float(o[c]);
+      }
+    }
+    // S^T (M = 64: rows in lanes 0-15 of each quadrant): KV row 16 q4 + (lane >> 2) + 8 (lane & 1),
+    // columns 32 h + 2 i + ((lane >> 1) & 1)
+    const int row = 16 * q4 + (lane >> 2) + 8 * (lane & 1), cpar = (lane >> 1) & 1;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+      uint32_t v[16];
+      tmem_ld_16x64b_x16(lane_base + kTTmemS + 32 * h, v);
+      tmem_ld_wait();
+      for (int i = 0; i < 16; ++i) s_out[row * 64 + 32 * h + 2 * i + cpar] = __uint_as_float(v[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x < 32) tmem_dealloc(tmem, 512);
+}
+
 }  // namespace
+
+cudaError_t launch_tensor_probe(const uint16_t* k_rows, const uint16_t* q, const uint16_t* pt, int reps, int grid,
+                                float* s_out, float* o_out, long long* cycles, int* status, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(tensor_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTSmem);
+  if (e != cudaSuccess) return e;
+  tensor_probe_kernel<<<grid, kTThreads, kTSmem, stream>>>(k_rows, q, pt, reps, s_out, o_out, cycles, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_gather_probe(const uint8_t* kv, long long row_stride, int row_bytes, long long num_slots,
                                 const int32_t* slots, long long n, int mode, uint32_t* out, int* timed_out,

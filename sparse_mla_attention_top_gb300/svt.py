@@ -34,7 +34,7 @@ EXPORTED = [
     "svt_build_group_union_workspace_size", "svt_build_group_union",
     "svt_sparse_mla_prefill_grouped_workspace_size", "svt_sparse_mla_prefill_grouped", "svt_merge_splits",
     "svt_topk_select",
-    "svt_sparse_mla_decode_noalloc", "svt_debug_pipeline_fault", "svt_gather_probe",
+    "svt_sparse_mla_decode_noalloc", "svt_debug_pipeline_fault", "svt_gather_probe", "svt_tensor_probe",
 ]
 
 
@@ -92,6 +92,7 @@ def lib():
                                                     P, P, i32, P, P]
         L.svt_debug_pipeline_fault.argtypes = [i32, i64]
         L.svt_gather_probe.argtypes = [ctypes.POINTER(_KV), P, i64, i32, P, P, sz, P]
+        L.svt_tensor_probe.argtypes = [P, P, P, i32, i32, P, P, P, P, sz, P]
         _lib = L
     return _lib
 
@@ -306,3 +307,20 @@ def gather_probe(kv: KVCache, slots, mode: int = 0, *, out=None, ws: Optional[Wo
     _check(lib().svt_gather_probe(ctypes.byref(kvc), _ptr(slots), n, int(mode), _ptr(out), ws.ptr, ws.nbytes,
                                   _stream()), "svt_gather_probe")
     return out
+
+
+def tensor_probe(k_rows, q, pt, reps: int = 1, grid: int = 1, *, ws: Optional[Workspace] = None):
+    """Issues one half-tile's S^T and PV MMA group of the attention kernels `reps` times on
+    `grid` CTAs (svt_tensor_probe). k_rows, q: [64, 576] bf16; pt: [64, 64] bf16 (P^T).
+    Returns (S^T [64, 64] fp32, O^T [512, 64] fp32 = reps * V^T P^T, cycles [grid] int64)."""
+    for name, t, shape in (("k_rows", k_rows, (64, 576)), ("q", q, (64, 576)), ("pt", pt, (64, 64))):
+        if t.dtype != torch.bfloat16 or tuple(t.shape) != shape or not t.is_contiguous() or not t.is_cuda:
+            raise SvtError(f"{name} must be a contiguous CUDA bf16 tensor of shape {shape}")
+    dev = k_rows.device
+    s_out = torch.empty((64, 64), dtype=torch.float32, device=dev)
+    o_out = torch.empty((512, 64), dtype=torch.float32, device=dev)
+    cycles = torch.empty((int(grid),), dtype=torch.int64, device=dev)
+    ws = default_workspace() if ws is None else ws
+    _check(lib().svt_tensor_probe(_ptr(k_rows), _ptr(q), _ptr(pt), int(reps), int(grid), _ptr(s_out), _ptr(o_out),
+                                  _ptr(cycles), ws.ptr, ws.nbytes, _stream()), "svt_tensor_probe")
+    return s_out, o_out, cycles

@@ -164,3 +164,16 @@ def test_debug_pipeline_fault_checks_its_arguments(L):
     assert L.svt_debug_pipeline_fault(0, -1) == svt.SVT_ERR_INVALID_ARG
     assert L.svt_debug_pipeline_fault(1, 1000) == svt.SVT_OK
     assert L.svt_debug_pipeline_fault(0, 0) == svt.SVT_OK  # back to ordinary behaviour
+
+
+def test_tensor_probe_checks_its_arguments(L):
+    P = ctypes.c_void_p
+    a, b, c, s, o, cyc = (P(0x20000 + 0x10000 * i) for i in range(6))
+    assert L.svt_tensor_probe(a, b, c, 0, 1, s, o, cyc, WS, 256, None) == svt.SVT_ERR_INVALID_ARG  # reps 0
+    assert L.svt_tensor_probe(a, b, c, 1, 0, s, o, cyc, WS, 256, None) == svt.SVT_ERR_INVALID_ARG  # grid 0
+    assert L.svt_tensor_probe(a, b, c, 1, 4097, s, o, cyc, WS, 256, None) == svt.SVT_ERR_INVALID_ARG
+    assert L.svt_tensor_probe(None, b, c, 1, 1, s, o, cyc, WS, 256, None) == svt.SVT_ERR_INVALID_ARG
+    assert L.svt_tensor_probe(a, b, c, 1, 1, s, None, cyc, WS, 256, None) == svt.SVT_ERR_INVALID_ARG
+    assert L.svt_tensor_probe(P(0x20008), b, c, 1, 1, s, o, cyc, WS, 256, None) == svt.SVT_ERR_INVALID_ARG
+    assert "aligned" in _err(L)
+    assert L.svt_tensor_probe(a, b, c, 1, 1, s, o, cyc, WS, 16, None) != svt.SVT_OK  # workspace too small

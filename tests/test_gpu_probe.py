@@ -44,3 +44,29 @@ def test_gather_probe_reads_every_row(S, mode, kv_dtype):
     live = (slots >= 0) & (slots < w.num_slots)
     want[live] = np.bitwise_xor.reduce(words[slots[live]], axis=1)
     assert np.array_equal(got.cpu().numpy().view(np.uint32), want)
+
+
+def _bf16_matrix(rng, shape, scale=1.0):
+    return torch.from_numpy((rng.standard_normal(shape) * scale).astype(np.float32)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("reps,grid", [(1, 1), (3, 1), (5, 4)])
+def test_tensor_probe_computes_the_half_tile_contractions(S, reps, grid):
+    # S^T = K Q^T over 576 channels and O^T = reps * V^T P^T over the 512 latent channels,
+    # against fp64 sums of the same bf16 values (fp32 accumulation in the tensor cores)
+    dev = torch.device("cuda", 0)
+    rng = np.random.default_rng(40 + reps)
+    k_rows = _bf16_matrix(rng, (64, 576))
+    q = _bf16_matrix(rng, (64, 576))
+    pt = torch.from_numpy(rng.random((64, 64)).astype(np.float32)).to(torch.bfloat16)
+    ws = S.Workspace(dev)
+    s_t, o_t, cycles = S.tensor_probe(k_rows.to(dev), q.to(dev), pt.to(dev), reps=reps, grid=grid, ws=ws)
+    torch.cuda.synchronize()
+    assert ws.read_status() == 0
+    kf, qf, pf = (t.float().double().numpy() for t in (k_rows, q, pt))
+    want_s = kf @ qf.T
+    want_o = reps * (kf[:, :512].T @ pf)
+    assert np.max(np.abs(s_t.cpu().numpy() - want_s)) < 1e-2 + 1e-5 * np.max(np.abs(want_s))
+    assert np.max(np.abs(o_t.cpu().numpy() - want_o)) < 1e-2 + 1e-5 * np.max(np.abs(want_o))
+    c = cycles.cpu().numpy()
+    assert c.shape == (grid,) and np.all(c > 0)
