@@ -163,7 +163,9 @@ constexpr int kDeadEntry = -2147483647 - 1;  // an entry past the list's live co
 // done, 9 end, 10 fillers have their first segment, 11 first list entry read (resolvers),
 // 12 S^T issuer sees the first Q^T, 13 cluster merge: LSEs exchanged, 14 half-tiles walked (a
 // count), 15 end (%globaltimer), 16 cluster merge: messages sent, 17 messages received, 18 own
-// channels combined, 19 the first slot computed (resolvers), 20 the second half-tile's slots. Per half-tile g:
+// channels combined and stored, 19 the first slot computed (resolvers), 20 the second
+// half-tile's slots, 21 cluster merge: weights computed, 22 past the barrier after them. Per
+// half-tile g:
 // 0 S^T buffer free, 1 rows landed, 2 S^T issued, 3 S^T done (softmax), 4 P^T written,
 // 5 PV issued, 6 slots ready (filler), 7 fill issued, 8 softmax has S^T in registers, 9 the
 // softmax warps agreed on the maxima, 10 P^T stored (before the proxy fence), 11 the S^T
@@ -1077,18 +1079,17 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
 // packs, for every other CTA j, one message in its own shared memory (its 64 column LSEs,
 // then n_k of j's channels as fp16 [channel][72]: 64 columns and a pad) and sends it with one
 // bulk copy into j's receive buffer, completing on j's merge barrier. Then it combines its
-// own channels with the C - 1 messages it received and writes them out, staged through
-// shared memory so that the global stores are whole 16-byte runs of a row. The only
+// own channels with the C - 1 messages it received and writes them out straight from
+// registers (a warp's lanes hold 32 consecutive channels of one column, so each store
+// instruction writes a 64-byte run of an output row). The only
 // cluster-wide wait is the cluster barrier whose arrival each CTA makes when its stages are
 // free (its receive buffer lives in them), waited for just before the sends.
 constexpr int kMrgPitch = 72;  // fp16 per channel row of a message: 64 columns + 8 pad
 __host__ __device__ constexpr int merge_msg_bytes(int C) { return 256 + (kVdim / C) * kMrgPitch * 2; }
 __host__ __device__ constexpr int merge_region_bytes(int C) { return ((C - 1) * merge_msg_bytes(C) + 255) & ~255; }
-// shared-memory use after the stages: messages out | messages in | the output tile [64][512 / C]
-// bf16 | weights [C][64] fp32 (own, then one row per message)
-__host__ __device__ constexpr int merge_bytes(int C) {
-  return 2 * merge_region_bytes(C) + kRowsetRows * (kVdim / C) * 2 + C * kRowsetRows * 4;
-}
+// shared-memory use after the stages: messages out | messages in | weights [C][64] fp32 (own,
+// then one row per message)
+__host__ __device__ constexpr int merge_bytes(int C) { return 2 * merge_region_bytes(C) + C * kRowsetRows * 4; }
 static_assert(merge_bytes(2) <= 2 * kStageBytes && merge_bytes(4) <= 2 * kStageBytes &&
                   merge_bytes(8) <= 2 * kStageBytes,
               "merge buffers");
@@ -1102,8 +1103,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   const int msg = merge_msg_bytes(C);
   uint8_t* send = smem + kOffStage;
   uint8_t* recv = send + merge_region_bytes(C);
-  uint16_t* tile = reinterpret_cast<uint16_t*>(recv + merge_region_bytes(C));  // [64][chunk] bf16
-  float* wts = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(tile) + kRowsetRows * chunk * 2);  // [C][64]
+  float* wts = reinterpret_cast<float*>(recv + merge_region_bytes(C));  // [C][64]
   const float* mrg_m = reinterpret_cast<const float*>(smem + kOffMrgM);
   const float* mrg_l = reinterpret_cast<const float*>(smem + kOffMrgL);
   const bool had = *reinterpret_cast<const int*>(smem + kOffMrgFlag) != 0;
@@ -1195,41 +1195,51 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
     }
     if (rank == 0 && p.lse != nullptr && tid < rr.nvalid) p.lse[rr.base + tid] = tot * 0.69314718055994530942f;
   }
+  if (tid == 0) SVT_TRACE(21);
   __syncthreads();
-  // 4. this CTA's channels: own n plus the messages', into the output tile
+  if (tid == 0) SVT_TRACE(22);
+  // 4. this CTA's channels: own n plus the messages', straight into the output rows
+  const int ncols = rr.nvalid - 16 * cg;  // this warp's columns c < ncols exist
 #pragma unroll
   for (int mb = 0; mb < 4; ++mb) {
     const int ch0 = 128 * mb + 32 * qd;
     if (ch0 / chunk != rank) continue;
     const int cl = ch0 + lane - rank * chunk;
     float acc[16];
+    {
+      const float4* w4 = reinterpret_cast<const float4*>(wts + 16 * cg);
 #pragma unroll
-    for (int c = 0; c < 16; ++c) acc[c] = __uint_as_float(o[mb][c]) * wts[16 * cg + c];
+      for (int j = 0; j < 4; ++j) {
+        const float4 w = w4[j];
+        acc[4 * j] = __uint_as_float(o[mb][4 * j]) * w.x;
+        acc[4 * j + 1] = __uint_as_float(o[mb][4 * j + 1]) * w.y;
+        acc[4 * j + 2] = __uint_as_float(o[mb][4 * j + 2]) * w.z;
+        acc[4 * j + 3] = __uint_as_float(o[mb][4 * j + 3]) * w.w;
+      }
+    }
 #pragma unroll 1
     for (int s = 0; s < C - 1; ++s) {
       const uint4* src = reinterpret_cast<const uint4*>(recv + s * msg + 256 + (cl * kMrgPitch + 16 * cg) * 2);
       const uint4 a = src[0], b = src[1];
       const uint32_t hw[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-      const float* wk = wts + (1 + s) * kRowsetRows + 16 * cg;
+      const float4* w4 = reinterpret_cast<const float4*>(wts + (1 + s) * kRowsetRows + 16 * cg);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        acc[2 * i] += __half2float(__ushort_as_half(static_cast<unsigned short>(hw[i] & 0xFFFFu))) * wk[2 * i];
-        acc[2 * i + 1] += __half2float(__ushort_as_half(static_cast<unsigned short>(hw[i] >> 16))) * wk[2 * i + 1];
+      for (int j = 0; j < 4; ++j) {
+        const float4 w = w4[j];
+        const float2 f0 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * j]));
+        const float2 f1 = __half22float2(*reinterpret_cast<const __half2*>(&hw[2 * j + 1]));
+        acc[4 * j] += f0.x * w.x;
+        acc[4 * j + 1] += f0.y * w.y;
+        acc[4 * j + 2] += f1.x * w.z;
+        acc[4 * j + 3] += f1.y * w.w;
       }
     }
+    uint16_t* dst = p.out + (rr.base + 16 * cg) * kVdim + rank * chunk + cl;
 #pragma unroll
-    for (int c = 0; c < 16; ++c) tile[(16 * cg + c) * chunk + cl] = static_cast<uint16_t>(pack_bf16x2(acc[c], 0.f));
+    for (int c = 0; c < 16; ++c)
+      if (c < ncols) dst[c * kVdim] = static_cast<uint16_t>(pack_bf16x2(acc[c], 0.f));
   }
-  __syncthreads();
   if (tid == 0) SVT_TRACE(18);
-  // 5. the tile's rows that exist, as whole 16-byte runs of each output row
-  const int per_row = chunk / 8;
-#pragma unroll 1
-  for (int item = tid; item < rr.nvalid * per_row; item += kThreads) {
-    const int q = item / per_row, c8 = item - q * per_row;
-    *reinterpret_cast<uint4*>(p.out + (rr.base + q) * kVdim + rank * chunk + 8 * c8) =
-        *reinterpret_cast<const uint4*>(tile + q * chunk + 8 * c8);
-  }
   // this CTA's messages must have been read before its shared memory goes away
   if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
