@@ -164,8 +164,9 @@ constexpr int kDeadEntry = -2147483647 - 1;  // an entry past the list's live co
 // 12 S^T issuer sees the first Q^T, 13 cluster merge: LSEs exchanged, 14 half-tiles walked (a
 // count), 15 end (%globaltimer), 16 cluster merge: messages sent, 17 messages received, 18 own
 // channels combined and stored, 19 the first slot computed (resolvers), 20 the second
-// half-tile's slots, 21 cluster merge: weights computed, 22 past the barrier after them. Per
-// half-tile g:
+// half-tile's slots, 21 cluster merge: weights computed, 22 past the barrier after them, 24
+// its LSEs in the headers, 25 O^T in registers, 26 messages packed, 27 past the cluster
+// barrier. Per half-tile g:
 // 0 S^T buffer free, 1 rows landed, 2 S^T issued, 3 S^T done (softmax), 4 P^T written,
 // 5 PV issued, 6 slots ready (filler), 7 fill issued, 8 softmax has S^T in registers, 9 the
 // softmax warps agreed on the maxima, 10 P^T stored (before the proxy fence), 11 the S^T
@@ -1120,6 +1121,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
     wts[tid] = l > 0.f ? 1.0f / l : 0.f;
   }
   __syncthreads();
+  if (tid == 0) SVT_TRACE(24);
   // 2. n_k of the other CTAs' channels into their messages. All four M-blocks' 16 columns
   //    come out of TMEM with one wait (a TMEM load takes hundreds of cycles to return) and
   //    stay in registers for step 4.
@@ -1128,6 +1130,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
 #pragma unroll
     for (int mb = 0; mb < 4; ++mb) tmem_ld16(tq + 64 * mb, o[mb]);
     tmem_ld_wait();
+    if (tid == 0) SVT_TRACE(25);
   } else {
 #pragma unroll
     for (int mb = 0; mb < 4; ++mb)
@@ -1151,7 +1154,9 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   }
   fence_proxy_async_smem();  // the messages (generic writes) are read by the bulk copies
   __syncthreads();
+  if (tid == 0) SVT_TRACE(26);
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (tid == 0) SVT_TRACE(27);
   if (tid == 0) {
 #pragma unroll 1
     for (int j = 0; j < C; ++j) {
