@@ -58,6 +58,9 @@ TRAFFIC_BY_SOURCE = {
     "d700b230a6228da8": (159.347712e6, 60.956416e6, "256 MB write"),
     # the same with the resolvers' first-round length read and the softmax's per-segment bounds
     "4ff596103d408444": (159.387392e6, 60.962304e6, "256 MB write"),
+    # the cluster merge storing its channels straight from registers (and the tensor probe's
+    # entry point in the API source)
+    "4293d95688b1c4ae": (159.183360e6, 60.931840e6, "256 MB write"),
 }
 
 
@@ -630,6 +633,16 @@ def analyse_trace(tr: np.ndarray) -> dict:
     out["epilogue_us"] = med((ctas[:, 6] - ctas[:, 5])[ctas[:, 6] != 0].tolist())
     merged = ctas[:, 8] != 0
     out["cluster_merge_us"] = med((ctas[merged, 8] - ctas[merged, 7]).tolist()) if np.any(merged) else None
+    if np.any(merged):
+        # the merge's steps (slots 24-27, 16, 17, 21, 22, 18 in order): headers written, O^T in
+        # registers, messages packed, past the cluster barrier, copies issued, messages landed,
+        # weights, past their barrier, own channels combined and stored
+        m = ctas[merged]
+        steps = [("lse_headers", 7, 24), ("o_from_tmem", 24, 25), ("pack", 25, 26), ("cluster_barrier", 26, 27),
+                 ("issue_copies", 27, 16), ("copies_land", 16, 17), ("weights", 17, 21), ("weights_barrier", 21, 22),
+                 ("combine_and_store", 22, 18), ("final_barrier", 18, 8)]
+        if all(np.all(m[:, b] != 0) for _, _, b in steps):
+            out["cluster_merge_steps_us"] = {name: med((m[:, b] - m[:, a]).tolist()) for name, a, b in steps}
     out["roles_done_us"] = float(np.median(rel(ctas[:, 7])))
     out["end_us"] = float(np.median(rel(ctas[:, 9])))
     return out

@@ -60,3 +60,23 @@ def test_phase_trace_analysis_on_a_synthetic_launch():
     assert out["s_issuer_wait_rows_us"] == pytest.approx(0.2)     # buffer free at -500, rows at -100
     assert out["softmax_tmem_load_us"] == pytest.approx(0.05)
     assert out["softmax_fence_arrive_us"] == pytest.approx(0.05)
+    assert out["cluster_merge_us"] is None and "cluster_merge_steps_us" not in out
+
+
+def test_phase_trace_merge_steps():
+    # one clustered CTA: merge stamps 1000 cycles apart from "roles done" (slot 7) on
+    slots = bench.TRACE_HEAD + bench.TRACE_G * bench.TRACE_EV
+    tr = np.zeros((1, slots), np.uint64)
+    c0, gt0 = 50_000, 9_000_000
+    tr[0, 0], tr[0, 1], tr[0, 7] = gt0, c0, c0 + 10_000
+    order = [24, 25, 26, 27, 16, 17, 21, 22, 18, 8]
+    for k, slot in enumerate(order):
+        tr[0, slot] = c0 + 10_000 + 1000 * (k + 1)
+    tr[0, 9] = c0 + 30_000
+    tr[0, 15] = gt0 + 15_000  # 2 cycles per ns
+    out = bench.analyse_trace(tr)
+    assert out["cluster_merge_us"] == pytest.approx(5.0)
+    steps = out["cluster_merge_steps_us"]
+    assert list(steps) == ["lse_headers", "o_from_tmem", "pack", "cluster_barrier", "issue_copies", "copies_land",
+                           "weights", "weights_barrier", "combine_and_store", "final_barrier"]
+    assert all(v == pytest.approx(0.5) for v in steps.values())
