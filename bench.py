@@ -13,8 +13,10 @@ workload is a line item of the same JSON line, timed the same way:
   prefill_fp8   the 8192-token prefill over an e4m3 cache
   gather_probe  the bf16 batch's 131072 rows read with no arithmetic (the gather ceiling)
   topk          top-k selection of 64 indexer rows of 8K-32K scores
+  tensor_probe  one half-tile's MMA group, 400 times on every SM (the contractions' ceiling)
 Decode items report HBM GB/s on algorithmic and on gathered bytes against the measured copy
-peak; prefill items report executed, union and useful TFLOP/s against the bf16 peak.
+peak; prefill items report executed, union and useful TFLOP/s against the bf16 peak and
+their executed rate against the tensor probe's.
 
 Timing: W untimed warm-up steps, then K steps each bracketed by CUDA events on the
 launching stream, with a 256 MB buffer written before every step (outside the events) so
