@@ -306,7 +306,8 @@ SVT_API svt_status svt_gather_probe(const svt_kv_cache* kv, const int32_t* slots
  *   k_rows  [64, 576] bf16 row-major (64 cache rows; V is their first 512 channels).
  *   q       [64, 576] bf16 row-major (64 query rows).
  *   pt      [64, 64] bf16: P^T, row = cache row, column = query row.
- *   reps    1 .. 1000000; grid 1 .. 4096 CTAs (one per SM at most: 153 KB of shared memory each).
+ *   reps    1 .. 100000; grid 1 .. 1024 CTAs (one per SM at most: 153 KB of shared memory each;
+ *           a repetition takes about 1.7 us, so the largest call runs about a second).
  *   s_out   [64, 64] fp32: S^T of CTA 0 (row = cache row, column = query row), rewritten each
  *           repetition.
  *   o_out   [512, 64] fp32: O^T of CTA 0 (row = channel), accumulated over the repetitions:

@@ -171,7 +171,8 @@ def test_tensor_probe_checks_its_arguments(L):
     a, b, c, s, o, cyc = (P(0x20000 + 0x10000 * i) for i in range(6))
     assert L.svt_tensor_probe(a, b, c, 0, 1, s, o, cyc, WS, 256, None) == svt.SVT_ERR_INVALID_ARG  # reps 0
     assert L.svt_tensor_probe(a, b, c, 1, 0, s, o, cyc, WS, 256, None) == svt.SVT_ERR_INVALID_ARG  # grid 0
-    assert L.svt_tensor_probe(a, b, c, 1, 4097, s, o, cyc, WS, 256, None) == svt.SVT_ERR_INVALID_ARG
+    assert L.svt_tensor_probe(a, b, c, 1, 1025, s, o, cyc, WS, 256, None) == svt.SVT_ERR_INVALID_ARG
+    assert L.svt_tensor_probe(a, b, c, 100001, 1, s, o, cyc, WS, 256, None) == svt.SVT_ERR_INVALID_ARG
     assert L.svt_tensor_probe(None, b, c, 1, 1, s, o, cyc, WS, 256, None) == svt.SVT_ERR_INVALID_ARG
     assert L.svt_tensor_probe(a, b, c, 1, 1, s, None, cyc, WS, 256, None) == svt.SVT_ERR_INVALID_ARG
     assert L.svt_tensor_probe(P(0x20008), b, c, 1, 1, s, o, cyc, WS, 256, None) == svt.SVT_ERR_INVALID_ARG
