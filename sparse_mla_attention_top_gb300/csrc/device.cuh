@@ -77,8 +77,11 @@ struct WaitCtl {
 // wc.limit_ns it records SVT_DEV_ERR_TIMEOUT, raises the CTA's abort flag and returns
 // false; once the abort flag is up every later wait returns at once, so each role runs its
 // (finite) loops to the end and the kernel exits.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& wc) {
-  if (mbar_try_wait(bar, parity)) return true;
+// One try_wait (which sleeps until the phase completes or its time hint runs out) almost
+// always succeeds; the bounded loop after it is either inlined at the wait site or, with
+// kOutOfLine, one shared out-of-line copy. Which is faster depends on the kernel's
+// instruction stream, so each kernel chooses.
+__device__ __forceinline__ bool mbar_wait_loop(uint32_t bar, uint32_t parity, const WaitCtl& wc) {
   if (*wc.abort_flag) return false;
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
@@ -92,6 +95,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
       }
     }
   }
+}
+static __device__ __noinline__ bool mbar_wait_loop_out_of_line(uint32_t bar, uint32_t parity, const WaitCtl& wc) {
+  return mbar_wait_loop(bar, parity, wc);
+}
+template <bool kOutOfLine = false>
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& wc) {
+  if (mbar_try_wait(bar, parity)) return true;
+  if constexpr (kOutOfLine) return mbar_wait_loop_out_of_line(bar, parity, wc);
+  return mbar_wait_loop(bar, parity, wc);
 }
 
 // The same wait, ignoring the abort flag (used once at the end of a kernel, to let work
