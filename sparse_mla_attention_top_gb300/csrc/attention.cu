@@ -148,10 +148,9 @@ constexpr int kNamedBarRes = 2;  // the two resolver warps
 constexpr int kNamedBarCols = 3;
 constexpr int kColThreads = 128;
 
-// Pipeline waits: every role passes kF16 as mbar_wait's kOutOfLine, so the e4m3 kernels share
-// one out-of-line copy of the bounded wait loop and the bf16 kernels inline it at each site
-// (measured: e4m3 decode 105 -> 99 us and e4m3 prefill -2.5 % out of line, while the bf16
-// decode and the 16-head decode were 1-3 % slower that way).
+// Pipeline waits: the roles take kOOL as mbar_wait's kOutOfLine; each kernel chooses (see
+// tile_attention_kernel) whether its roles share one out-of-line copy of the bounded wait loop
+// or inline it at every wait site, by measurement of its instruction stream.
 
 // operand type of both contractions: bf16 for a bf16 cache; f16 for an e4m3 cache, whose rows
 // become code x block scale in f16 on the way into shared memory (Q^T and P^T follow)
@@ -331,7 +330,7 @@ __device__ __forceinline__ float rows16_column_reduce(float (&v)[16], int lane, 
 // ---------------------------------------------------------------------------------- resolvers
 // Decode: half-tile k's 64 entries -> slot / mask ring entry k % 4 (waiting until the softmax
 // and the fillers are done with half-tile k - 4), then SlotsReady(k % 4).
-template <bool kF16>
+template <bool kF16, bool kOOL>
 __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars, const WaitCtl& wc) {
   const int ltid = static_cast<int>(threadIdx.x) - kResWarp0 * 32;
   int* slot_tab = reinterpret_cast<int*>(smem + kOffSlot);
@@ -414,7 +413,7 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
       if (slot >= 0)
         prefetch_l2_bulk(p.kv + static_cast<long long>(slot) * p.row_stride, kF16 ? kRowBytesFp8 : kRowBytesBf16);
       const uint32_t e = k % kSlotRing;
-      if (k >= kSlotRing && !mbar_wait<kF16>(bar(kBarSlotFree + e), ((k / kSlotRing) - 1) & 1u, wc)) {
+      if (k >= kSlotRing && !mbar_wait<kOOL>(bar(kBarSlotFree + e), ((k / kSlotRing) - 1) & 1u, wc)) {
         live = false;
         break;
       }
@@ -441,7 +440,7 @@ __device__ __forceinline__ uint32_t rowset_member_bits(int rpar, int H) {
   return ((2u << hi) - 1u) & ~((1u << lo) - 1u);
 }
 
-template <bool kF16>
+template <bool kF16, bool kOOL>
 __device__ void resolver_prefill_role(const AttnParams& p, uint8_t* smem, uint32_t bars, const WaitCtl& wc) {
   const int ltid = static_cast<int>(threadIdx.x) - kResWarp0 * 32;
   const int rw = ltid >> 5, lane = ltid & 31;
@@ -490,7 +489,7 @@ __device__ void resolver_prefill_role(const AttnParams& p, uint8_t* smem, uint32
       const uint32_t e = k % kSlotRing;
       // both warps stop together if the wait gives up (they share named barriers)
       const bool freed =
-          k < kSlotRing || mbar_wait<kF16>(bar(kBarSlotFree + e), ((k / kSlotRing) - 1) & 1u, wc);
+          k < kSlotRing || mbar_wait<kOOL>(bar(kBarSlotFree + e), ((k / kSlotRing) - 1) & 1u, wc);
       if (!named_bar_red_and(kNamedBarRes, kResThreads, freed)) {
         live = false;
         break;
@@ -604,7 +603,7 @@ struct E4m3Rows {
   }
 };
 
-template <bool kF16>
+template <bool kF16, bool kOOL>
 __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, const WaitCtl& wc) {
   const int ftid = static_cast<int>(threadIdx.x) - kFillWarp0 * 32;
   const int lane = threadIdx.x & 31;
@@ -619,7 +618,7 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, c
   // past the row-set's last are other queries' rows or zeros past the tensor; their columns
   // of S^T and O^T are never written out)
   auto load_q = [&](const Seg& s) -> bool {
-    if (!mbar_wait<kF16>(bar(kBarQEmpty), (qk & 1u) ^ 1u, wc)) return false;
+    if (!mbar_wait<kOOL>(bar(kBarQEmpty), (qk & 1u) ^ 1u, wc)) return false;
     if (ftid == 0) {
       const RowsetRows rr = rowset_rows(p, s.r);
       mbar_arrive_expect_tx(bar(kBarQFull), kBlocks * kQBlk);
@@ -658,7 +657,7 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, c
       if constexpr (kF16) {
         // e4m3: the raw rows go into registers as soon as their slots are known, so that they
         // are in flight while the stage is still busy; converted and stored when it frees
-        if (!mbar_wait<kF16>(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, wc)) {
+        if (!mbar_wait<kOOL>(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, wc)) {
           live = false;
           break;
         }
@@ -669,7 +668,7 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, c
         if (lane == 0) mbar_arrive(bar(kBarSlotFree + e));
         // the converting stores go in one sweep once the whole stage is free (the last part
         // frees last); storing part by part costs registers the conversion needs
-        if (!mbar_wait<kF16>(bar(kBarEmpty + kEmptyParts * st + kEmptyParts - 1), ((g >> 1) & 1u) ^ 1u, wc)) {
+        if (!mbar_wait<kOOL>(bar(kBarEmpty + kEmptyParts * st + kEmptyParts - 1), ((g >> 1) & 1u) ^ 1u, wc)) {
           live = false;
           break;
         }
@@ -680,7 +679,7 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, c
       } else {
         // half-tile g's slots; the stage's parts are waited for below, each as PV of
         // half-tile g - 2 frees it
-        if (!mbar_wait<kF16>(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, wc)) {
+        if (!mbar_wait<kOOL>(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, wc)) {
           live = false;
           break;
         }
@@ -702,7 +701,7 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, c
         }
 #pragma unroll
         for (int part = 0; part < kEmptyParts; ++part) {
-          if (!mbar_wait<kF16>(bar(kBarEmpty + kEmptyParts * st + part), ((g >> 1) & 1u) ^ 1u, wc)) {
+          if (!mbar_wait<kOOL>(bar(kBarEmpty + kEmptyParts * st + part), ((g >> 1) & 1u) ^ 1u, wc)) {
             live = false;
             break;
           }
@@ -733,7 +732,7 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, c
 // ---------------------------------------------------------------------------------- issuers
 // S^T(g) into TMEM buffer g % 2 from stage g % 2, once the stage holds half-tile g and the
 // softmax is done with the buffer's previous contents (half-tile g - 2).
-template <bool kF16>
+template <bool kF16, bool kOOL>
 __device__ void s_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars,
                               const WaitCtl& wc) {
   const uint32_t sbase = smem_u32(smem);
@@ -745,14 +744,14 @@ __device__ void s_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   while (walk.next(p, s)) {
     if (s.n == 0) continue;
     // Q^T landed (bf16), or landed and converted to f16 (e4m3 caches)
-    if (!mbar_wait<kF16>(bar(kF16 ? kBarQReady : kBarQFull), qk & 1u, wc)) return;
+    if (!mbar_wait<kOOL>(bar(kF16 ? kBarQReady : kBarQFull), qk & 1u, wc)) return;
     if (qk == 0) SVT_TRACE(12);
     ++qk;
     for (int i = 0; i < s.n; ++i, ++g) {
       const uint32_t b = g & 1u;
-      if (g >= 2 && !mbar_wait<kF16>(bar(kBarPready + b), ((g - 2) >> 1) & 1u, wc)) return;
+      if (g >= 2 && !mbar_wait<kOOL>(bar(kBarPready + b), ((g - 2) >> 1) & 1u, wc)) return;
       SVT_TRACE_G(0, g);
-      if (!mbar_wait<kF16>(bar(kBarFull + b), (g >> 1) & 1u, wc)) return;
+      if (!mbar_wait<kOOL>(bar(kBarFull + b), (g >> 1) & 1u, wc)) return;
       SVT_TRACE_G(1, g);
       fence_proxy_async_smem();  // cp.async data (generic proxy) -> MMA operand reads
       tc_fence_after();
@@ -777,7 +776,7 @@ __device__ void s_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem,
 
 // PV(g) from stage g % 2 and P^T, once the softmax has written P^T(g) (and, for a segment's
 // first half-tile, once the previous segment's epilogue has read O^T).
-template <bool kF16>
+template <bool kF16, bool kOOL>
 __device__ void pv_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars,
                                const WaitCtl& wc) {
   const uint32_t sbase = smem_u32(smem);
@@ -788,11 +787,11 @@ __device__ void pv_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem
   Seg s;
   while (walk.next(p, s)) {
     if (s.n == 0) continue;
-    if (qk > 0 && !mbar_wait<kF16>(bar(kBarOFree), (qk - 1) & 1u, wc)) return;
+    if (qk > 0 && !mbar_wait<kOOL>(bar(kBarOFree), (qk - 1) & 1u, wc)) return;
     ++qk;
     for (int i = 0; i < s.n; ++i, ++g) {
       const uint32_t b = g & 1u;
-      if (!mbar_wait<kF16>(bar(kBarPready + b), (g >> 1) & 1u, wc)) return;
+      if (!mbar_wait<kOOL>(bar(kBarPready + b), (g >> 1) & 1u, wc)) return;
       tc_fence_after();
       const uint32_t stage = sbase + kOffStage + b * kStageBytes;
       const uint32_t pt = stage + 8 * kBlk;
@@ -813,7 +812,7 @@ __device__ void pv_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem
 }
 
 // ---------------------------------------------------------------------------------- softmax
-template <bool kF16>
+template <bool kF16, bool kOOL>
 __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars,
                              const WaitCtl& wc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -843,7 +842,7 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
     if constexpr (kF16) {
       if (nh > 0) {
         // the segment's Q^T (bf16, as it landed) becomes f16 in place for the f16 contractions
-        mbar_wait<kF16>(bar(kBarQFull), qs & 1u, wc);
+        mbar_wait<kOOL>(bar(kBarQFull), qs & 1u, wc);
         uint4* qv = reinterpret_cast<uint4*>(smem + kOffQ);
         bool q_range = false;
         for (int idx = threadIdx.x; idx < kBlocks * kQBlk / 16; idx += kSmThreads) {
@@ -865,9 +864,9 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
     for (int i = 0; i < nh; ++i, ++g) {
       const uint32_t b = g & 1u;
       const uint32_t e = g % kSlotRing;
-      mbar_wait<kF16>(bar(kBarSFull + b), (g >> 1) & 1u, wc);
+      mbar_wait<kOOL>(bar(kBarSFull + b), (g >> 1) & 1u, wc);
       if (threadIdx.x == 0) SVT_TRACE_G(3, g);
-      mbar_wait<kF16>(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, wc);
+      mbar_wait<kOOL>(bar(kBarSlotsReady + e), (g / kSlotRing) & 1u, wc);
       tc_fence_after();
       float x[16];
       {
@@ -929,7 +928,7 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
         if (i > 0) {
           // O^T holds every PV so far once the previous half-tile's PV is done
           const uint32_t gp = g - 1;
-          mbar_wait<kF16>(bar(kBarPvDone + (gp & 1u)), (gp >> 1) & 1u, wc);
+          mbar_wait<kOOL>(bar(kBarPvDone + (gp & 1u)), (gp >> 1) & 1u, wc);
           tc_fence_after();
 #pragma unroll 1
           for (int part = 0; part < 8; ++part) {  // 4 M-blocks x my 32 columns in halves
@@ -986,7 +985,7 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
     if (threadIdx.x == 0) SVT_TRACE(5);
     if (nh > 0) {
       const uint32_t gp = g - 1;
-      mbar_wait<kF16>(bar(kBarPvDone + (gp & 1u)), (gp >> 1) & 1u, wc);
+      mbar_wait<kOOL>(bar(kBarPvDone + (gp & 1u)), (gp >> 1) & 1u, wc);
       tc_fence_after();
     }
     const RowsetRows rr = rowset_rows(p, s.r);
@@ -1254,8 +1253,14 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
-template <bool kF16>
+// One kernel per cache type and mode: a decode kernel carries no prefill resolver and a prefill
+// kernel no cluster merge, so that each holds only the code it runs.
+template <bool kF16, bool kPrefill>
 __global__ void __launch_bounds__(kThreads, 1) tile_attention_kernel(const __grid_constant__ AttnParams p) {
+  // waits out of line in the e4m3 kernels (e4m3 decode 103 -> 99 us, e4m3 prefill -2.8 %) and
+  // the prefill kernels (bf16 prefill -1.3 %, 16-head prefill -0.7 %); inline in the bf16
+  // decode kernel, which was 1-3 % slower out of line
+  constexpr bool kOOL = kF16 || kPrefill;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t bars = smem_u32(smem) + kOffBars;
@@ -1313,25 +1318,25 @@ __global__ void __launch_bounds__(kThreads, 1) tile_attention_kernel(const __gri
   const WaitCtl wc{p.status, abort_flag, p.wait_limit_ns > 0 ? p.wait_limit_ns : kWaitLimitNs};
 
   if (warp >= kFillWarp0) {
-    filler_role<kF16>(p, smem, bars, wc);
+    filler_role<kF16, kOOL>(p, smem, bars, wc);
   } else if (warp >= kResWarp0) {
-    if (p.mode == kModeDecode)
-      resolver_role<kF16>(p, smem, bars, wc);
+    if constexpr (kPrefill)
+      resolver_prefill_role<kF16, kOOL>(p, smem, bars, wc);
     else
-      resolver_prefill_role<kF16>(p, smem, bars, wc);
+      resolver_role<kF16, kOOL>(p, smem, bars, wc);
   } else if (warp == kSIssuerWarp || warp == kPvIssuerWarp) {
     if ((threadIdx.x & 31) == 0) {
       if (warp == kSIssuerWarp)
-        s_issuer_role<kF16>(p, smem, tmem, bars, wc);
+        s_issuer_role<kF16, kOOL>(p, smem, tmem, bars, wc);
       else
-        pv_issuer_role<kF16>(p, smem, tmem, bars, wc);
+        pv_issuer_role<kF16, kOOL>(p, smem, tmem, bars, wc);
       // Drain arrives when every MMA this thread issued has completed (at once on a normal
       // run; after a timed-out wait the MMAs already issued may still be running)
       umma_commit(bars + 8u * kBarDrain);
     }
     __syncwarp();
   } else {
-    softmax_role<kF16>(p, smem, tmem, bars, wc);
+    softmax_role<kF16, kOOL>(p, smem, tmem, bars, wc);
   }
 
   // no MMA may still write TMEM (or read shared memory) when the roles below reuse it
@@ -1340,12 +1345,14 @@ __global__ void __launch_bounds__(kThreads, 1) tile_attention_kernel(const __gri
   __syncthreads();
   tc_fence_after();
   if (threadIdx.x == 0) SVT_TRACE(7);
-  if (p.cluster > 1) {
-    cluster_merge(p, smem, tmem, bars, wc);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (threadIdx.x == 0) SVT_TRACE(8);
+  if constexpr (!kPrefill) {
+    if (p.cluster > 1) {
+      cluster_merge(p, smem, tmem, bars, wc);
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (threadIdx.x == 0) SVT_TRACE(8);
+    }
   }
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 #ifdef SVT_PHASE_TRACE
@@ -1358,10 +1365,10 @@ __global__ void __launch_bounds__(kThreads, 1) tile_attention_kernel(const __gri
 #endif
 }
 
-template <bool kF16>
+template <bool kF16, bool kPrefill>
 cudaError_t launch_tile_attention(const AttnParams& p, cudaStream_t stream) {
-  cudaError_t e =
-      cudaFuncSetAttribute(tile_attention_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  cudaError_t e = cudaFuncSetAttribute(tile_attention_kernel<kF16, kPrefill>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   if (p.cluster > 1) {
     cudaLaunchConfig_t cfg = {};
@@ -1376,16 +1383,17 @@ cudaError_t launch_tile_attention(const AttnParams& p, cudaStream_t stream) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, tile_attention_kernel<kF16>, p);
+    return cudaLaunchKernelEx(&cfg, tile_attention_kernel<kF16, kPrefill>, p);
   }
-  tile_attention_kernel<kF16><<<p.num_ctas, kThreads, kSmemBytes, stream>>>(p);
+  tile_attention_kernel<kF16, kPrefill><<<p.num_ctas, kThreads, kSmemBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
 template <bool kF16>
 int max_active_clusters(int cluster) {
-  if (cudaFuncSetAttribute(tile_attention_kernel<kF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-      cudaSuccess)
+  // clusters are a decode plan: the decode kernel of the cache type is the one asked about
+  if (cudaFuncSetAttribute(tile_attention_kernel<kF16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(cluster));
@@ -1399,7 +1407,7 @@ int max_active_clusters(int cluster) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tile_attention_kernel<kF16>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, tile_attention_kernel<kF16, false>, &cfg) != cudaSuccess) {
     (void)cudaGetLastError();
     return 0;
   }
@@ -1425,7 +1433,10 @@ int attention_max_active_clusters(int cluster, int kv_dtype) {
 
 cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream) {
   if (p.num_ctas == 0) return cudaSuccess;
-  return p.kv_dtype == SVT_KV_BF16 ? launch_tile_attention<false>(p, stream) : launch_tile_attention<true>(p, stream);
+  const bool prefill = p.mode == kModePrefill;
+  if (p.kv_dtype == SVT_KV_BF16)
+    return prefill ? launch_tile_attention<false, true>(p, stream) : launch_tile_attention<false, false>(p, stream);
+  return prefill ? launch_tile_attention<true, true>(p, stream) : launch_tile_attention<true, false>(p, stream);
 }
 
 }  // namespace svt
