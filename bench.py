@@ -63,6 +63,8 @@ TRAFFIC_BY_SOURCE = {
     # the cluster merge storing its channels straight from registers (and the tensor probe's
     # entry point in the API source)
     "4293d95688b1c4ae": (159.183360e6, 60.931840e6, "256 MB write"),
+    # one kernel per cache type and mode, waits out of line in the e4m3 and prefill kernels
+    "895581153be257dc": (157.544448e6, 61.046272e6, "256 MB write"),
 }
 
 
