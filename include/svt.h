@@ -10,7 +10,8 @@
  *    and never synchronises the stream (except svt_read_status, whose job is to read back).
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream)
  *    and enqueues a fixed set of kernels whose grids depend only on the scalar arguments and
- *    the device, so a call can be captured in a CUDA graph.
+ *    the device, so the calls that take a caller's workspace can be captured in a CUDA graph
+ *    (this rule makes no statement about svt_sparse_mla_decode_noalloc).
  *  - Arguments are checked on the host before anything is enqueued. A failed check returns a
  *    non-zero svt_status, enqueues nothing, and svt_last_error_string() says why.
  *  - Faults found on the device (an index outside the request or the cache, a wait that ran
