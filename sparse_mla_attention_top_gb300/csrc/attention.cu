@@ -214,14 +214,26 @@ struct Seg {
   int slot;  // the partial slot (stream-K)
 };
 
-// The CTA's segments in order; every role walks its own copy.
+// The CTA's segments in order; every role walks its own copy. Decode launches split their
+// row-sets stream-K, prefill launches hand out whole row-sets. kMode: the launch's mode when
+// the kernel fixes it at compile time (kModeDecode / kModePrefill), or -1 to read it from p.
+template <int kMode>
+__device__ __forceinline__ bool mode_is_decode(const AttnParams& p) {
+  return kMode >= 0 ? kMode == kModeDecode : p.mode == kModeDecode;
+}
+// decode launches walk stream-K ranges, prefill launches whole row-sets
+template <int kMode>
+__device__ __forceinline__ bool sched_is_streamk(const AttnParams& p) {
+  return kMode >= 0 ? kMode == kModeDecode : p.sched == kSchedStreamK;
+}
+template <int kMode>
 struct SegWalk {
   long long pos, lo, hi;  // stream-K range in half-tiles
   int next_rowset, idx;
 
   __device__ void init(const AttnParams& p) {
     idx = 0;
-    if (p.sched == kSchedStreamK) {
+    if (sched_is_streamk<kMode>(p)) {
       lo = streamk_lo(blockIdx.x, p.total_tiles, p.num_ctas);
       hi = streamk_lo(blockIdx.x + 1ll, p.total_tiles, p.num_ctas);
       pos = lo;
@@ -231,7 +243,7 @@ struct SegWalk {
   }
 
   __device__ static int list_len(const AttnParams& p, int r) {
-    if (p.mode == kModeDecode) {
+    if (mode_is_decode<kMode>(p)) {
       const int t = r / p.hchunks;
       const int len = p.topk_len ? p.topk_len[t] : p.K;
       return len < 0 ? 0 : (len > p.K ? p.K : len);
@@ -243,7 +255,7 @@ struct SegWalk {
   // list length is filled in by with_len, so that a caller can put other reads in flight
   // before it waits for the length.
   __device__ bool next_range(const AttnParams& p, Seg& s, int& te) {
-    if (p.sched == kSchedStreamK) {
+    if (sched_is_streamk<kMode>(p)) {
       if (pos >= hi) return false;
       const long long nt = p.tiles_per_rowset;
       const long long r = pos / nt;
@@ -330,7 +342,7 @@ __device__ __forceinline__ float rows16_column_reduce(float (&v)[16], int lane, 
 // ---------------------------------------------------------------------------------- resolvers
 // Decode: half-tile k's 64 entries -> slot / mask ring entry k % 4 (waiting until the softmax
 // and the fillers are done with half-tile k - 4), then SlotsReady(k % 4).
-template <bool kF16, bool kOOL>
+template <bool kF16, bool kOOL, int kMode>
 __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars, const WaitCtl& wc) {
   const int ltid = static_cast<int>(threadIdx.x) - kResWarp0 * 32;
   int* slot_tab = reinterpret_cast<int*>(smem + kOffSlot);
@@ -339,7 +351,7 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
   const bool has_table = p.block_table != nullptr;
   int err = 0;
   uint32_t k = 0;
-  SegWalk walk;
+  SegWalk<kMode> walk;
   walk.init(p);
   Seg s;
   bool live = true;
@@ -372,7 +384,7 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
         if (p.seq_lens != nullptr) rc.seq_len = __ldg(p.seq_lens + req);
       }
     }
-    SegWalk::with_len(s, len_raw < 0 ? 0 : (len_raw > p.K ? p.K : len_raw), te);
+    SegWalk<kMode>::with_len(s, len_raw < 0 ? 0 : (len_raw > p.K ? p.K : len_raw), te);
     if (s.n == 0) continue;
     if (e0 >= s.len) raw = kDeadEntry;
 #ifdef SVT_PHASE_TRACE
@@ -440,7 +452,7 @@ __device__ __forceinline__ uint32_t rowset_member_bits(int rpar, int H) {
   return ((2u << hi) - 1u) & ~((1u << lo) - 1u);
 }
 
-template <bool kF16, bool kOOL>
+template <bool kF16, bool kOOL, int kMode>
 __device__ void resolver_prefill_role(const AttnParams& p, uint8_t* smem, uint32_t bars, const WaitCtl& wc) {
   const int ltid = static_cast<int>(threadIdx.x) - kResWarp0 * 32;
   const int rw = ltid >> 5, lane = ltid & 31;
@@ -449,7 +461,7 @@ __device__ void resolver_prefill_role(const AttnParams& p, uint8_t* smem, uint32
   volatile int* xch = reinterpret_cast<volatile int*>(smem + kOffResX);  // [0..1] the warps' kept counts
   auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
   uint32_t k = 0;
-  SegWalk walk;
+  SegWalk<kMode> walk;
   walk.init(p);
   Seg s;
   bool live = true;
@@ -459,7 +471,7 @@ __device__ void resolver_prefill_role(const AttnParams& p, uint8_t* smem, uint32
     const int32_t* list = p.enc + static_cast<long long>(g) * p.list_stride;
     int ulen = __ldg(p.lens + g);
     ulen = ulen < 0 ? 0 : (ulen > p.list_stride ? p.list_stride : ulen);
-    SegWalk::with_len(s, prefill_kept(p, s.r), te);
+    SegWalk<kMode>::with_len(s, prefill_kept(p, s.r), te);
     if (s.n == 0) continue;
     const uint32_t mbits = rowset_member_bits(s.r & 1, p.H);
     auto load = [&](int base) -> uint32_t {
@@ -603,7 +615,7 @@ struct E4m3Rows {
   }
 };
 
-template <bool kF16, bool kOOL>
+template <bool kF16, bool kOOL, int kMode>
 __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, const WaitCtl& wc) {
   const int ftid = static_cast<int>(threadIdx.x) - kFillWarp0 * 32;
   const int lane = threadIdx.x & 31;
@@ -620,7 +632,7 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, c
   auto load_q = [&](const Seg& s) -> bool {
     if (!mbar_wait<kOOL>(bar(kBarQEmpty), (qk & 1u) ^ 1u, wc)) return false;
     if (ftid == 0) {
-      const RowsetRows rr = rowset_rows(p, s.r);
+      const RowsetRows rr = rowset_rows<kMode>(p, s.r);
       mbar_arrive_expect_tx(bar(kBarQFull), kBlocks * kQBlk);
       for (int kb = 0; kb < kBlocks; ++kb)
         tma_load_2d(sbase + kOffQ + kb * kQBlk, &p.q_map, 64 * kb, static_cast<int>(rr.base), bar(kBarQFull));
@@ -628,17 +640,17 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, c
     ++qk;
     return true;
   };
-  SegWalk walk;
+  SegWalk<kMode> walk;
   walk.init(p);
-  if (p.sched == kSchedStreamK && ftid < kRowsetRows) {
+  if (sched_is_streamk<kMode>(p) && ftid < kRowsetRows) {
     // a stream-K range holds at most a few segments: their Q rows go to L2 now, so that a
     // segment boundary reloads Q^T from L2
-    SegWalk ahead = walk;
+    SegWalk<kMode> ahead = walk;
     Seg sa;
     int te;
     bool first = true;
     while (ahead.next_range(p, sa, te)) {
-      const RowsetRows rr = rowset_rows(p, sa.r);
+      const RowsetRows rr = rowset_rows<kMode>(p, sa.r);
       if (!first && ftid < rr.nvalid) prefetch_l2_bulk(qb + (rr.base + ftid) * (kRow * 2), kRow * 2);
       first = false;
     }
@@ -732,13 +744,13 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, c
 // ---------------------------------------------------------------------------------- issuers
 // S^T(g) into TMEM buffer g % 2 from stage g % 2, once the stage holds half-tile g and the
 // softmax is done with the buffer's previous contents (half-tile g - 2).
-template <bool kF16, bool kOOL>
+template <bool kF16, bool kOOL, int kMode>
 __device__ void s_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars,
                               const WaitCtl& wc) {
   const uint32_t sbase = smem_u32(smem);
   auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
   uint32_t g = 0, qk = 0;
-  SegWalk walk;
+  SegWalk<kMode> walk;
   walk.init(p);
   Seg s;
   while (walk.next(p, s)) {
@@ -776,13 +788,13 @@ __device__ void s_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem,
 
 // PV(g) from stage g % 2 and P^T, once the softmax has written P^T(g) (and, for a segment's
 // first half-tile, once the previous segment's epilogue has read O^T).
-template <bool kF16, bool kOOL>
+template <bool kF16, bool kOOL, int kMode>
 __device__ void pv_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars,
                                const WaitCtl& wc) {
   const uint32_t sbase = smem_u32(smem);
   auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
   uint32_t g = 0, qk = 0;
-  SegWalk walk;
+  SegWalk<kMode> walk;
   walk.init(p);
   Seg s;
   while (walk.next(p, s)) {
@@ -812,7 +824,7 @@ __device__ void pv_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem
 }
 
 // ---------------------------------------------------------------------------------- softmax
-template <bool kF16, bool kOOL>
+template <bool kF16, bool kOOL, int kMode>
 __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint32_t bars,
                              const WaitCtl& wc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -829,9 +841,9 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
   float* red = reinterpret_cast<float*>(smem + kOffRed);
   float* lfin = reinterpret_cast<float*>(smem + kOffLfin);
   auto bar = [&](int i) -> uint32_t { return bars + 8u * static_cast<uint32_t>(i); };
-  const bool decode = p.mode == kModeDecode;
+  const bool decode = mode_is_decode<kMode>(p);
   uint32_t g = 0, qs = 0;
-  SegWalk walk;
+  SegWalk<kMode> walk;
   walk.init(p);
   Seg s;
   float lpart[16];
@@ -988,14 +1000,14 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
       mbar_wait<kOOL>(bar(kBarPvDone + (gp & 1u)), (gp >> 1) & 1u, wc);
       tc_fence_after();
     }
-    const RowsetRows rr = rowset_rows(p, s.r);
+    const RowsetRows rr = rowset_rows<kMode>(p, s.r);
     {
       int idx;
       const float l = rows16_column_reduce<false>(lpart, lane, idx);  // this warp's 16 rows
       red[warp * 32 + 2 * idx + cp] = l;
     }
     named_bar_sync(kNamedBarSm, kSmThreads);
-    if (p.cluster > 1) {
+    if (kMode != kModePrefill && p.cluster > 1) {
       // a slice of a clustered row-set: its column maxima and sums go to the cluster merge,
       // which reads O^T from TMEM once every role of every CTA of the cluster is done
       if (threadIdx.x < kRowsetRows) {
@@ -1112,7 +1124,7 @@ __device__ void cluster_merge(const AttnParams& p, uint8_t* smem, uint32_t tmem,
   const float* mrg_m = reinterpret_cast<const float*>(smem + kOffMrgM);
   const float* mrg_l = reinterpret_cast<const float*>(smem + kOffMrgL);
   const bool had = *reinterpret_cast<const int*>(smem + kOffMrgFlag) != 0;
-  const RowsetRows rr = rowset_rows(p, static_cast<int>(blockIdx.x) / C);
+  const RowsetRows rr = rowset_rows<kModeDecode>(p, static_cast<int>(blockIdx.x) / C);
   const uint32_t tq = tmem + (static_cast<uint32_t>(32 * qd) << 16) + kTmemO + 16 * cg;
   // this CTA's stages are free: the other CTAs may send into them once all have arrived
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
@@ -1261,6 +1273,10 @@ __global__ void __launch_bounds__(kThreads, 1) tile_attention_kernel(const __gri
   // the prefill kernels (bf16 prefill -1.3 %, 16-head prefill -0.7 %); inline in the bf16
   // decode kernel, which was 1-3 % slower out of line
   constexpr bool kOOL = kF16 || kPrefill;
+  // the prefill kernels fix the mode at compile time inside their roles (bf16 prefill -1.9 %,
+  // e4m3 -0.9 %, 16-head -1.5 %); the decode kernels read it at run time, as the 16-head
+  // decode was 1.5 % slower with it fixed
+  constexpr int kMode = kPrefill ? static_cast<int>(kModePrefill) : -1;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const uint32_t bars = smem_u32(smem) + kOffBars;
@@ -1318,25 +1334,25 @@ __global__ void __launch_bounds__(kThreads, 1) tile_attention_kernel(const __gri
   const WaitCtl wc{p.status, abort_flag, p.wait_limit_ns > 0 ? p.wait_limit_ns : kWaitLimitNs};
 
   if (warp >= kFillWarp0) {
-    filler_role<kF16, kOOL>(p, smem, bars, wc);
+    filler_role<kF16, kOOL, kMode>(p, smem, bars, wc);
   } else if (warp >= kResWarp0) {
     if constexpr (kPrefill)
-      resolver_prefill_role<kF16, kOOL>(p, smem, bars, wc);
+      resolver_prefill_role<kF16, kOOL, kMode>(p, smem, bars, wc);
     else
-      resolver_role<kF16, kOOL>(p, smem, bars, wc);
+      resolver_role<kF16, kOOL, kMode>(p, smem, bars, wc);
   } else if (warp == kSIssuerWarp || warp == kPvIssuerWarp) {
     if ((threadIdx.x & 31) == 0) {
       if (warp == kSIssuerWarp)
-        s_issuer_role<kF16, kOOL>(p, smem, tmem, bars, wc);
+        s_issuer_role<kF16, kOOL, kMode>(p, smem, tmem, bars, wc);
       else
-        pv_issuer_role<kF16, kOOL>(p, smem, tmem, bars, wc);
+        pv_issuer_role<kF16, kOOL, kMode>(p, smem, tmem, bars, wc);
       // Drain arrives when every MMA this thread issued has completed (at once on a normal
       // run; after a timed-out wait the MMAs already issued may still be running)
       umma_commit(bars + 8u * kBarDrain);
     }
     __syncwarp();
   } else {
-    softmax_role<kF16, kOOL>(p, smem, tmem, bars, wc);
+    softmax_role<kF16, kOOL, kMode>(p, smem, tmem, bars, wc);
   }
 
   // no MMA may still write TMEM (or read shared memory) when the roles below reuse it

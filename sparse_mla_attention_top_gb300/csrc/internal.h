@@ -103,9 +103,12 @@ struct RowsetRows {
   int nvalid;
 };
 
+// kMode: the launch's mode when the caller knows it at compile time (kModeDecode or
+// kModePrefill), else -1 to read it from p.
+template <int kMode = -1>
 __device__ __forceinline__ RowsetRows rowset_rows(const AttnParams& p, int r) {
   RowsetRows rr;
-  if (p.mode == kModeDecode) {
+  if (kMode >= 0 ? kMode == kModeDecode : p.mode == kModeDecode) {
     const int t = r / p.hchunks;
     const int hc = r - t * p.hchunks;
     rr.base = static_cast<long long>(t) * p.H + hc * kRowsetRows;
