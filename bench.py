@@ -65,6 +65,8 @@ TRAFFIC_BY_SOURCE = {
     "4293d95688b1c4ae": (159.183360e6, 60.931840e6, "256 MB write"),
     # one kernel per cache type and mode, waits out of line in the e4m3 and prefill kernels
     "895581153be257dc": (157.544448e6, 61.046272e6, "256 MB write"),
+    # the prefill kernels' mode fixed at compile time (the decode kernels' code unchanged)
+    "3b8854cb7d11f6cb": (157.325568e6, 61.010432e6, "256 MB write"),
 }
 
 
