@@ -86,7 +86,7 @@ def parse():
     ap.add_argument("--phase-trace", action="store_true",
                     help="build the phase-trace library and print per-phase times of the attention kernel")
     ap.add_argument("--item", choices=["decode_fp8", "decode_mixed", "prefill", "prefill_mixed", "prefill_fp8",
-                                       "tensor_probe"],
+                                       "prefill_union_tile", "prefill_mixed_union_tile", "tensor_probe"],
                     help="run that one line item alone and print it (for profiling one workload)")
     return ap.parse_args()
 
@@ -427,8 +427,9 @@ def bench_decode(S, w, dev, stream, flush, steps, warmup, hbm_peak, ws=None):
             "launches_per_call": 2 if ws_need > 256 else 1, "_times": times, "_d": d, "_out": out, "_lse": lse}
 
 
-def bench_prefill(S, pw, dev, stream, flush, steps, warmup, bf16_peak):
-    """One grouped-prefill workload: slot resolution + union build, then attention, timed apart."""
+def bench_prefill(S, pw, dev, stream, flush, steps, warmup, bf16_peak, union_tile=False):
+    """One grouped-prefill workload: slot resolution + union build, then attention, timed apart
+    (union_tile: the two-CTA union-tile kernel instead of the row-set kernel)."""
     import torch
 
     d = dev_inputs(S, pw, dev)
@@ -446,7 +447,8 @@ def bench_prefill(S, pw, dev, stream, flush, steps, warmup, bf16_peak):
         S.build_group_union(slots, pw.G, pw.num_slots, enc=enc, lens=lens, ws=ws)
 
     def attn_step():
-        S.sparse_mla_prefill_grouped(d["q"], pw.G, d["kv"], enc, lens, pw.K, pw.scale, out=pout, lse=plse, ws=ws)
+        S.sparse_mla_prefill_grouped(d["q"], pw.G, d["kv"], enc, lens, pw.K, pw.scale, out=pout, lse=plse, ws=ws,
+                                     union_tile=union_tile)
 
     for _ in range(max(3, warmup)):
         union_step()
@@ -463,11 +465,16 @@ def bench_prefill(S, pw, dev, stream, flush, steps, warmup, bf16_peak):
     # each, the last one padded). A 128-row tile over the whole union would execute `union`
     # flops instead; useful flops count each query's own live entries.
     kept = rowset_kept_counts(enc.cpu().numpy(), lens_h, pw.H)
-    executed = float(2 * 64 * 64 * ((kept + 63) // 64).sum() * (576 + 512))
+    if union_tile:
+        # every group's 128 rows over its whole union, in 64-entry tiles (the last one padded)
+        executed = float(2 * 128 * 64 * ((lens_h + 63) // 64).sum() * (576 + 512))
+    else:
+        executed = float(2 * 64 * 64 * ((kept + 63) // 64).sum() * (576 + 512))
     union = float(2 * 128 * lens_h.sum() * (576 + 512))
     useful = float(2 * pw.H * live.sum() * (576 + 512))
     a_ms, u_ms = statistics.mean(at), statistics.mean(ut)
     return {"workload": pw.name, "kv_dtype": "bf16" if pw.kv_dtype == 0 else "e4m3",
+            "kernel": "union tile (pair_prefill_kernel)" if union_tile else "row-sets (tile_attention_kernel)",
             "union_ms": round(u_ms, 4), "attention_ms": round(a_ms, 4), "step_ms": round(u_ms + a_ms, 4),
             "tflops_executed": executed / (a_ms / 1e3) / 1e12,
             "tflops_union": union / (a_ms / 1e3) / 1e12,
@@ -726,9 +733,11 @@ def run_item(args):
     elif args.item == "tensor_probe":
         item = bench_tensor_probe(S, dev, stream, flush, args.steps, bf16_peak)
     else:
-        pw = {"prefill": W.grouped_prefill, "prefill_mixed": W.mixed_prefill,
-              "prefill_fp8": W.grouped_prefill_fp8}[args.item](args.prefill_T)
-        item = bench_prefill(S, pw, dev, stream, flush, args.steps, args.warmup, bf16_peak)
+        pw = {"prefill": W.grouped_prefill, "prefill_mixed": W.mixed_prefill, "prefill_fp8": W.grouped_prefill_fp8,
+              "prefill_union_tile": W.grouped_prefill, "prefill_mixed_union_tile": W.mixed_prefill}[args.item](
+                  args.prefill_T)
+        item = bench_prefill(S, pw, dev, stream, flush, args.steps, args.warmup, bf16_peak,
+                             union_tile=args.item.endswith("union_tile"))
     print(json.dumps({args.item: item}), flush=True)
 
 
@@ -832,12 +841,14 @@ def main():
         items["prefill"] = bench_prefill(S, W.grouped_prefill(args.prefill_T), dev, stream, flush, psteps,
                                          args.warmup, bf16_peak)
         if not args.no_items:
+            items["prefill_union_tile"] = bench_prefill(S, W.grouped_prefill(args.prefill_T), dev, stream, flush,
+                                                        psteps, args.warmup, bf16_peak, union_tile=True)
             items["prefill_mixed"] = bench_prefill(S, W.mixed_prefill(args.prefill_T), dev, stream, flush, psteps,
                                                    args.warmup, bf16_peak)
             items["prefill_fp8"] = bench_prefill(S, W.grouped_prefill_fp8(args.prefill_T), dev, stream, flush,
                                                  psteps, args.warmup, bf16_peak)
         # the prefill's executed rate against the same half-tiles' MMAs with nothing else running
-        for key in ("prefill", "prefill_mixed", "prefill_fp8"):
+        for key in ("prefill", "prefill_mixed", "prefill_fp8"):  # the row-set kernel's half-tiles
             if key in items:
                 items[key]["frac_of_tensor_probe"] = items[key]["tflops_executed"] / tp["tflops"]
 

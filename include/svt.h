@@ -249,6 +249,25 @@ SVT_API svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T,
                                           size_t ws_bytes, svt_stream_t stream);
 
 /*
+ * Grouped sparse prefill with one gathered union tile for all 128 packed rows of a group
+ * (vLLM PR #63104, Overview and Details / Why: the group's union is gathered once and every
+ * row of the tile keeps to its member's entries through the mask bit). Same arguments,
+ * layouts, results and workspace as svt_sparse_mla_prefill_grouped, for a bf16 cache only
+ * (SVT_ERR_UNSUPPORTED otherwise). Each group runs on a thread-block cluster of two CTAs that
+ * split the 576 channels between them (latent 0-255 and rope 0-31 on one, latent 256-511 and
+ * rope 32-63 on the other) and exchange partial scores and P rows through distributed shared
+ * memory; every row is computed over the whole union (its member's entries live, the others
+ * masked), where svt_sparse_mla_prefill_grouped lets each half of the group walk only the
+ * entries live for its own members. A group whose members selected nothing gets out = 0 and
+ * lse = -inf. The workspace is only read for its status header.
+ */
+SVT_API svt_status svt_sparse_mla_prefill_grouped_union_tile(const void* q_bf16, int32_t T, int32_t H, int32_t G,
+                                                     const svt_kv_cache* kv, const int32_t* enc,
+                                                     const int32_t* lens, int32_t K, float softmax_scale,
+                                                     void* out_bf16, float* lse, void* ws, size_t ws_bytes,
+                                                     svt_stream_t stream);
+
+/*
  * Merge of split-KV partials (explainer of arXiv 2511.11581, section 4.5: programs that own
  * slices of the KV list produce partial results that are merged):
  *   lse = ln sum_s exp(lse_part[s]),  out = sum_s exp(lse_part[s] - lse) * o_part[s].

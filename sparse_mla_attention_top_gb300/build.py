@@ -18,7 +18,8 @@ BUILD_DIR = PKG / "_build"
 # pipeline step of the attention kernel); a separate library that only profiling loads.
 TRACE_LIB = PKG / "libsvt_trace.so"
 TRACE_BUILD_DIR = PKG / "_build_trace"
-SOURCES = ["api.cu", "attention.cu", "resolve.cu", "union.cu", "merge.cu", "noalloc.cu", "topk.cu", "probe.cu"]
+SOURCES = ["api.cu", "attention.cu", "resolve.cu", "union.cu", "merge.cu", "noalloc.cu", "topk.cu", "probe.cu",
+           "pair_prefill.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden", f"-I{INCLUDE}", f"-I{CSRC}"]
 

@@ -408,10 +408,13 @@ size_t svt_sparse_mla_prefill_grouped_workspace_size(int32_t T, int32_t, int32_t
   return svt::kStatusBytes + round_up(2 * groups * sizeof(int32_t), 256);
 }
 
-svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T, int32_t H, int32_t G,
-                                          const svt_kv_cache* kv, const int32_t* enc, const int32_t* lens, int32_t K,
-                                          float softmax_scale, void* out_bf16, float* lse, void* ws,
-                                          size_t ws_bytes, svt_stream_t stream) {
+namespace {
+
+// Both grouped-prefill entry points: the same checks, then the row-set kernel (after the
+// row-set count kernel) or, with union_tile, the two-CTA union tile (bf16 caches only).
+svt_status prefill_grouped(const void* q_bf16, int32_t T, int32_t H, int32_t G, const svt_kv_cache* kv,
+                           const int32_t* enc, const int32_t* lens, int32_t K, float softmax_scale, void* out_bf16,
+                           float* lse, void* ws, size_t ws_bytes, svt_stream_t stream, bool union_tile) {
   if (T < 0 || K <= 0 || H <= 0) return fail(SVT_ERR_INVALID_ARG, "T must be >= 0, K and H > 0");
   if (G != 2 && G != 4 && G != 8) return fail(SVT_ERR_UNSUPPORTED, "G must be 2, 4 or 8, got %d", G);
   if (H * G != 128) return fail(SVT_ERR_UNSUPPORTED, "H * G must be 128 (H = %d, G = %d)", H, G);
@@ -421,6 +424,8 @@ svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T, int32_t
   if (st != SVT_OK) return st;
   const long long num_slots = kv->num_pages * static_cast<long long>(kv->page_size);
   if (num_slots >= 0xFFFFFF) return fail(SVT_ERR_UNSUPPORTED, "grouped prefill needs fewer than 2^24-1 cache rows");
+  if (union_tile && kv->dtype != SVT_KV_BF16)
+    return fail(SVT_ERR_UNSUPPORTED, "the union-tile prefill takes a bf16 cache");
   st = check_ws(ws, ws_bytes, svt_sparse_mla_prefill_grouped_workspace_size(T, H, G));
   if (st != SVT_OK) return st;
   if (T == 0) return SVT_OK;
@@ -460,6 +465,16 @@ svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T, int32_t
 #ifdef SVT_PHASE_TRACE
   p.trace = svt::trace_for(p.num_ctas);
 #endif
+  if (union_tile) {
+    // one gathered union tile for the group's 128 rows, on a cluster of two CTAs per group
+    const int clusters = svt::pair_prefill_clusters();
+    if (clusters <= 0) return fail(SVT_ERR_CUDA, "the two-CTA prefill cluster cannot be scheduled on this device");
+    p.num_rowsets = groups;
+    p.num_ctas = 2 * (groups < clusters ? groups : clusters);
+    cudaError_t e = svt::launch_pair_prefill(p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
+    return SVT_OK;
+  }
   int* counts = reinterpret_cast<int*>(static_cast<char*>(ws) + svt::kStatusBytes);
   p.counts = counts;
   cudaError_t e = svt::launch_rowset_counts(enc, lens, groups, p.list_stride, H, num_slots, counts, p.status,
@@ -468,6 +483,24 @@ svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T, int32_t
   e = svt::launch_attention(p, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
   return SVT_OK;
+}
+
+}  // namespace
+
+svt_status svt_sparse_mla_prefill_grouped(const void* q_bf16, int32_t T, int32_t H, int32_t G,
+                                          const svt_kv_cache* kv, const int32_t* enc, const int32_t* lens, int32_t K,
+                                          float softmax_scale, void* out_bf16, float* lse, void* ws,
+                                          size_t ws_bytes, svt_stream_t stream) {
+  return prefill_grouped(q_bf16, T, H, G, kv, enc, lens, K, softmax_scale, out_bf16, lse, ws, ws_bytes, stream,
+                         false);
+}
+
+svt_status svt_sparse_mla_prefill_grouped_union_tile(const void* q_bf16, int32_t T, int32_t H, int32_t G,
+                                                     const svt_kv_cache* kv, const int32_t* enc, const int32_t* lens,
+                                                     int32_t K, float softmax_scale, void* out_bf16, float* lse,
+                                                     void* ws, size_t ws_bytes, svt_stream_t stream) {
+  return prefill_grouped(q_bf16, T, H, G, kv, enc, lens, K, softmax_scale, out_bf16, lse, ws, ws_bytes, stream,
+                         true);
 }
 
 svt_status svt_merge_splits(const float* o_part, const float* lse_part, int32_t S, int32_t T, int32_t H,

@@ -132,6 +132,15 @@ __device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uin
                : "memory");
 }
 
+// 1-D bulk copy from this CTA's shared memory to a cluster peer's (dst and bar are
+// shared::cluster addresses of the peer; 16-byte aligned, size a multiple of 16); completes
+// `bytes` of transactions on the peer's `bar`.
+__device__ __forceinline__ void bulk_copy_s2c(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "r"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
 // 2-D tiled TMA load of the box at (x, y) of the tensor `tmap` describes (a __grid_constant__
 // kernel parameter) into shared memory at dst; completes the box's bytes on `bar`. x is the
 // innermost coordinate, in elements; x * element size must be a multiple of 16 bytes.
@@ -163,6 +172,70 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 // cluster, global memory) are visible to reads after it.
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// One arrival on the mbarrier at `remote_bar` (a shared::cluster address, possibly another
+// CTA's); this thread's earlier memory operations are released at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+
+// The same arrival without release semantics (no wait for this thread's earlier stores): for
+// a consumer telling a producer it may overwrite data whose loads have completed.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t remote_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_relaxed(uint32_t bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// 16 bytes (or 4) into another CTA's shared memory at `remote_addr`, completing that many
+// bytes of transactions on its mbarrier `remote_bar` (both shared::cluster addresses); the
+// receiver sees the data once it has waited for the barrier's phase.
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint4 v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   remote_addr),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(remote_bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr), "r"(v),
+               "r"(remote_bar)
+               : "memory");
+}
+
+// The bounded wait for a barrier whose phase other CTAs of the cluster complete (remote
+// arrivals, st.async bytes, multicast commits): the same as mbar_wait, with the phase
+// observed at cluster scope.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+static __device__ __noinline__ bool mbar_wait_cluster_loop(uint32_t bar, uint32_t parity, const WaitCtl& wc) {
+  if (*wc.abort_flag) return false;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*wc.abort_flag) return false;
+      if (globaltimer() - t0 > wc.limit_ns) {
+        atomicOr(wc.status, SVT_DEV_ERR_TIMEOUT);
+        *wc.abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const WaitCtl& wc) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  return mbar_wait_cluster_loop(bar, parity, wc);
 }
 
 // Named barrier among `count` threads that also returns whether `pred` held in all of them.
@@ -240,10 +313,30 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16: A (M rows in TMEM lanes, two 16-bit K
+// elements per 32-bit column, K = 16 in 8 columns from a_tmem) read from tensor memory.
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrives once on `bar` when every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
+}
+// The same arrival on the mbarrier at this shared-memory offset in every CTA of the cluster
+// whose bit is set in cta_mask.
+__device__ __forceinline__ void umma_commit_multicast(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -290,6 +383,16 @@ __device__ __forceinline__ void tmem_ld_16x64b_x16(uint32_t taddr, uint32_t (&r)
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
         "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
+      : "memory");
+}
+
+// The store with the same 16-lane layout as tmem_ld_16x64b_x16.
+__device__ __forceinline__ void tmem_st_16x64b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x64b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
       : "memory");
 }
 
@@ -342,6 +445,24 @@ __host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, int a_mn, int 
   return (1u << 4) | (static_cast<uint32_t>(fmt) << 7) | (static_cast<uint32_t>(fmt) << 10) |
          (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The same descriptor for the 64-byte swizzle (rows of 64 bytes; every 8 rows form a 512-byte
+// atom whose 16-byte chunks are XOR-permuted by (row / 2) % 4; layout 4 in bits 61-63).
+//   K-major operand (rows of 32 K-elements): SBO = distance between 8-row groups; LBO unused.
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t start, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((start >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 4ull << 61;
+  return d;
+}
+
+// Position of the 16-byte chunk `chunk` (0..3) of row `row` in the 64-byte swizzle layout.
+__device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t chunk) {
+  return row * 64u + ((chunk ^ ((row >> 1) & 3u)) << 4);
 }
 
 // Position of the 16-byte chunk `chunk` (0..7) of row `row` inside a 128-byte-swizzled atom.

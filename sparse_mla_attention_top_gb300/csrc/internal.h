@@ -180,6 +180,13 @@ cudaError_t launch_attention(const AttnParams& p, cudaStream_t stream);
 // How many clusters of `cluster` attention CTAs (one per SM) the current device runs at once
 // (0 if the query fails); cached per device.
 int attention_max_active_clusters(int cluster, int kv_dtype);
+// Grouped prefill over a bf16 cache with G * H = 128: one thread-block cluster of two CTAs
+// per group (round-robin over p.num_rowsets groups on p.num_ctas CTAs, an even number), each
+// CTA holding half of the channels, one gathered union tile for all 128 packed rows.
+cudaError_t launch_pair_prefill(const AttnParams& p, cudaStream_t stream);
+// How many of those two-CTA clusters the current device runs at once (0 if the query fails);
+// cached per device.
+int pair_prefill_clusters();
 // Merges the partial results of the row-sets a stream-K decode split between CTAs; launched
 // right behind the attention kernel (programmatic dependent launch) and waiting for it.
 cudaError_t launch_streamk_merge(const AttnParams& p, cudaStream_t stream);

@@ -32,7 +32,8 @@ EXPORTED = [
     "svt_last_error_string", "svt_workspace_init", "svt_read_status", "svt_resolve_workspace_size",
     "svt_resolve_topk_slots", "svt_sparse_mla_decode_workspace_size", "svt_sparse_mla_decode",
     "svt_build_group_union_workspace_size", "svt_build_group_union",
-    "svt_sparse_mla_prefill_grouped_workspace_size", "svt_sparse_mla_prefill_grouped", "svt_merge_splits",
+    "svt_sparse_mla_prefill_grouped_workspace_size", "svt_sparse_mla_prefill_grouped",
+    "svt_sparse_mla_prefill_grouped_union_tile", "svt_merge_splits",
     "svt_topk_select",
     "svt_sparse_mla_decode_noalloc", "svt_debug_pipeline_fault", "svt_gather_probe", "svt_tensor_probe",
 ]
@@ -86,6 +87,7 @@ def lib():
         L.svt_sparse_mla_prefill_grouped_workspace_size.restype = sz
         L.svt_sparse_mla_prefill_grouped.argtypes = [P, i32, i32, i32, ctypes.POINTER(_KV), P, P, i32, f32, P, P, P,
                                                      sz, P]
+        L.svt_sparse_mla_prefill_grouped_union_tile.argtypes = L.svt_sparse_mla_prefill_grouped.argtypes
         L.svt_merge_splits.argtypes = [P, P, i32, i32, i32, P, P, P]
         L.svt_topk_select.argtypes = [P, i32, i32, i64, P, i32, P, P]
         L.svt_sparse_mla_decode_noalloc.argtypes = [P, i32, i32, ctypes.POINTER(_KV), P, i32, i32, P, P, P, i32, P, f32,
@@ -238,8 +240,10 @@ def build_group_union(slots, G: int, num_slots: int, *, topk_len=None, enc=None,
 
 
 def sparse_mla_prefill_grouped(q, G: int, kv: KVCache, enc, lens, K: int, softmax_scale: float, *, out=None,
-                               lse=None, return_lse: bool = True, ws: Optional[Workspace] = None):
-    """svt_sparse_mla_prefill_grouped. q [T, H, 576] bf16 token-major, H * G = 128."""
+                               lse=None, return_lse: bool = True, ws: Optional[Workspace] = None,
+                               union_tile: bool = False):
+    """svt_sparse_mla_prefill_grouped (or, with union_tile, svt_sparse_mla_prefill_grouped_union_tile).
+    q [T, H, 576] bf16 token-major, H * G = 128."""
     if q.dtype != torch.bfloat16 or q.dim() != 3 or q.shape[2] != 576 or not q.is_contiguous():
         raise TypeError("q must be a contiguous bf16 [T, H, 576] tensor")
     T, H, _ = q.shape
@@ -249,10 +253,10 @@ def sparse_mla_prefill_grouped(q, G: int, kv: KVCache, enc, lens, K: int, softma
         lse = torch.empty((T, H), dtype=torch.float32, device=q.device)
     ws = (ws or default_workspace()).ensure(lib().svt_sparse_mla_prefill_grouped_workspace_size(T, H, G))
     kvc = kv._c()
-    _check(lib().svt_sparse_mla_prefill_grouped(_ptr(q), T, H, int(G), ctypes.byref(kvc), _ptr(_i32(enc, "enc")),
-                                                _ptr(_i32(lens, "lens")), int(K), float(softmax_scale), _ptr(out),
-                                                _ptr(lse), ws.ptr, ws.nbytes, _stream()),
-           "svt_sparse_mla_prefill_grouped")
+    name = "svt_sparse_mla_prefill_grouped_union_tile" if union_tile else "svt_sparse_mla_prefill_grouped"
+    _check(getattr(lib(), name)(_ptr(q), T, H, int(G), ctypes.byref(kvc), _ptr(_i32(enc, "enc")),
+                                _ptr(_i32(lens, "lens")), int(K), float(softmax_scale), _ptr(out), _ptr(lse), ws.ptr,
+                                ws.nbytes, _stream()), name)
     return out, lse
 
 

@@ -69,13 +69,14 @@ def test_decode_fp8_batch_every_query(S, dev):
     check_decode_sampled(S, w, dev, np.arange(w.T))
 
 
-def run_prefill_and_check(S, w, dev, ids):
+def run_prefill_and_check(S, w, dev, ids, union_tile=False):
     ws = S.Workspace(dev)
     slots = S.resolve_topk_slots(to_dev(w.topk, dev), block_table=to_dev(w.block_table, dev),
                                  seq_lens=to_dev(w.seq_lens, dev), req_of_token=to_dev(w.req_of_token, dev),
                                  page_size=w.page_size, num_pages=w.num_pages, ws=ws)
     enc, lens = S.build_group_union(slots, w.G, w.num_slots, ws=ws)
-    out, lse = S.sparse_mla_prefill_grouped(to_dev(w.q_bits, dev), w.G, kv_of(w, dev), enc, lens, w.K, w.scale, ws=ws)
+    out, lse = S.sparse_mla_prefill_grouped(to_dev(w.q_bits, dev), w.G, kv_of(w, dev), enc, lens, w.K, w.scale, ws=ws,
+                                            union_tile=union_tile)
     torch.cuda.synchronize()
     assert ws.read_status() == 0
     ref_slots, err = oracle.resolve(w.topk, req_of_token=w.req_of_token, block_table=w.block_table,
@@ -110,12 +111,13 @@ def stratified_groups(w, n_spread: int) -> np.ndarray:
     return np.array(ids, np.int64)
 
 
-def test_grouped_prefill_stratified(S, dev):
-    # both members of more than 128 groups (over 256 queries), every head of each
+@pytest.mark.parametrize("union_tile", [False, True], ids=["rowsets", "union_tile"])
+def test_grouped_prefill_stratified(S, dev, union_tile):
+    # both members of more than 128 groups (over 256 queries), every head of each; both kernels
     w = W.grouped_prefill()
     ids = stratified_groups(w, 130)
     assert len(ids) >= 256
-    union_lists = run_prefill_and_check(S, w, dev, ids)
+    union_lists = run_prefill_and_check(S, w, dev, ids, union_tile)
     assert 1.0 < union_lists < 2.0
 
 

@@ -52,12 +52,13 @@ def oracle_decode(w):
     return ref, ref_lse
 
 
-def gpu_prefill(S, w, dev, ws):
+def gpu_prefill(S, w, dev, ws, union_tile=False):
     slots = S.resolve_topk_slots(to_dev(w.topk, dev), block_table=to_dev(w.block_table, dev),
                                  seq_lens=to_dev(w.seq_lens, dev), req_of_token=to_dev(w.req_of_token, dev),
                                  page_size=w.page_size, num_pages=w.num_pages, ws=ws)
     enc, lens = S.build_group_union(slots, w.G, w.num_slots, ws=ws)
-    out, lse = S.sparse_mla_prefill_grouped(to_dev(w.q_bits, dev), w.G, kv_of(w, dev), enc, lens, w.K, w.scale, ws=ws)
+    out, lse = S.sparse_mla_prefill_grouped(to_dev(w.q_bits, dev), w.G, kv_of(w, dev), enc, lens, w.K, w.scale, ws=ws,
+                                            union_tile=union_tile)
     return enc, lens, out, lse
 
 
@@ -93,15 +94,19 @@ def test_decode_wait_that_runs_out_is_reported_and_the_next_call_is_correct(S, d
     assert ws.read_status() == 0
 
 
-def test_prefill_wait_that_runs_out_is_reported_and_the_next_call_is_correct(S, dev):
+@pytest.mark.parametrize("union_tile", [False, True], ids=["rowsets", "union_tile"])
+def test_prefill_wait_that_runs_out_is_reported_and_the_next_call_is_correct(S, dev, union_tile):
+    # the union tile: every CTA of every two-CTA cluster times out on its first rows, the
+    # peers then on the messages that never come; the cluster still ends and the next call
+    # on the stream is correct
     w = W.make_prefill(155, n_new=12, n_cached=150, H=64, G=2, K=160, page_size=16)
     ws = S.Workspace(dev)
     with planted_fault(S):
-        gpu_prefill(S, w, dev, ws)
+        gpu_prefill(S, w, dev, ws, union_tile)
         torch.cuda.synchronize()
     status = ws.read_status()
     assert status & S.svt.DEV_ERR_TIMEOUT, status
-    enc, lens, out, lse = gpu_prefill(S, w, dev, ws)
+    enc, lens, out, lse = gpu_prefill(S, w, dev, ws, union_tile)
     torch.cuda.synchronize()
     ref, ref_lse, err = oracle.prefill_grouped(w.q_bits, w.G, w.kv, w.kv_dtype, w.num_slots, enc.cpu().numpy(),
                                                lens.cpu().numpy(), w.K, w.scale)

@@ -319,19 +319,27 @@ def test_merge_splits_matches_oracle(S, dev):
 
 # -------------------------------------------------------------------------- grouped prefill
 
-def gpu_prefill(S, w, dev, ws):
+def gpu_prefill(S, w, dev, ws, union_tile=False):
     slots = S.resolve_topk_slots(to_dev(w.topk, dev), block_table=to_dev(w.block_table, dev),
                                  seq_lens=to_dev(w.seq_lens, dev), req_of_token=to_dev(w.req_of_token, dev),
                                  page_size=w.page_size, num_pages=w.num_pages, ws=ws)
     enc, lens = S.build_group_union(slots, w.G, w.num_slots, ws=ws)
-    out, lse = S.sparse_mla_prefill_grouped(to_dev(w.q_bits, dev), w.G, kv_of(w, dev), enc, lens, w.K, w.scale, ws=ws)
+    out, lse = S.sparse_mla_prefill_grouped(to_dev(w.q_bits, dev), w.G, kv_of(w, dev), enc, lens, w.K, w.scale, ws=ws,
+                                            union_tile=union_tile)
     return slots, enc, lens, out, lse
 
 
+# Both grouped-prefill kernels (bf16 cache): row-sets of 64 rows that walk their members'
+# entries (svt_sparse_mla_prefill_grouped) and one union tile for all 128 rows on a pair of
+# CTAs (svt_sparse_mla_prefill_grouped_union_tile).
+TILES = pytest.mark.parametrize("union_tile", [False, True], ids=["rowsets", "union_tile"])
+
+
+@TILES
 @pytest.mark.parametrize("H,G,T", [(64, 2, 13), (32, 4, 22), (16, 8, 37)])
-def test_prefill_matches_oracle(S, dev, ws, H, G, T):
+def test_prefill_matches_oracle(S, dev, ws, H, G, T, union_tile):
     w = W.make_prefill(60 + G, n_new=T, n_cached=150, H=H, G=G, K=160, page_size=16)
-    slots, enc, lens, out, lse = gpu_prefill(S, w, dev, ws)
+    slots, enc, lens, out, lse = gpu_prefill(S, w, dev, ws, union_tile)
     ref_slots, _ = oracle.resolve(w.topk, req_of_token=w.req_of_token, block_table=w.block_table,
                                   seq_lens=w.seq_lens, page_size=w.page_size, num_pages=w.num_pages)
     assert np.array_equal(slots.cpu().numpy().astype(np.int64), ref_slots)
@@ -344,8 +352,9 @@ def test_prefill_matches_oracle(S, dev, ws, H, G, T):
     assert ws.read_status() == 0
 
 
+@TILES
 @pytest.mark.parametrize("H,G", [(64, 2), (32, 4), (16, 8)])
-def test_prefill_row_sets_keep_only_their_members_entries(S, dev, ws, H, G):
+def test_prefill_row_sets_keep_only_their_members_entries(S, dev, ws, H, G, union_tile):
     # Each 64-row half of a group walks only the union entries live for one of its members.
     # Odd tokens select nothing (a half may keep no entry at all), and tokens 4 apart share
     # their lists, so some entries are live for several members and others for one.
@@ -360,7 +369,8 @@ def test_prefill_row_sets_keep_only_their_members_entries(S, dev, ws, H, G):
                                  seq_lens=to_dev(w.seq_lens, dev), req_of_token=to_dev(w.req_of_token, dev),
                                  page_size=w.page_size, num_pages=w.num_pages, ws=ws)
     enc, lens = S.build_group_union(slots, G, w.num_slots, ws=ws)
-    out, lse = S.sparse_mla_prefill_grouped(to_dev(w.q_bits, dev), G, kv_of(w, dev), enc, lens, w.K, w.scale, ws=ws)
+    out, lse = S.sparse_mla_prefill_grouped(to_dev(w.q_bits, dev), G, kv_of(w, dev), enc, lens, w.K, w.scale, ws=ws,
+                                            union_tile=union_tile)
     ref_enc, ref_lens, _ = oracle.group_union(slots.cpu().numpy(), G, w.num_slots)
     assert np.array_equal(enc.cpu().numpy(), ref_enc)
     ref, ref_lse, err = oracle.prefill_grouped(w.q_bits, G, w.kv, w.kv_dtype, w.num_slots, ref_enc, ref_lens, w.K,
@@ -368,6 +378,35 @@ def test_prefill_row_sets_keep_only_their_members_entries(S, dev, ws, H, G):
     assert err == 0
     compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
     assert torch.all(out[1::2] == 0) and torch.all(torch.isneginf(lse[1::2]))
+    assert ws.read_status() == 0
+
+
+@TILES
+@pytest.mark.parametrize("H,G", [(64, 2), (16, 8)])
+def test_prefill_rescales_and_empty_groups(S, dev, ws, H, G, union_tile):
+    # A wide score spread (softmax scale 0.5) moves the reference maximum in the middle of the
+    # lists (in the union tile, both the CTA that runs the softmax of a row and the one holding
+    # the other half of its channels rescale their O); the second group's members all select
+    # nothing (a group with no tile between groups with several), and the unions span several
+    # tiles with a ragged last one.
+    w = W.make_prefill(140 + G, n_new=3 * G, n_cached=700, H=H, G=G, K=300, page_size=16)
+    topk = w.topk.copy()
+    topk[G:2 * G] = -1
+    scale = 0.5
+    slots = S.resolve_topk_slots(to_dev(topk, dev), block_table=to_dev(w.block_table, dev),
+                                 seq_lens=to_dev(w.seq_lens, dev), req_of_token=to_dev(w.req_of_token, dev),
+                                 page_size=w.page_size, num_pages=w.num_pages, ws=ws)
+    enc, lens = S.build_group_union(slots, G, w.num_slots, ws=ws)
+    out, lse = S.sparse_mla_prefill_grouped(to_dev(w.q_bits, dev), G, kv_of(w, dev), enc, lens, w.K, scale, ws=ws,
+                                            union_tile=union_tile)
+    ref_enc, ref_lens, _ = oracle.group_union(slots.cpu().numpy(), G, w.num_slots)
+    assert np.array_equal(enc.cpu().numpy(), ref_enc)
+    assert ref_lens[1] == 0 and ref_lens[0] > 4 * 64 and ref_lens[0] % 64 != 0
+    ref, ref_lse, err = oracle.prefill_grouped(w.q_bits, G, w.kv, w.kv_dtype, w.num_slots, ref_enc, ref_lens, w.K,
+                                               scale)
+    assert err == 0
+    compare(out, lse, ref, ref_lse, BF16_OUT_TOL)
+    assert torch.all(out[G:2 * G] == 0) and torch.all(torch.isneginf(lse[G:2 * G]))
     assert ws.read_status() == 0
 
 
@@ -394,24 +433,27 @@ def test_prefill_row_set_counts_bit_exact(S, dev, H, G, T):
     assert ws.read_status() == 0
 
 
-def test_prefill_equals_per_query_decode_on_gpu(S, dev, ws):
+@TILES
+def test_prefill_equals_per_query_decode_on_gpu(S, dev, ws, union_tile):
     w = W.make_prefill(70, n_new=9, n_cached=300, H=64, G=2, K=200, page_size=64)
-    _, _, _, out, lse = gpu_prefill(S, w, dev, ws)
+    _, _, _, out, lse = gpu_prefill(S, w, dev, ws, union_tile)
     out_d, lse_d = gpu_decode(S, w, dev, ws)
     assert float((out.float() - out_d.float()).abs().max()) <= BF16_OUT_TOL
     assert float((lse - lse_d).abs().max()) <= LSE_TOL
 
 
-def test_prefill_membership_bit_negative_control(S, dev, ws):
+@TILES
+def test_prefill_membership_bit_negative_control(S, dev, ws, union_tile):
     # A flipped membership bit must change that member's rows: the parity check has teeth.
     w = W.make_prefill(71, n_new=4, n_cached=400, H=64, G=2, K=128, page_size=64)
-    slots, enc, lens, out, lse = gpu_prefill(S, w, dev, ws)
+    slots, enc, lens, out, lse = gpu_prefill(S, w, dev, ws, union_tile)
     e = enc.clone()
     row = e[0, : int(lens[0])]
     has1 = ((row.view(torch.int32) >> 24) & 2) != 0
     idx = int(torch.nonzero(~has1)[0])
     e[0, idx] = row[idx] | (2 << 24)
-    out2, lse2 = S.sparse_mla_prefill_grouped(to_dev(w.q_bits, dev), w.G, kv_of(w, dev), e, lens, w.K, w.scale, ws=ws)
+    out2, lse2 = S.sparse_mla_prefill_grouped(to_dev(w.q_bits, dev), w.G, kv_of(w, dev), e, lens, w.K, w.scale, ws=ws,
+                                              union_tile=union_tile)
     assert float((lse2[1] - lse[1]).abs().max()) > LSE_TOL
     assert torch.equal(out2[0], out[0])
 
