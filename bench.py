@@ -661,6 +661,46 @@ def analyse_trace(tr: np.ndarray) -> dict:
     return out
 
 
+PAIR_TRACE_FROM = 1000  # the union-tile kernel stamps tiles 1000 .. 1047 of each CTA (pair_prefill.cu)
+
+
+def analyse_pair_trace(tr: np.ndarray) -> dict:
+    """Per-step times (µs) of the union-tile prefill kernel from one traced launch: tiles
+    PAIR_TRACE_FROM .. + 47 of each CTA, the middle of a long launch (see the slot map in
+    pair_prefill.cu). Medians over CTAs and tiles."""
+    tr = tr.astype(np.int64)
+    ctas = tr[tr[:, 1] != 0]
+    if len(ctas) == 0:
+        return {"ctas": 0}
+    gt0, c0, gt1, c9 = ctas[:, 0], ctas[:, 1], ctas[:, 15], ctas[:, 9]
+    ghz = float(np.median((c9 - c0) / np.maximum(gt1 - gt0, 1)))
+    ev = ctas[:, TRACE_HEAD:].reshape(len(ctas), TRACE_G, TRACE_EV).astype(np.float64)
+
+    def step(ea, eb, off=0):
+        vals = []
+        for k in range(2, TRACE_G - 4):
+            a, b = ev[:, k, ea], ev[:, k + off, eb]
+            ok = (a > 1) & (b > 1)
+            vals.extend(((b - a)[ok] / ghz / 1e3).tolist())
+        return float(np.median(vals)) if vals else None
+
+    moved = ev[:, 2:TRACE_G - 4, 0]
+    return {"ctas": int(len(ctas)), "sm_ghz": ghz, "tiles": f"{PAIR_TRACE_FROM}..{PAIR_TRACE_FROM + TRACE_G - 1}",
+            "launch_span_us": float(gt1.max() - gt0.min()) / 1e3,
+            "tile_period_us": step(2, 2, 1),
+            "s_issuer_rows_landed_to_s_issued_us": step(1, 2),
+            "s_issued_to_next_rows_landed_us": step(2, 1, 1),
+            "softmax_sees_s_to_peer_partial_us": step(3, 4),
+            "softmax_partial_to_p_buffer_free_us": step(4, 11),
+            "softmax_p_rows_stored_us": step(11, 6),
+            "softmax_fence_barrier_arrive_us": step(6, 10),
+            "softmax_loop_us": step(3, 3, 1),
+            "pv_own_p_to_peer_p_us": step(7, 8),
+            "pv_peer_p_to_issued_us": step(8, 9),
+            "pv_issued_to_rows_landed_3_tiles_on_us": step(9, 1, 3),
+            "tiles_moving_maxima": float((moved == 1).mean())}
+
+
 def run_phase_trace(args):
     """Builds the phase-trace library, runs the bf16 decode batch, the e4m3 batch and the
     grouped prefill once each (after warm-up and an L2 flush) and prints per-phase times."""
@@ -710,6 +750,17 @@ def run_phase_trace(args):
     enc, lens = S.build_group_union(slots, pw.G, pw.num_slots, ws=ws)
     traced(lambda: S.sparse_mla_prefill_grouped(d["q"], pw.G, d["kv"], enc, lens, pw.K, pw.scale, ws=ws),
            "prefill_bf16")
+    # the union-tile kernel: its own slot map, mid-launch tiles
+    for _ in range(3):
+        S.sparse_mla_prefill_grouped(d["q"], pw.G, d["kv"], enc, lens, pw.K, pw.scale, ws=ws, union_tile=True)
+    torch.cuda.synchronize()
+    buf.zero_()
+    L.svt_trace_attach(ctypes.c_void_p(buf.data_ptr()), buf.numel() * 8)
+    flush()
+    S.sparse_mla_prefill_grouped(d["q"], pw.G, d["kv"], enc, lens, pw.K, pw.scale, ws=ws, union_tile=True)
+    torch.cuda.synchronize()
+    L.svt_trace_attach(None, 0)
+    res["prefill_bf16_union_tile"] = analyse_pair_trace(buf.cpu().numpy())
     print(json.dumps(res), flush=True)
 
 

@@ -87,8 +87,9 @@ constexpr int kOffStage = 0;
 constexpr int kOffP = kOffStage + kStages * kStageBytes;   // P buffer j at + j * kPBytes
 constexpr int kOffQRope = kOffP + kPBufs * kPBytes;        // Q's 32 rope channels, 128 rows (64-byte swizzle)
 constexpr int kOffRecv = kOffQRope + 128 * 64;             // float[2][64][64], swizzled
-// A P message's header: the rescale factors of the sender's 64 rows and whether any moved.
-constexpr int kHdrBytes = 64 * 4 + 16;                     // float alpha[64]; int flag; pad
+// A P message's header: the rescale factors of the sender's 64 rows and, per TMEM quadrant,
+// whether any of its 16 rows moved.
+constexpr int kHdrBytes = 64 * 4 + 16;                     // float alpha[64]; int flag[4]
 constexpr int kOffHdrRecv = kOffRecv + 2 * kRecvBytes;     // [3] headers from the peer
 constexpr int kOffHdrOut = kOffHdrRecv + kPBufs * kHdrBytes;  // [3] headers to the peer
 constexpr int kOffLRecv = kOffHdrOut + kPBufs * kHdrBytes; // float[64]: the peer's row sums
@@ -125,8 +126,10 @@ constexpr int kBarRescaled = 39;    // the send warps rescaled their rows of O f
 constexpr int kBarDrain = 40;       // both issuers' last commits
 static_assert(kBarDrain < kNumBars, "");
 
-constexpr int kNamedBarSm = 1;  // the eight softmax warps
-constexpr int kSmThreads = kOwnWarps * 32;
+// The two softmax warps of quadrant q (the same 16 rows, column halves) agree through named
+// barrier 1 + q.
+constexpr int kNamedBarPair0 = 1;
+constexpr int kPairThreads = 64;
 
 constexpr int kTmemCols = 512;
 constexpr int kTmemQ = 0;    // Q_c's latent blocks: 32 columns per 64 channels (two bf16 a column)
@@ -407,7 +410,8 @@ __device__ void pv_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem
       mbar_arrive_expect_tx(bar(kBarPRecv + j), kPRecvBytes);
       if (!mbar_wait_cluster(bar(kBarPRecv + j), jph, wc)) return;
       PTRACE_G(8, k);
-      if (*reinterpret_cast<const volatile int*>(smem + kOffHdrRecv + j * kHdrBytes + 256) != 0) {
+      const volatile int* flags = reinterpret_cast<const volatile int*>(smem + kOffHdrRecv + j * kHdrBytes + 256);
+      if ((flags[0] | flags[1] | flags[2] | flags[3]) != 0) {
         if (!mbar_wait<true>(bar(kBarRescaled), nresc & 1u, wc)) return;
         ++nresc;
       }
@@ -579,12 +583,16 @@ __device__ void row_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint
     const uint32_t jp = kp % kPBufs;
     mbar_wait_cluster(bar(kBarPRecv + jp), (kp / kPBufs) & 1u, wc);
     const uint8_t* hdr = smem + kOffHdrRecv + jp * kHdrBytes;
-    if (*reinterpret_cast<const volatile int*>(hdr + 256) != 0) {
-      const uint32_t kq = kp - 1;
-      mbar_wait<true>(bar(kBarPvDone + (kq & 1u)), (kq >> 1) & 1u, wc);
-      tc_fence_after();
-      rescale_o16(lane16 + kTmemO, 8, reinterpret_cast<const volatile float*>(hdr)[rl]);
-      tc_fence_before();
+    const volatile int* flags = reinterpret_cast<const volatile int*>(hdr + 256);
+    if ((flags[0] | flags[1] | flags[2] | flags[3]) != 0) {
+      // the PV issuer waits for all four send warps; those whose quadrant moved rescale first
+      if (flags[q] != 0) {
+        const uint32_t kq = kp - 1;
+        mbar_wait<true>(bar(kBarPvDone + (kq & 1u)), (kq >> 1) & 1u, wc);
+        tc_fence_after();
+        rescale_o16(lane16 + kTmemO, 8, reinterpret_cast<const volatile float*>(hdr)[rl]);
+        tc_fence_before();
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kBarRescaled));
     }
@@ -662,7 +670,7 @@ __device__ void row_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint
         bool exceed = false;
 #pragma unroll
         for (int c = 0; c < 16; ++c) exceed |= x[c] > m + kTau;
-        const bool any = !named_bar_red_and(kNamedBarSm, kSmThreads, !exceed);
+        const bool any = !named_bar_red_and(kNamedBarPair0 + q, kPairThreads, !exceed);
 #ifdef SVT_PHASE_TRACE
         if (arm_own && any && p.trace != nullptr && k >= kTraceFrom && k - kTraceFrom < static_cast<uint32_t>(kTraceG))
           p.trace[static_cast<long long>(blockIdx.x) * kTraceSlots + kTraceHead + (k - kTraceFrom) * kTraceEv + 0] = 1;
@@ -676,9 +684,9 @@ __device__ void row_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint
           for (int c = 1; c < 16; ++c) mx = fmaxf(mx, x[c]);
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
           red[ch * 64 + rl] = mx;
-          named_bar_sync(kNamedBarSm, kSmThreads);
+          named_bar_sync(kNamedBarPair0 + q, kPairThreads);
           const float mn = fmaxf(m, fmaxf(mx, red[(ch ^ 1) * 64 + rl]));
-          named_bar_sync(kNamedBarSm, kSmThreads);  // red is rewritten by the next tile
+          named_bar_sync(kNamedBarPair0 + q, kPairThreads);  // red is rewritten by the next tile
           alpha = (m == -CUDART_INF_F) ? 0.f : ex2_approx(m - mn);
           m = mn;
           l *= alpha;
@@ -716,12 +724,14 @@ __device__ void row_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint
         // rescaling (a later tile of the group only)
         uint8_t* hdr_out = smem + kOffHdrOut + pj * kHdrBytes;
         if (ch == 0 && cp == 0) reinterpret_cast<float*>(hdr_out)[rl] = alpha;
-        if (arm_own) *reinterpret_cast<int*>(hdr_out + 256) = (any && t > 0) ? 1 : 0;
-        fence_proxy_async_smem();  // local P rows and header -> MMA operand reads and the bulk copies
+        if (ch == 0 && lane == 0) reinterpret_cast<int*>(hdr_out + 256)[q] = (any && t > 0) ? 1 : 0;
+        // local P rows and header -> MMA operand reads and the bulk copies, which the PV issuer
+        // starts once all eight softmax warps have arrived
+        fence_proxy_async_smem();
         tc_fence_before();
-        named_bar_sync(kNamedBarSm, kSmThreads);
+        __syncwarp();
         if (arm_own) PTRACE_G(10, k);
-        if (lane == 0) mbar_arrive(bar(kBarPReady + pj));  // the PV issuer also sends them to the peer
+        if (lane == 0) mbar_arrive(bar(kBarPReady + pj));
         if (arm_own) PTRACE_G(5, k);
       } else {
         // ---------------------------------------------------------------- the peer's rows
@@ -765,7 +775,7 @@ __device__ void row_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint
     float lt;
     if (own) {
       lsum[ch * 64 + rl] = l + __shfl_xor_sync(0xffffffffu, l, 2);
-      named_bar_sync(kNamedBarSm, kSmThreads);
+      named_bar_sync(kNamedBarPair0 + q, kPairThreads);
       lt = lsum[rl] + lsum[64 + rl];
       if (ch == 0 && cp == 0) {
         if (!*wc.abort_flag) st_async_b32(l_peer + rl * 4, __float_as_uint(lt), peer_bar(kBarLRecv));
