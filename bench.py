@@ -697,7 +697,7 @@ def analyse_pair_trace(tr: np.ndarray) -> dict:
             "softmax_loop_us": step(3, 3, 1),
             "pv_own_p_to_peer_p_us": step(7, 8),
             "pv_peer_p_to_issued_us": step(8, 9),
-            "pv_issued_to_rows_landed_3_tiles_on_us": step(9, 1, 3),
+            "pv_issued_to_rows_landed_4_tiles_on_us": step(9, 1, 4),
             "tiles_moving_maxima": float((moved == 1).mean())}
 
 
