@@ -691,9 +691,10 @@ def analyse_pair_trace(tr: np.ndarray) -> dict:
             "s_issuer_rows_landed_to_s_issued_us": step(1, 2),
             "s_issued_to_next_rows_landed_us": step(2, 1, 1),
             "softmax_sees_s_to_peer_partial_us": step(3, 4),
-            "softmax_partial_to_p_buffer_free_us": step(4, 11),
+            "softmax_partial_to_masks_us": step(4, 5),
+            "softmax_masks_to_maxima_agreed_us": step(5, 10),
+            "softmax_agreed_to_p_buffer_free_us": step(10, 11),
             "softmax_p_rows_stored_us": step(11, 6),
-            "softmax_fence_barrier_arrive_us": step(6, 10),
             "softmax_loop_us": step(3, 3, 1),
             "pv_own_p_to_peer_p_us": step(7, 8),
             "pv_peer_p_to_issued_us": step(8, 9),

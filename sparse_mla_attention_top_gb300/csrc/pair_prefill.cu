@@ -187,11 +187,11 @@ __device__ __forceinline__ int union_len(const AttnParams& p, int g) {
 
 // Phase trace (compiled only with SVT_PHASE_TRACE, into the trace build of the library): per
 // CTA the header slots 0 start (%globaltimer), 1 start, 2 set-up done, 7 roles done, 9 end,
-// 15 end (%globaltimer), and for each of kTraceG tiles from its kTraceFrom-th: 0 1 if the softmax moved its
-// reference maxima, 1 rows landed, 2 S MMAs issued, 3 softmax sees S, 4 the peer's partial
-// landed, 5 own P rows written and sent, 6 softmax has the tile's masks, 7 PV issuer sees own P
-// rows, 8 sees the peer's, 9 PV issued, 10 softmax agreed whether to move maxima, 11 softmax
-// past the P buffer's free wait.
+// 15 end (%globaltimer), and for each of kTraceG tiles from its kTraceFrom-th: 0 1 if the
+// softmax moved its reference maxima, 1 rows landed, 2 S MMAs issued, 3 softmax sees S, 4 the
+// peer's partial landed, 5 the tile's live masks ready, 6 own P rows stored, 7 PV issuer sees
+// own P rows, 8 sees the peer's, 9 PV issued, 10 softmax warps of a quadrant agreed whether to
+// move maxima, 11 softmax past the P buffer's free wait.
 #ifdef SVT_PHASE_TRACE
 __device__ __forceinline__ void ptrace_at(const AttnParams& p, int slot, unsigned long long v) {
   if (p.trace != nullptr) p.trace[static_cast<long long>(blockIdx.x) * kTraceSlots + slot] = v;
@@ -651,6 +651,7 @@ __device__ void row_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint
           }
         }
         mbar_wait<true>(bar(kBarSlotsReady + ring), (k / kRing) & 1u, wc);
+        if (arm_own) PTRACE_G(5, k);
         {
           // x[i]: column 32 ch + 2 i + cp; the member's live entries of this half
           const uint32_t wl = live_tab[(ring * 8 + member) * 2 + ch] >> cp;
@@ -671,6 +672,7 @@ __device__ void row_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint
 #pragma unroll
         for (int c = 0; c < 16; ++c) exceed |= x[c] > m + kTau;
         const bool any = !named_bar_red_and(kNamedBarPair0 + q, kPairThreads, !exceed);
+        if (arm_own) PTRACE_G(10, k);
 #ifdef SVT_PHASE_TRACE
         if (arm_own && any && p.trace != nullptr && k >= kTraceFrom && k - kTraceFrom < static_cast<uint32_t>(kTraceG))
           p.trace[static_cast<long long>(blockIdx.x) * kTraceSlots + kTraceHead + (k - kTraceFrom) * kTraceEv + 0] = 1;
@@ -730,9 +732,7 @@ __device__ void row_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, uint
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
-        if (arm_own) PTRACE_G(10, k);
         if (lane == 0) mbar_arrive(bar(kBarPReady + pj));
-        if (arm_own) PTRACE_G(5, k);
       } else {
         // ---------------------------------------------------------------- the peer's rows
         uint32_t sv[32];
