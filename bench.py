@@ -67,6 +67,8 @@ TRAFFIC_BY_SOURCE = {
     "895581153be257dc": (157.544448e6, 61.046272e6, "256 MB write"),
     # the prefill kernels' mode fixed at compile time (the decode kernels' code unchanged)
     "3b8854cb7d11f6cb": (157.325568e6, 61.010432e6, "256 MB write"),
+    # the API source with the union-tile prefill's entry point (the decode kernels unchanged)
+    "89f3154b7fd2c791": (157.413888e6, 60.970496e6, "256 MB write"),
 }
 
 
