@@ -28,17 +28,20 @@
 //   - O_c[128 x 256] += P . V_c (M = 128, N = 256, 4 MMAs of K = 16; P K-major, V MN-major).
 // Every MMA has M = 128 and N >= 64; none runs at M = 64.
 //
-// Warp roles (512 threads per CTA):
-//   warps 0-7   row warps: warp w reads TMEM lanes 32 (w % 4) .. + 31 (rows of the tile) and
-//               score columns / O channels of half w / 4. Warps whose rows this CTA owns run
-//               the softmax and the epilogue of their rows; the others send those rows'
-//               partial scores to the peer, look at the peer's message of the tile before (a
-//               flagged one has them rescale their rows of this CTA's O) and normalise those
-//               rows at the end. All of them load Q_c into TMEM.
-//   warp 8      S issuer (lane 0), warp 9 PV issuer (lane 0).
-//   warps 10-11 resolvers: one union entry per thread into a ring of slot / mask tables, each
-//               resolved row's bytes of this CTA bulk-prefetched into L2.
-//   warps 12-15 fillers: cp.async of the tile's rows into a stage as soon as PV frees it.
+// Warp roles (640 threads per CTA):
+//   warps 0-7   softmax of this CTA's 64 rows: lanes 32 q + 16 c .. + 15 of TMEM quadrant
+//               q = w % 4 (so the rows spread over the four SM sub-partitions), score columns
+//               and O channels of half w / 4, read with the 16-lane load shape (two threads a
+//               row); they also write the rows' P and, at the end of a group, their output.
+//   warps 8-11  the peer's 64 rows in quadrant w % 4: send those rows' partial scores to the
+//               peer, take the peer's P message two tiles behind (a flagged one has them
+//               rescale those rows of this CTA's O) and normalise those rows at the end.
+//               All twelve row warps load Q_c into TMEM at each group's start.
+//   warp 12     S issuer (lane 0); warp 13 PV issuer (lane 0), which also sends this CTA's P
+//               rows and header to the peer by bulk copies once they are written.
+//   warps 14-15 resolvers: one union entry per thread into a ring of slot tables and, per
+//               member, 64-bit masks of the tile's entries it selected.
+//   warps 16-19 fillers: cp.async of the tile's rows into a stage as soon as PV frees it.
 // Every wait is bounded (2 s, or the launch's limit); the status word records range errors
 // and timeouts. Neither CTA leaves while messages to it may still be in flight (two final
 // cluster barriers around a measured wait), so no message addresses a CTA that has exited.
