@@ -98,6 +98,29 @@ def test_prefill_rejects_unsupported_shapes(L):
     assert call(64, 2, _kv(pages=(1 << 24) // 64, page_size=64)) == svt.SVT_ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("entry", ["svt_sparse_mla_prefill_grouped", "svt_sparse_mla_prefill_grouped_union_tile"])
+def test_both_prefill_entry_points_check_arguments_before_enqueueing(L, entry):
+    # The same host checks run for the row-set and the union-tile kernel; a failed one returns
+    # before anything is enqueued (no device here: any launch would fail differently).
+    kv = _kv()
+    fn = getattr(L, entry)
+    call = lambda H=64, G=2, kvd=kv, ws_bytes=1 << 20, q=0x20000, scale=0.04: fn(  # noqa: E731
+        ctypes.c_void_p(q) if q else None, 8, H, G, ctypes.byref(kvd), ctypes.c_void_p(0x40000),
+        ctypes.c_void_p(0x50000), 2048, ctypes.c_float(scale), ctypes.c_void_p(0x30000), None, WS, ws_bytes, None)
+    assert call(H=64, G=4) == svt.SVT_ERR_UNSUPPORTED
+    assert call(ws_bytes=8) == svt.SVT_ERR_WORKSPACE
+    assert call(q=0) == svt.SVT_ERR_INVALID_ARG
+    assert call(scale=float("inf")) == svt.SVT_ERR_INVALID_ARG
+
+
+def test_union_tile_prefill_takes_a_bf16_cache(L):
+    kv = _kv(dtype=svt.KV_FP8_E4M3)
+    st = L.svt_sparse_mla_prefill_grouped_union_tile(
+        ctypes.c_void_p(0x20000), 8, 64, 2, ctypes.byref(kv), ctypes.c_void_p(0x40000), ctypes.c_void_p(0x50000),
+        2048, ctypes.c_float(0.04), ctypes.c_void_p(0x30000), None, WS, 1 << 20, None)
+    assert st == svt.SVT_ERR_UNSUPPORTED and "bf16" in _err(L)
+
+
 def test_union_rejects_unsupported_arguments(L):
     call = lambda T=8, K=16, G=2, ns=1000, ws_bytes=1 << 20: L.svt_build_group_union(  # noqa: E731
         ctypes.c_void_p(0x20000), None, T, K, G, ns, ctypes.c_void_p(0x30000), ctypes.c_void_p(0x40000), WS,
