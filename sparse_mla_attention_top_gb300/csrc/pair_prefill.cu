@@ -17,14 +17,15 @@
 //   - S_c[128 x 64] = Q_c . K_c^T (M = 128, N = 64; 18 MMAs of K = 16), double-buffered in
 //     TMEM; Q_c's latent channels are held in TMEM as the MMA's A operand, its rope channels in
 //     shared memory (TMEM has no room for them beside two S buffers and O_c);
-//   - rows 0-63 belong to CTA 0's softmax and rows 64-127 to CTA 1's: each CTA sends the other
-//     its partial scores of the other's rows (fp32, 16 KB, st.async into one of the peer's two
-//     receive buffers), adds the peer's partial of its own rows, and runs the online softmax on
-//     them;
-//   - the bf16 P rows (8 KB) go into this CTA's P buffer and, by st.async, the peer's, so that
-//     both hold P for all 128 rows; the PV issuer waits for the peer's rows itself. When the
-//     softmax moves a row's reference maximum, the message carries a flag and the rescale
-//     factors, and the CTA holding the other half of those rows' O rescales it before PV;
+//   - CTA c runs the softmax of 64 of the rows (lanes 32 q + 16 c .. + 15 of each TMEM quadrant
+//     q): each CTA sends the other its partial scores of the other's rows (fp32, 16 KB,
+//     st.async into one of the peer's two receive buffers), adds the peer's partial of its own
+//     rows, and runs the online softmax on them;
+//   - the bf16 P rows go into this CTA's P buffer, and the PV issuer sends them (8 KB, bulk
+//     copies) into the peer's, so that both hold P for all 128 rows; it then waits for the
+//     peer's rows itself. When the softmax moves a row's reference maximum, the message's
+//     header carries a flag and the rescale factors, and the CTA holding the other half of
+//     those rows' O rescales it before PV;
 //   - O_c[128 x 256] += P . V_c (M = 128, N = 256, 4 MMAs of K = 16; P K-major, V MN-major).
 // Every MMA has M = 128 and N >= 64; none runs at M = 64.
 //
@@ -89,12 +90,12 @@ static_assert(kFillThreads == 2 * kTile, "each filler thread copies one 16-byte 
 constexpr int kOffStage = 0;
 constexpr int kOffP = kOffStage + kStages * kStageBytes;   // P buffer j at + j * kPBytes
 constexpr int kOffQRope = kOffP + kPBufs * kPBytes;        // Q's 32 rope channels, 128 rows (64-byte swizzle)
-constexpr int kOffRecv = kOffQRope + 128 * 64;             // float[2][64][64], swizzled
+constexpr int kOffRecv = kOffQRope + 128 * 64;             // [2] the peer's partial scores (16 KB each)
 // A P message's header: the rescale factors of the sender's 64 rows and, per TMEM quadrant,
 // whether any of its 16 rows moved.
 constexpr int kHdrBytes = 64 * 4 + 16;                     // float alpha[64]; int flag[4]
-constexpr int kOffHdrRecv = kOffRecv + 2 * kRecvBytes;     // [3] headers from the peer
-constexpr int kOffHdrOut = kOffHdrRecv + kPBufs * kHdrBytes;  // [3] headers to the peer
+constexpr int kOffHdrRecv = kOffRecv + 2 * kRecvBytes;     // [kPBufs] headers from the peer
+constexpr int kOffHdrOut = kOffHdrRecv + kPBufs * kHdrBytes;  // [kPBufs] headers to the peer
 constexpr int kOffLRecv = kOffHdrOut + kPBufs * kHdrBytes; // float[64]: the peer's row sums
 constexpr int kOffSlot = kOffLRecv + 64 * 4;               // int[4][64]
 constexpr int kOffLive = kOffSlot + kRing * kTile * 4;     // uint32[4][8][2]: per member, the live entries
@@ -107,11 +108,12 @@ constexpr int kSmemUsed = kOffMisc + 16;
 constexpr int kSmemBytes = kSmemUsed + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory map exceeds 227 KB");
 static_assert(kOffQRope % 1024 == 0, "swizzled operand blocks start on 1024-byte boundaries");
+static_assert(kStages <= 4 && kPBufs <= 3, "barrier index map");
 
 // barriers
-constexpr int kBarFull = 0;         // 3: stage s holds its tile's rows (cp.async arrivals)
-constexpr int kBarEmpty = 4;        // 3: PV done with stage s
-constexpr int kBarSlotsReady = 8;   // 4: ring entry holds a tile's slots and masks
+constexpr int kBarFull = 0;         // kStages: stage s holds its tile's rows (cp.async arrivals)
+constexpr int kBarEmpty = 4;        // kStages: PV done with stage s
+constexpr int kBarSlotsReady = 8;   // 4: ring entry holds a tile's slots and live masks
 constexpr int kBarSlotFree = 12;    // 4: fillers and softmax are done with the ring entry
 constexpr int kBarQFull = 16;       // Q_c of the group is in TMEM
 constexpr int kBarQEmpty = 17;      // the group's last S MMA is done with Q_c
@@ -119,9 +121,9 @@ constexpr int kBarSFull = 18;       // 2: S_c of the tile is in TMEM buffer b
 constexpr int kBarSFree = 20;       // 2: every row warp has read S_c buffer b
 constexpr int kBarSPart = 22;       // 2: the peer's partial scores of this CTA's rows landed in buffer b
 constexpr int kBarRecvFree = 24;    // 2: the peer has read receive buffer b of this CTA's messages
-constexpr int kBarPFree = 26;       // 3: PV of both CTAs done with P buffer j (multicast commits)
-constexpr int kBarPRecv = 29;       // 3: the peer's P rows, rescale factors and flag landed in buffer j
-constexpr int kBarPReady = 32;      // 3: this CTA's own P rows (and O rescale) are in buffer j
+constexpr int kBarPFree = 26;       // kPBufs: PV of both CTAs done with P buffer j (multicast commits)
+constexpr int kBarPRecv = 29;       // kPBufs: the peer's P rows and header landed in buffer j
+constexpr int kBarPReady = 32;      // kPBufs: this CTA's own P rows (and O rescale) are in buffer j
 constexpr int kBarPvDone = 35;      // 2: PV of the tile k done (k % 2)
 constexpr int kBarOFree = 37;       // the group's epilogue has read O_c
 constexpr int kBarLRecv = 38;       // the peer's final row sums landed
@@ -249,7 +251,10 @@ __device__ void resolver_role(const AttnParams& p, uint8_t* smem, uint32_t bars,
         }
       }
       const uint32_t r = k % kRing;
-      if (k >= kRing && !mbar_wait<true>(bar(kBarSlotFree + r), ((k / kRing) - 1) & 1u, wc)) {
+      // the warp leaves together (a timed-out wait may be seen by some lanes only) before the
+      // ballots below
+      const bool freed = k < kRing || mbar_wait<true>(bar(kBarSlotFree + r), ((k / kRing) - 1) & 1u, wc);
+      if (!__all_sync(0xffffffffu, freed)) {
         live = false;
         break;
       }
@@ -282,7 +287,8 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, u
   while (live && walk.next(p, g, nt)) {
     for (int t = 0; t < nt; ++t, ++k) {
       const uint32_t r = k % kRing, st = k % kStages;
-      if (!mbar_wait<true>(bar(kBarSlotsReady + r), (k / kRing) & 1u, wc)) {
+      // each wait's outcome is made warp-uniform: the warp leaves together before __syncwarp
+      if (!__all_sync(0xffffffffu, mbar_wait<true>(bar(kBarSlotsReady + r), (k / kRing) & 1u, wc))) {
         live = false;
         break;
       }
@@ -298,7 +304,7 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, u
         nbytes[j] = slot >= 0 ? 16u : 0u;
         dst[j] = stage + sw128_offset(row, chunk);
       }
-      if (k >= kStages && !mbar_wait<true>(bar(kBarEmpty + st), ((k / kStages) - 1) & 1u, wc)) {
+      if (!__all_sync(0xffffffffu, k < kStages || mbar_wait<true>(bar(kBarEmpty + st), ((k / kStages) - 1) & 1u, wc))) {
         live = false;
         break;
       }
