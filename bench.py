@@ -582,12 +582,15 @@ def public(item: dict) -> dict:
 
 # ------------------------------------------------------------------------------ phase trace
 
-TRACE_HEAD, TRACE_G, TRACE_EV = 48, 48, 12
+TRACE_HEAD, TRACE_G, TRACE_EV = 48, 48, 16
+TRACE_PREFILL_FROM = 1000  # grouped-prefill launches stamp half-tiles 1000 .. 1047 (attention.cu)
 
 
-def analyse_trace(tr: np.ndarray) -> dict:
+def analyse_trace(tr: np.ndarray, window: bool = False) -> dict:
     """Per-phase times (µs) from the stamps of one traced launch ([CTAs, slots] uint64): see
-    the slot map in attention.cu. Medians over CTAs (and over half-tiles where per half-tile)."""
+    the slot map in attention.cu. Medians over CTAs (and over half-tiles where per half-tile).
+    window: the stamps are of half-tiles from the middle of the launch (grouped prefill), so
+    the first half-tile's times are not reported."""
     tr = tr.astype(np.int64)
     ctas = tr[tr[:, 0] != 0]
     if len(ctas) == 0:
@@ -609,14 +612,14 @@ def analyse_trace(tr: np.ndarray) -> dict:
     if np.any(ok):
         out["first_slots_resolved_us"] = float(np.median([us(x) for x in (first_slots - c0)[ok]]))
     has0 = ev[:, 0, 1] != 0
-    if np.any(has0):
+    if np.any(has0) and not window:
         out["first_rows_landed_us"] = float(np.median([us(x) for x in (ev[has0, 0, 1] - c0[has0])]))
         out["first_s_issued_us"] = float(np.median([us(x) for x in (ev[has0, 0, 2] - c0[has0])]))
         out["first_p_written_us"] = float(np.median([us(x) for x in (ev[has0, 0, 4] - c0[has0])]))
     periods, fill_lat, s_lat, sm_lat, pv_gap, wait_rows, wait_buf = [], [], [], [], [], [], []
     sm_ld, sm_bar, sm_exp, sm_arrive = [], [], [], []
     for i in range(len(ctas)):
-        n = int(min(n_half[i], TRACE_G))
+        n = int(np.count_nonzero(ev[i, :, 2])) if window else int(min(n_half[i], TRACE_G))
         if n < 4:
             continue
         e = ev[i, :n]
@@ -640,7 +643,7 @@ def analyse_trace(tr: np.ndarray) -> dict:
                 "softmax_tmem_load_us": med(sm_ld), "softmax_scale_max_us": med(sm_bar),
                 "softmax_exp_store_us": med(sm_exp), "softmax_fence_arrive_us": med(sm_arrive)})
     last_p = []
-    for i in range(len(ctas)):
+    for i in range(len(ctas) if not window else 0):
         n = int(min(n_half[i], TRACE_G))
         if n > 0 and n_half[i] <= TRACE_G:
             last_p.append(ctas[i, 7] - ev[i, n - 1, 4])
@@ -660,6 +663,75 @@ def analyse_trace(tr: np.ndarray) -> dict:
             out["cluster_merge_steps_us"] = {name: med((m[:, b] - m[:, a]).tolist()) for name, a, b in steps}
     out["roles_done_us"] = float(np.median(rel(ctas[:, 7])))
     out["end_us"] = float(np.median(rel(ctas[:, 9])))
+    return out
+
+
+def analyse_boundaries(tr: np.ndarray) -> dict:
+    """What a row-set switch costs in the middle of a grouped-prefill launch: for each traced
+    half-tile that opens a segment (stamp 12 = 1) with three more after it, the S^T issue
+    times around it against the launch's steady half-tile period, and the steps the switch
+    waits for (µs, medians over the switches of all CTAs)."""
+    tr = tr.astype(np.int64)
+    ctas = tr[tr[:, 0] != 0]
+    if len(ctas) == 0:
+        return {"switches": 0}
+    gt0, c0, gt1, c9 = ctas[:, 0], ctas[:, 1], ctas[:, 15], ctas[:, 9]
+    ghz = float(np.median((c9 - c0) / np.maximum(gt1 - gt0, 1)))
+    us = lambda cyc: float(cyc) / ghz / 1e3  # noqa: E731
+    ev = ctas[:, TRACE_HEAD:].reshape(len(ctas), TRACE_G, TRACE_EV)
+    inner, cols = [], {k: [] for k in ("period_into", "period_1", "period_2", "period_3", "extra_over_4",
+                                      "epilogue", "first_p_to_pv", "first_s_done_to_epilogue_done",
+                                      "first_softmax", "s_issue_after_prev", "first_rows_wait",
+                                      "prev_s_issued_to_q_issued", "q_issued_to_q_seen", "q_seen_to_s_issued",
+                                      "prev_s_done_to_q_issued", "q_seen_to_buffer_free", "rows_to_fenced",
+                                      "fenced_to_s_accepted", "prev_pv_issued_to_s_accepted",
+                                      "prev_p_to_prev_pv_issued", "steady_fenced_to_s_accepted")}
+    seg_len = []
+    for i in range(len(ctas)):
+        e = ev[i]
+        n = int(np.count_nonzero(e[:, 2]))
+        idx = e[:n, 12]
+        for k in range(1, n):
+            if idx[k] > 1 and idx[k - 1] >= 1:
+                inner.append(e[k, 2] - e[k - 1, 2])
+        for k in range(1, n - 3):
+            if idx[k] != 1 or idx[k - 1] < 1 or not np.all(idx[k + 1:k + 4] > 1):
+                continue
+            seg_len.append(int(idx[k - 1]))
+            cols["period_into"].append(e[k, 2] - e[k - 1, 2])
+            cols["period_1"].append(e[k + 1, 2] - e[k, 2])
+            cols["period_2"].append(e[k + 2, 2] - e[k + 1, 2])
+            cols["period_3"].append(e[k + 3, 2] - e[k + 2, 2])
+            cols["extra_over_4"].append(e[k + 3, 2] - e[k - 1, 2])
+            cols["epilogue"].append(e[k, 13] - e[k - 1, 4])
+            cols["first_p_to_pv"].append(e[k, 5] - e[k, 4])
+            cols["first_s_done_to_epilogue_done"].append(e[k, 13] - e[k, 3])
+            cols["first_softmax"].append(e[k, 4] - e[k, 13])
+            cols["s_issue_after_prev"].append(e[k, 2] - e[k - 1, 2])
+            cols["first_rows_wait"].append(max(0, e[k, 1] - e[k, 0]))
+            cols["prev_s_issued_to_q_issued"].append(e[k, 14] - e[k - 1, 2])
+            cols["q_issued_to_q_seen"].append(e[k, 15] - e[k, 14])
+            cols["q_seen_to_s_issued"].append(e[k, 2] - e[k, 15])
+            cols["prev_s_done_to_q_issued"].append(e[k, 14] - e[k - 1, 3])
+            cols["q_seen_to_buffer_free"].append(e[k, 0] - e[k, 15])
+            cols["rows_to_fenced"].append(e[k, 11] - e[k, 1])
+            cols["fenced_to_s_accepted"].append(e[k, 2] - e[k, 11])
+            cols["prev_pv_issued_to_s_accepted"].append(e[k, 2] - e[k - 1, 5])
+            cols["prev_p_to_prev_pv_issued"].append(e[k - 1, 5] - e[k - 1, 4])
+            cols["steady_fenced_to_s_accepted"].append(e[k + 2, 2] - e[k + 2, 11])
+    if not inner or not cols["period_into"]:
+        return {"switches": 0}
+    steady = float(np.median(inner))
+    out = {"switches": len(cols["period_into"]), "steady_period_us": us(steady),
+           "half_tiles_per_cta_median": float(np.median(ctas[:, 14])),
+           "segments_per_cta_median": float(np.median(ctas[:, 23])),
+           "roles_done_per_half_tile_us": float(np.median([us(x) for x in (ctas[:, 7] - c0) / np.maximum(ctas[:, 14], 1)])),
+           "previous_segment_half_tiles_median": float(np.median(seg_len))}
+    for k, v in cols.items():
+        if k == "extra_over_4":
+            out["switch_extra_us"] = float(np.median([us(x - 4 * steady) for x in v]))
+        else:
+            out[k + "_us"] = float(np.median([us(x) for x in v]))
     return out
 
 
@@ -727,7 +799,7 @@ def run_phase_trace(args):
     buf = torch.zeros((1024, slots_per_cta), dtype=torch.int64, device=dev)
     res = {"trace": "phase stamps of one launch (clock64 per SM; medians over CTAs)"}
 
-    def traced(step, label):
+    def traced(step, label, window=False):
         for _ in range(3):
             step()
         torch.cuda.synchronize()
@@ -737,7 +809,9 @@ def run_phase_trace(args):
         step()
         torch.cuda.synchronize()
         L.svt_trace_attach(None, 0)
-        res[label] = analyse_trace(buf.cpu().numpy())
+        res[label] = analyse_trace(buf.cpu().numpy(), window=window)
+        if window:
+            res[label + "_row_set_switch"] = analyse_boundaries(buf.cpu().numpy())
 
     for name, w in (("decode_bf16", W.decode_bf16_batch(args.decode_T)), ("decode_fp8", W.decode_fp8_batch())):
         d = dev_inputs(S, w, dev)
@@ -752,7 +826,7 @@ def run_phase_trace(args):
                                  page_size=pw.page_size, num_pages=pw.num_pages, ws=ws)
     enc, lens = S.build_group_union(slots, pw.G, pw.num_slots, ws=ws)
     traced(lambda: S.sparse_mla_prefill_grouped(d["q"], pw.G, d["kv"], enc, lens, pw.K, pw.scale, ws=ws),
-           "prefill_bf16")
+           "prefill_bf16", window=True)
     # the union-tile kernel: its own slot map, mid-launch tiles
     for _ in range(3):
         S.sparse_mla_prefill_grouped(d["q"], pw.G, d["kv"], enc, lens, pw.K, pw.scale, ws=ws, union_tile=True)

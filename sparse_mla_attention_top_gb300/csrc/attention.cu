@@ -174,22 +174,30 @@ constexpr int kDeadEntry = -2147483647 - 1;  // an entry past the list's live co
 // 0 S^T buffer free, 1 rows landed, 2 S^T issued, 3 S^T done (softmax), 4 P^T written,
 // 5 PV issued, 6 slots ready (filler), 7 fill issued, 8 softmax has S^T in registers, 9 the
 // softmax warps agreed on the maxima, 10 P^T stored (before the proxy fence), 11 the S^T
-// issuer past its fences.
+// issuer past its fences, 12 the half-tile's index within its segment plus one (a value),
+// 13 the softmax warps done with the previous segment's epilogue, 14 the segment's Q^T
+// copies issued (filler), 15 the S^T issuer has the segment's Q^T (the last three on a
+// segment's first half-tile). Header slot 23 counts the segments with live entries the S^T
+// issuer walked. Decode launches stamp their first kTraceG half-tiles, grouped-prefill
+// launches half-tiles kTracePrefillFrom onwards (the middle of a long launch).
 #ifdef SVT_PHASE_TRACE
 __device__ __forceinline__ void trace_at(const AttnParams& p, int slot, unsigned long long v) {
   if (p.trace != nullptr) p.trace[static_cast<long long>(blockIdx.x) * kTraceSlots + slot] = v;
 }
-__device__ __forceinline__ void trace_g(const AttnParams& p, int ev, uint32_t g) {
-  if (p.trace != nullptr && g < static_cast<uint32_t>(kTraceG))
-    p.trace[static_cast<long long>(blockIdx.x) * kTraceSlots + kTraceHead + g * kTraceEv + ev] = clock64();
+__device__ __forceinline__ void trace_g(const AttnParams& p, int ev, uint32_t g, unsigned long long v) {
+  const uint32_t from = p.mode == kModePrefill ? kTracePrefillFrom : 0u;
+  if (p.trace != nullptr && g >= from && g - from < static_cast<uint32_t>(kTraceG))
+    p.trace[static_cast<long long>(blockIdx.x) * kTraceSlots + kTraceHead + (g - from) * kTraceEv + ev] = v;
 }
 #define SVT_TRACE(slot) trace_at(p, (slot), clock64())
 #define SVT_TRACE_VALUE(slot, v) trace_at(p, (slot), (v))
-#define SVT_TRACE_G(ev, g) trace_g(p, (ev), (g))
+#define SVT_TRACE_G(ev, g) trace_g(p, (ev), (g), clock64())
+#define SVT_TRACE_GV(ev, g, v) trace_g(p, (ev), (g), (v))
 #else
 #define SVT_TRACE(slot) ((void)0)
 #define SVT_TRACE_VALUE(slot, v) ((void)0)
 #define SVT_TRACE_G(ev, g) ((void)0)
+#define SVT_TRACE_GV(ev, g, v) ((void)0)
 #endif
 
 __device__ __forceinline__ int halves_of(int len) { return (len + kHalf - 1) / kHalf; }
@@ -636,6 +644,7 @@ __device__ void filler_role(const AttnParams& p, uint8_t* smem, uint32_t bars, c
       mbar_arrive_expect_tx(bar(kBarQFull), kBlocks * kQBlk);
       for (int kb = 0; kb < kBlocks; ++kb)
         tma_load_2d(sbase + kOffQ + kb * kQBlk, &p.q_map, 64 * kb, static_cast<int>(rr.base), bar(kBarQFull));
+      SVT_TRACE_G(14, g);
     }
     ++qk;
     return true;
@@ -758,6 +767,7 @@ __device__ void s_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem,
     // Q^T landed (bf16), or landed and converted to f16 (e4m3 caches)
     if (!mbar_wait<kOOL>(bar(kF16 ? kBarQReady : kBarQFull), qk & 1u, wc)) return;
     if (qk == 0) SVT_TRACE(12);
+    SVT_TRACE_G(15, g);
     ++qk;
     for (int i = 0; i < s.n; ++i, ++g) {
       const uint32_t b = g & 1u;
@@ -780,10 +790,12 @@ __device__ void s_issuer_role(const AttnParams& p, uint8_t* smem, uint32_t tmem,
       }
       umma_commit(bar(kBarSFull + b));
       SVT_TRACE_G(2, g);
+      SVT_TRACE_GV(12, g, i + 1);
       if (i == s.n - 1) umma_commit(bar(kBarQEmpty));
     }
   }
   SVT_TRACE_VALUE(14, g);
+  SVT_TRACE_VALUE(23, qk);
 }
 
 // PV(g) from stage g % 2 and P^T, once the softmax has written P^T(g) (and, for a segment's
@@ -1082,6 +1094,7 @@ __device__ void softmax_role(const AttnParams& p, uint8_t* smem, uint32_t tmem, 
     }
     named_bar_sync(kNamedBarSm, kSmThreads);
     if (threadIdx.x == 0) SVT_TRACE(6);
+    if (threadIdx.x == 0) SVT_TRACE_G(13, g);
   }
 }
 

@@ -79,12 +79,14 @@ struct AttnParams {
   unsigned long long* trace;
 };
 
-// Phase trace layout, per CTA: kTraceHead header slots, then kTraceEv stamps for each of the
-// first kTraceG half-tiles the CTA walks. Stamps are clock64 of the CTA's SM except slots 0
-// and 15, which hold %globaltimer (ns) at the start and the end of the CTA.
+// Phase trace layout, per CTA: kTraceHead header slots, then kTraceEv stamps for each of
+// kTraceG half-tiles the CTA walks (decode launches: its first ones; grouped-prefill launches:
+// kTracePrefillFrom onwards, the middle of a long launch). Stamps are clock64 of the CTA's SM
+// except slots 0 and 15, which hold %globaltimer (ns) at the start and the end of the CTA.
 constexpr int kTraceHead = 48;
 constexpr int kTraceG = 48;
-constexpr int kTraceEv = 12;
+constexpr int kTraceEv = 16;
+constexpr unsigned kTracePrefillFrom = 1000;
 constexpr int kTraceSlots = kTraceHead + kTraceG * kTraceEv;
 
 // Planted fault: the gathering warps withhold the arrival that announces the first KV
