@@ -69,6 +69,9 @@ TRAFFIC_BY_SOURCE = {
     "3b8854cb7d11f6cb": (157.325568e6, 61.010432e6, "256 MB write"),
     # the API source with the union-tile prefill's entry point (the decode kernels unchanged)
     "89f3154b7fd2c791": (157.413888e6, 60.970496e6, "256 MB write"),
+    # the trace build's mid-launch prefill window and row-set switch stamps (the decode kernels'
+    # code unchanged)
+    "66995d98d7f56091": (157.3632e6, 59.189248e6, "256 MB write"),
 }
 
 
