@@ -1,5 +1,6 @@
 """Host-side accounting of bench.py: the kept-entry counts behind the executed-flop figure of
-grouped prefill, against a brute-force count over the union's membership masks."""
+grouped prefill, against a brute-force count over the union's membership masks, and the
+phase-trace analyses on synthetic stamps with known answers."""
 
 import numpy as np
 import pytest
@@ -80,3 +81,42 @@ def test_phase_trace_merge_steps():
     assert list(steps) == ["lse_headers", "o_from_tmem", "pack", "cluster_barrier", "issue_copies", "copies_land",
                            "weights", "weights_barrier", "combine_and_store", "final_barrier"]
     assert all(v == pytest.approx(0.5) for v in steps.values())
+
+
+def test_row_set_switch_analysis_on_a_synthetic_window():
+    # one CTA at 2 GHz; traced half-tiles 0..11 of a mid-launch window: the last six of a
+    # 32-half-tile row-set (index 27..32), then a new row-set (index 1..6). S^T issues every
+    # 4000 cycles except into the new row-set (8000); the new row-set's Q^T is issued 2600
+    # cycles after the last S^T and seen 1800 later; the epilogue ends 5000 cycles after the
+    # old row-set's last P^T.
+    slots = bench.TRACE_HEAD + bench.TRACE_G * bench.TRACE_EV
+    tr = np.zeros((1, slots), np.uint64)
+    c0, gt0 = 100_000, 7_000_000
+    ev = np.zeros((bench.TRACE_G, bench.TRACE_EV), np.int64)
+    issue = c0 + 50_000
+    for k in range(12):
+        if k > 0:
+            issue += 8000 if k == 6 else 4000
+        ev[k, 0], ev[k, 1], ev[k, 11], ev[k, 2] = issue - 3000, issue - 2900, issue - 2800, issue
+        ev[k, 3], ev[k, 4], ev[k, 5] = issue + 300, issue + 1900, issue + 3500
+        ev[k, 12] = 27 + k if k < 6 else k - 5
+    ev[6, 14] = ev[5, 2] + 2600
+    ev[6, 15] = ev[6, 14] + 1800
+    ev[6, 13] = ev[5, 4] + 5000
+    tr[0, 0], tr[0, 1], tr[0, 7], tr[0, 9] = gt0, c0, c0 + 3_000_000, c0 + 3_000_100
+    tr[0, 14], tr[0, 23], tr[0, 15] = 1500, 50, gt0 + 3_000_100 // 2
+    tr[0, bench.TRACE_HEAD:] = ev.reshape(-1).astype(np.uint64)
+    out = bench.analyse_boundaries(tr)
+    assert out["switches"] == 1
+    assert out["steady_period_us"] == pytest.approx(2.0)
+    assert out["period_into_us"] == pytest.approx(4.0)
+    assert out["switch_extra_us"] == pytest.approx(2.0)           # 20000 cycles against 4 x 4000
+    assert out["prev_s_issued_to_q_issued_us"] == pytest.approx(1.3)
+    assert out["q_issued_to_q_seen_us"] == pytest.approx(0.9)
+    assert out["epilogue_us"] == pytest.approx(2.5)
+    assert out["previous_segment_half_tiles_median"] == 32
+    assert out["segments_per_cta_median"] == 50
+    assert out["roles_done_per_half_tile_us"] == pytest.approx(1.0)  # 3e6 cycles / 1500 at 2 GHz
+    # the window analysis of the same stamps reports the mid-launch period and no first-tile times
+    w = bench.analyse_trace(tr, window=True)
+    assert w["half_tile_period_us"] == pytest.approx(2.0) and "first_s_issued_us" not in w
