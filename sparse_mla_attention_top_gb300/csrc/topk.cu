@@ -7,10 +7,12 @@
 //
 // One CTA per query. Scores become order-preserving 32-bit keys (NaN -> 0, the lowest),
 // kept in shared memory when the row fits. A most-significant-digit-first radix select
-// (four 8-bit digits, per-warp shared histograms) finds the K-th largest key exactly and
-// how many keys equal to it are kept; the kept positions are then compacted in position
-// order (warp-contiguous ranges, ballots, one scan over the warps), so the output is
-// ascending by construction.
+// (up to four 8-bit digits, per-warp shared histograms) finds the K-th largest key exactly
+// and how many keys equal to it are kept; it stops early once every key still matching the
+// chosen digits has the same lower bits (each pass ORs and ANDs them), as with scores of
+// low precision (a bf16 score's key ends in 16 zero bits). The kept positions are then
+// compacted in position order (warp-contiguous ranges, ballots, one scan over the warps), so
+// the output is ascending by construction.
 #include <cooperative_groups.h>
 
 #include <cstdint>
@@ -36,6 +38,8 @@ __device__ __forceinline__ uint32_t score_key(float x) {
 
 struct TopkShared {
   uint32_t hist[2][256];  // per pass, alternating (a cluster peer reads the previous one)
+  uint32_t low_or[2], low_and[2];  // per pass: OR / AND of the lower bits of the matching keys
+  uint32_t low_same, low_val;      // they agree over the cluster (and their value)
   uint32_t cnt[2 * kTopkWarps];  // per-warp counts of keys > thr, then their exclusive prefix
   uint32_t off[2 * kTopkWarps];  // the same for keys == thr
   uint32_t digit, above;
@@ -99,14 +103,32 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   uint32_t rank = static_cast<uint32_t>(K);  // 1-based rank still to find among the matching keys
   uint32_t* my_hist = warp_hist + warp * 256;
   int buf = 0;
+  bool done = false;
 #pragma unroll 1
-  for (int shift = 24; shift >= 0; shift -= 8, buf ^= 1) {
+  for (int shift = 24; shift >= 0 && !done; shift -= 8, buf ^= 1) {
     for (int b = lane; b < 256; b += 32) my_hist[b] = 0;
+    if (tid == 0) {
+      sh.low_or[buf] = 0u;
+      sh.low_and[buf] = 0xFFFFFFFFu;
+    }
     __syncthreads();
-    // one histogram per warp, so warps never contend with each other
+    // one histogram per warp, so warps never contend with each other; the bits below this
+    // digit of the matching keys are ORed and ANDed on the way
+    const uint32_t low_mask = (1u << shift) - 1u;
+    uint32_t lor = 0u, land = 0xFFFFFFFFu;
     for (int j = tid; j < n; j += kTopkThreads) {
       const uint32_t k = key_at(j);
-      if ((k & prefix_mask) == prefix) atomicAdd(&my_hist[(k >> shift) & 255u], 1u);
+      if ((k & prefix_mask) == prefix) {
+        atomicAdd(&my_hist[(k >> shift) & 255u], 1u);
+        lor |= k;
+        land &= k;
+      }
+    }
+    lor = __reduce_or_sync(0xffffffffu, lor & low_mask);
+    land = __reduce_and_sync(0xffffffffu, land | ~low_mask);
+    if (lane == 0) {
+      atomicOr(&sh.low_or[buf], lor);
+      atomicAnd(&sh.low_and[buf], land);
     }
     __syncthreads();
     if (tid < 256) {
@@ -155,10 +177,31 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
         }
       }
     }
+    if (tid == 0) {
+      // the lower bits of the matching keys, over the cluster: when they agree, every key
+      // that matches the digits chosen so far is the threshold itself and the select is done
+      uint32_t all_or = sh.low_or[buf], all_and = sh.low_and[buf];
+      if constexpr (kSplit > 1) {
+        auto cl = cooperative_groups::this_cluster();
+#pragma unroll
+        for (int q = 1; q < kSplit; ++q) {
+          const unsigned peer = static_cast<unsigned>((cr + q) % kSplit);
+          all_or |= *cl.map_shared_rank(&sh.low_or[buf], peer);
+          all_and &= *cl.map_shared_rank(&sh.low_and[buf], peer);
+        }
+      }
+      sh.low_same = (all_or & low_mask) == (all_and & low_mask) ? 1u : 0u;
+      sh.low_val = all_and & low_mask;
+    }
     __syncthreads();
     prefix |= sh.digit << shift;
     prefix_mask |= 255u << shift;
     rank -= sh.above;
+    if (sh.low_same) {
+      prefix |= sh.low_val;
+      prefix_mask = 0xFFFFFFFFu;
+      done = true;
+    }
   }
   const uint32_t thr = prefix;
   const uint32_t need = rank;  // keys equal to thr to keep, lowest positions first
