@@ -10,8 +10,9 @@
 // (up to four 8-bit digits, per-warp shared histograms) finds the K-th largest key exactly
 // and how many keys equal to it are kept; it stops early once every key still matching the
 // chosen digits has the same lower bits (each pass ORs and ANDs them), as with scores of
-// low precision (a bf16 score's key ends in 16 zero bits). The kept positions are then
-// compacted in position order (warp-contiguous ranges, ballots, one scan over the warps), so
+// low precision (a bf16 score's key ends in 16 zero bits). The first pass's histogram is
+// taken as the keys arrive. The kept positions are then compacted in position order
+// (warp-contiguous ranges, ballots kept from the counting sweep, one scan over the warps), so
 // the output is ascending by construction.
 #include <cooperative_groups.h>
 
@@ -43,7 +44,7 @@ struct TopkShared {
   uint32_t cnt[2 * kTopkWarps];  // per-warp counts of keys > thr, then their exclusive prefix
   uint32_t off[2 * kTopkWarps];  // the same for keys == thr
   uint32_t digit, above;
-  uint32_t tot_gt, tot_eq;  // this CTA's kept-key counts (read by the next CTA of a cluster)
+  uint32_t tot_gt[2], tot_eq[2];  // kept-key counts of each CTA of the cluster (pushed by each to the later ones)
 };
 
 // keys + per-warp histograms (dynamic) + the block's scalars (static) within 227 KB
@@ -57,6 +58,7 @@ template <int kSplit>
 __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restrict__ scores, int N, long long stride,
                                                              const int32_t* __restrict__ lens, int K,
                                                              int32_t* __restrict__ out) {
+  static_assert(kSplit == 1 || kSplit == 2, "the kept-key totals hold two CTAs");
   extern __shared__ uint32_t dyn_smem[];
   uint32_t* warp_hist = dyn_smem;                   // [32 warps][256 bins]
   uint32_t* keys_smem = dyn_smem + kTopkWarps * 256;  // this CTA's keys, when they fit
@@ -78,7 +80,17 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   const int lo = min(len, cr * half), hi = min(len, lo + half);
   const int n = hi - lo;  // this CTA's positions lo .. hi - 1
   const bool in_smem = n <= kKeysInSmemMax;
+  uint32_t* my_hist = warp_hist + warp * 256;
+  // the first pass's histogram (and the OR / AND of the bits below its digit) is taken as
+  // the keys arrive when they are kept in shared memory
+  uint32_t lor = 0u, land = 0xFFFFFFFFu;
   if (in_smem) {
+    for (int b = lane; b < 256; b += 32) my_hist[b] = 0;
+    if (tid == 0) {
+      sh.low_or[0] = 0u;
+      sh.low_and[0] = 0xFFFFFFFFu;
+    }
+    __syncthreads();
     // eight loads in flight per thread, then their keys
 #pragma unroll 1
     for (int j0 = 0; j0 < n; j0 += 8 * kTopkThreads) {
@@ -91,7 +103,13 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int j = j0 + u * kTopkThreads + tid;
-        if (j < n) keys_smem[j] = score_key(v[u]);
+        if (j < n) {
+          const uint32_t k = score_key(v[u]);
+          keys_smem[j] = k;
+          atomicAdd(&my_hist[k >> 24], 1u);
+          lor |= k;
+          land &= k;
+        }
       }
     }
   }
@@ -101,27 +119,29 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   // are kept (the ones at the lowest positions)
   uint32_t prefix = 0, prefix_mask = 0;
   uint32_t rank = static_cast<uint32_t>(K);  // 1-based rank still to find among the matching keys
-  uint32_t* my_hist = warp_hist + warp * 256;
   int buf = 0;
   bool done = false;
 #pragma unroll 1
   for (int shift = 24; shift >= 0 && !done; shift -= 8, buf ^= 1) {
-    for (int b = lane; b < 256; b += 32) my_hist[b] = 0;
-    if (tid == 0) {
-      sh.low_or[buf] = 0u;
-      sh.low_and[buf] = 0xFFFFFFFFu;
-    }
-    __syncthreads();
-    // one histogram per warp, so warps never contend with each other; the bits below this
-    // digit of the matching keys are ORed and ANDed on the way
     const uint32_t low_mask = (1u << shift) - 1u;
-    uint32_t lor = 0u, land = 0xFFFFFFFFu;
-    for (int j = tid; j < n; j += kTopkThreads) {
-      const uint32_t k = key_at(j);
-      if ((k & prefix_mask) == prefix) {
-        atomicAdd(&my_hist[(k >> shift) & 255u], 1u);
-        lor |= k;
-        land &= k;
+    if (shift != 24 || !in_smem) {
+      for (int b = lane; b < 256; b += 32) my_hist[b] = 0;
+      if (tid == 0) {
+        sh.low_or[buf] = 0u;
+        sh.low_and[buf] = 0xFFFFFFFFu;
+      }
+      __syncthreads();
+      // one histogram per warp, so warps never contend with each other; the bits below this
+      // digit of the matching keys are ORed and ANDed on the way
+      lor = 0u;
+      land = 0xFFFFFFFFu;
+      for (int j = tid; j < n; j += kTopkThreads) {
+        const uint32_t k = key_at(j);
+        if ((k & prefix_mask) == prefix) {
+          atomicAdd(&my_hist[(k >> shift) & 255u], 1u);
+          lor |= k;
+          land &= k;
+        }
       }
     }
     lor = __reduce_or_sync(0xffffffffu, lor & low_mask);
@@ -215,12 +235,22 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
   const int w0 = warp * seg;
   const int w1 = min(n, w0 + seg);
   const uint32_t lt_mask = (1u << lane) - 1u;
+  // the counting sweep keeps each 32-key chunk's two ballots (in the histograms' space, free
+  // now) for the writing sweep, when the warp has at most 64 chunks
+  uint32_t* ballots = warp_hist + warp * 128;
+  const bool keep_ballots = seg <= 64 * 32;
   uint32_t n_gt = 0, n_eq = 0;
-  for (int j0 = w0; j0 < w1; j0 += 32) {
+  for (int j0 = w0, c = 0; j0 < w1; j0 += 32, ++c) {
     const int j = j0 + lane;
     const uint32_t k = j < w1 ? key_at(j) : 0u;
-    n_gt += __popc(__ballot_sync(0xffffffffu, j < w1 && k > thr));
-    n_eq += __popc(__ballot_sync(0xffffffffu, j < w1 && k == thr));
+    const uint32_t b_gt = __ballot_sync(0xffffffffu, j < w1 && k > thr);
+    const uint32_t b_eq = __ballot_sync(0xffffffffu, j < w1 && k == thr);
+    if (keep_ballots && lane == 0) {
+      ballots[2 * c] = b_gt;
+      ballots[2 * c + 1] = b_eq;
+    }
+    n_gt += __popc(b_gt);
+    n_eq += __popc(b_eq);
   }
   if (lane == 0) {
     sh.cnt[warp] = n_gt;
@@ -240,30 +270,41 @@ __global__ void __launch_bounds__(kTopkThreads) topk_kernel(const float* __restr
     }
     sh.cnt[32 + lane] = gi - g;  // exclusive prefixes
     sh.off[32 + lane] = ei - e;
-    if (lane == 31) {
-      sh.tot_gt = gi;
-      sh.tot_eq = ei;
+    if constexpr (kSplit > 1) {
+      // this CTA's totals go into every later CTA of the cluster (it reads them locally after
+      // the cluster barrier, so no CTA touches another's shared memory after it)
+      if (lane == 31) {
+        auto cl = cooperative_groups::this_cluster();
+        for (int q = cr + 1; q < kSplit; ++q) {
+          TopkShared* peer = cl.map_shared_rank(&sh, static_cast<unsigned>(q));
+          peer->tot_gt[cr] = gi;
+          peer->tot_eq[cr] = ei;
+        }
+      }
     }
   }
   uint32_t base_gt = 0, base_eq = 0;
   if constexpr (kSplit > 1) {
-    auto cl = cooperative_groups::this_cluster();
-    cl.sync();  // every CTA's totals are written
+    cooperative_groups::this_cluster().sync();  // every earlier CTA's totals have landed here
     for (int q = 0; q < cr; ++q) {
-      const TopkShared* peer = cl.map_shared_rank(&sh, static_cast<unsigned>(q));
-      base_gt += peer->tot_gt;
-      base_eq += peer->tot_eq;
+      base_gt += sh.tot_gt[q];
+      base_eq += sh.tot_eq[q];
     }
-    cl.sync();  // the totals are read: no CTA touches another's shared memory after this
   } else {
     __syncthreads();
   }
   uint32_t gt_before = base_gt + sh.cnt[32 + warp], eq_before = base_eq + sh.off[32 + warp];
-  for (int j0 = w0; j0 < w1; j0 += 32) {
+  for (int j0 = w0, c = 0; j0 < w1; j0 += 32, ++c) {
     const int j = j0 + lane;
-    const uint32_t k = j < w1 ? key_at(j) : 0u;
-    const uint32_t b_gt = __ballot_sync(0xffffffffu, j < w1 && k > thr);
-    const uint32_t b_eq = __ballot_sync(0xffffffffu, j < w1 && k == thr);
+    uint32_t b_gt, b_eq;
+    if (keep_ballots) {
+      b_gt = ballots[2 * c];
+      b_eq = ballots[2 * c + 1];
+    } else {
+      const uint32_t k = j < w1 ? key_at(j) : 0u;
+      b_gt = __ballot_sync(0xffffffffu, j < w1 && k > thr);
+      b_eq = __ballot_sync(0xffffffffu, j < w1 && k == thr);
+    }
     const uint32_t g = gt_before + __popc(b_gt & lt_mask);
     const uint32_t e = eq_before + __popc(b_eq & lt_mask);
     const bool kept = ((b_gt >> lane) & 1u) || (((b_eq >> lane) & 1u) && e < need);
