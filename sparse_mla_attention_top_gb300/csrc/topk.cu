@@ -44,7 +44,8 @@ struct TopkShared {
   uint32_t cnt[2 * kTopkWarps];  // per-warp counts of keys > thr, then their exclusive prefix
   uint32_t off[2 * kTopkWarps];  // the same for keys == thr
   uint32_t digit, above;
-  uint32_t tot_gt[2], tot_eq[2];  // kept-key counts of each CTA of the cluster (pushed by each to the later ones)
+  // kept-key counts of each CTA of the cluster, pushed by each CTA to the later ones
+  uint32_t tot_gt[2], tot_eq[2];
 };
 
 // keys + per-warp histograms (dynamic) + the block's scalars (static) within 227 KB
